@@ -1,0 +1,568 @@
+"""Benchmark of the batched speculative-decoding verify step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2]
+    python bench.py --impl reference ...     # the oracle on the host cores
+
+A step is one verify call over one batch of the workload (all of its rows).
+The timed region runs exactly K steps between a barrier and a device
+synchronisation, timed with CUDA events on the launching stream; inputs
+rotate over enough seeded sets that their total exceeds twice the L2 cache,
+so every step reads its logits from HBM. The printed JSON line reports
+rows/s (the headline), the achieved HBM bandwidth of the verify kernel
+against the measured copy peak, an end-to-end number through the public API
+with host buffers, and the oracle timed on the host cores.
+
+With N > 1 (torchrun), each rank runs its own batches on its own GPU (the
+sequences of a batch are independent, so the work shards with no
+collective); value is the rows of all ranks divided by the slowest rank's
+time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_24_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, only while the
+    kernel sources still hash to the value recorded with the counters."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        entry = d[workload]
+        if entry.get("source_hash") != kernel_source_hash():
+            return None, "stale (kernel changed since the ncu capture)"
+        return float(entry["dram_bytes_per_launch"]), entry.get("note", "")
+    except Exception:
+        return None, "no ncu capture recorded"
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+        self.t_marks = []
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def mark(self):
+        self.t_marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[1].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[5:10]))
+                except Exception:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        t0, t1 = (self.t_marks[0], self.t_marks[-1]) if len(self.t_marks) >= 2 else (0, 1e18)
+        inside = [r for r in rows if t0 - 1 <= r[0] <= t1 + 1]
+        note = "samples within the timed region (1 s timestamp resolution)"
+        if not inside:
+            inside = rows
+            note = "timed region shorter than the sampling interval: samples around it under the same load"
+        reasons = set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for r in inside:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.strip().lower() in ("active", "1"):
+                    reasons.add(n)
+        sm = sorted(r[1] for r in inside)
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+# ----------------------------------------------------------------- workloads
+
+
+def workload_sets(name: str, device, l2_bytes: int):
+    """Seeded input sets for a workload, enough that they exceed 2 x L2."""
+    import synth
+    from synth.workloads import WORKLOADS
+
+    w = WORKLOADS[name]
+    esize = 4 if w["dtype"] == "f32" else 2
+    B, K, V = w["B"], w["K"], w["V"]
+    set_bytes = B * (2 * K + 1) * V * esize
+    n_sets = max(2, math.ceil(2 * l2_bytes / set_bytes))
+    taus = list(w["tau"]) if name == "c2" else [None]
+    if name == "c2":
+        n_sets = int(math.ceil(n_sets / len(taus)) * len(taus))
+    sets = []
+    for k in range(n_sets):
+        tau = taus[k % len(taus)]
+        sets.append(synth.make_workload(name, seed={"c1": 0, "c2": 2, "c3": 3, "c4": 4}[name] + k,
+                                        device=device, tau=tau))
+    return sets, set_bytes
+
+
+def describe(name: str) -> str:
+    return {
+        "c1": "B=1 K=4 V=1000 fp32, N(0,3^2)+Zipf(1.1) target, draft=target+N(0,1), T=1",
+        "c2": "B=8 K=5 V=32000 fp32 sample T=1, N(0,3^2)+Zipf(1.1) target, "
+              "draft=target+N(0,tau^2), tau cycling over {0.3,1.0,3.0}",
+        "c3": "B=64 K=4 V=128256 bf16, T=0.8, seqs 0-31 greedy 32-63 sample, "
+              "N(0,4^2)+Zipf(1.05) target, draft=0.8*target+N(0,1.5^2)",
+        "c4": "B=256 K=8 V=151936 bf16 sample T=1, N(0,4^2)+Zipf(1.1) target, "
+              "draft=target+N(0,tau_b^2), tau_b~U[0.2,3.0] per sequence",
+    }[name]
+
+
+def alg_bytes(case, n_accepted: np.ndarray) -> int:
+    """Bytes the verify step must read: every target row, the draft rows of
+    sample-mode sequences, plus the second pass actually taken (target and
+    draft row j after a rejection, target row K for a bonus)."""
+    B, K1, V = case.target.shape
+    K = K1 - 1
+    s = case.target.element_size()
+    modes = case.modes.cpu().numpy()
+    n_sample = int((modes == 1).sum())
+    total = B * K1 * V * s + n_sample * K * V * s
+    samp = (modes == 1) & (n_accepted >= 0)
+    total += int(((n_accepted < K) & samp).sum()) * 2 * V * s
+    total += int(((n_accepted == K) & samp).sum()) * V * s
+    return total
+
+
+def min_bytes(case) -> int:
+    B, K1, V = case.target.shape
+    s = case.target.element_size()
+    n_sample = int((case.modes.cpu().numpy() == 1).sum())
+    return B * K1 * V * s + n_sample * (K1 - 1) * V * s
+
+
+# ----------------------------------------------------------------- our arm
+
+
+def time_device(sets, steps, warmup, stream, seed0=0):
+    from speculative_decoding_verification_24_gb300 import spec_verify_ex
+
+    B, K1, _ = sets[0].target.shape
+    dev = sets[0].target.device
+    out_tok = torch.empty(steps + warmup, B, K1, dtype=torch.int32, device=dev)
+    out_n = torch.empty(steps + warmup, B, dtype=torch.int32, device=dev)
+
+    def step(i):
+        c = sets[i % len(sets)]
+        spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=c.modes, seed=seed0 + i,
+                       out_tokens=out_tok[i], out_n_accepted=out_n[i], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    return step, out_n
+
+
+def capture(step, first, count, stream):
+    """A CUDA graph of steps first..first+count-1 (one verify launch each)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(first, first + count):
+            step(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def replay_ms(graph, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        graph.replay()
+        stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop)
+
+
+def run_ours(args, rank, world, device):
+    from speculative_decoding_verification_24_gb300 import spec_verify_ex
+    from speculative_decoding_verification_24_gb300.build import build
+
+    build()
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+    sets, set_bytes = workload_sets(args.workload, device, l2)
+    case0 = sets[0]
+    B, K1, V = case0.target.shape
+    rows_per_step = B * K1
+    stream = torch.cuda.Stream(device)
+    step, out_n = time_device(sets, args.steps, args.warmup, stream, seed0=1000 * rank)
+
+    # The timed steps replay from one CUDA graph (launch overhead of the
+    # Python binding off the device timeline); the eager number is reported too.
+    graph = capture(step, args.warmup, args.steps, stream)
+    replay_ms(graph, stream)  # warm replay: same launches, same inputs
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    # keep the GPU busy briefly so the sampler sees clocks under this load
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        replay_ms(graph, stream)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark()
+    ms = replay_ms(graph, stream)
+    sampler.mark()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.25)
+    clocks = sampler.stop()
+
+    # eager launches from Python, for comparison (not the headline)
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e_start.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup, args.warmup + args.steps):
+            step(i)
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = e_start.elapsed_time(e_stop)
+
+    # exact algorithmic bytes of every timed step, from its own outputs
+    n_all = out_n.cpu().numpy()
+    bytes_alg = sum(alg_bytes(sets[i % len(sets)], n_all[i])
+                    for i in range(args.warmup, args.warmup + args.steps))
+    bytes_min = sum(min_bytes(sets[i % len(sets)])
+                    for i in range(args.warmup, args.warmup + args.steps))
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = world * rows_per_step * args.steps / (ms_max / 1e3)
+    gbs = bytes_alg / (ms / 1e3) / 1e9
+    peak, peak_src = measured_peaks()
+    traffic, traffic_note = profiled_traffic(args.workload)
+
+    result = {
+        "metric": "verify rows/s",
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32" if case0.target.dtype == torch.float32 else "bf16 in, f32 arithmetic",
+        "data": "synthetic (seeded generators in synth/; no dataset or weights)",
+        "config": {
+            "workload": f"{args.workload}: {describe(args.workload)}",
+            "B": B, "K": K1 - 1, "V": V, "rows_per_step": rows_per_step,
+            "l2": f"inputs rotate over {len(sets)} seeded sets "
+                  f"({len(sets) * set_bytes / 2**20:.0f} MiB > 2 x L2 of {l2 / 2**20:.0f} MiB)",
+            "parallelism": f"replicas x{world} (sequences shard with no collective)",
+        },
+        "hbm_gbs": gbs,
+        "hbm_bytes_per_step": bytes_alg / args.steps,
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "sv::verify_logits_kernel",
+            "achieved": gbs,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": gbs / peak,
+            "peak_source": peak_src,
+            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+            "traffic": None if traffic is None else traffic,
+            "traffic_note": traffic_note,
+            "algorithmic_bytes_per_launch": bytes_alg / args.steps,
+            "min_bytes_per_launch": bytes_min / args.steps,
+            "timing": "CUDA events on the launching stream over the timed region / steps",
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "timing": "one CUDA graph of the K steps, replayed between CUDA events on the "
+                  "launching stream",
+        "eager_rows_per_s": world * rows_per_step * args.steps / (eager_ms / 1e3),
+    }
+    result["e2e"] = run_e2e(args, sets, device, stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(sets, args.cpu_seconds)
+    if rank == 0 and not args.no_extra and world == 1:
+        result["other_workloads"] = other_workloads(args, device, l2, stream)
+    return result
+
+
+def run_e2e(args, sets, device, stream, world):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory, verifies, and reads the results back."""
+    from speculative_decoding_verification_24_gb300 import spec_verify_ex
+    import synth
+
+    n_host = min(len(sets), 4)
+    host = []
+    for c in sets[:n_host]:
+        host.append(tuple(t.cpu().pin_memory() for t in (c.target, c.draft, c.tokens, c.modes)))
+    c0 = sets[0]
+    dev_t = torch.empty_like(c0.target)
+    dev_d = torch.empty_like(c0.draft)
+    dev_x = torch.empty_like(c0.tokens)
+    dev_m = torch.empty_like(c0.modes)
+    B, K1, _ = c0.target.shape
+    out_t = torch.empty(B, K1, dtype=torch.int32, device=device)
+    out_n = torch.empty(B, dtype=torch.int32, device=device)
+    res_t = torch.empty(B, K1, dtype=torch.int32).pin_memory()
+    res_n = torch.empty(B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0])
+    d2h = res_t.numel() * 4 + res_n.numel() * 4
+
+    def step(i):
+        ht, hd, hx, hm = host[i % n_host]
+        dev_t.copy_(ht, non_blocking=True)
+        dev_d.copy_(hd, non_blocking=True)
+        dev_x.copy_(hx, non_blocking=True)
+        dev_m.copy_(hm, non_blocking=True)
+        spec_verify_ex(dev_t, dev_d, dev_x, c0.temperature, modes=dev_m, seed=i,
+                       out_tokens=out_t, out_n_accepted=out_n, stream=stream)
+        res_t.copy_(out_t, non_blocking=True)
+        res_n.copy_(out_n, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            step(i)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(stop)
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    value = world * B * K1 * args.steps / (float(t.item()) / 1e3)
+    return {"value": value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "how": "pinned host inputs copied to the device, spec_verify_ex, results copied "
+                   "back, every step, on one stream; CUDA events around all steps"}
+
+
+def cpu_baseline(sets, seconds):
+    """The oracle as it stands on the host cores, over a bounded sample."""
+    from oracle import oracle as orc
+    from synth.workloads import to_numpy_logits
+
+    cores = os.cpu_count() or 1
+    rows = 0
+    used = 1
+    t0 = time.perf_counter()
+    calls = 0
+    for k, c in enumerate(sets):
+        B, K1, _ = c.target.shape
+        threads = min(cores, B)
+        used = max(used, threads)
+        tgt, drf = to_numpy_logits(c.target), to_numpy_logits(c.draft)
+        tok, modes = c.tokens.cpu().numpy(), c.modes.cpu().numpy()
+        t1 = time.perf_counter()
+        orc.verify(tgt, drf, tok, c.temperature, modes, seed=k, threads=threads)
+        rows += B * K1
+        calls += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": rows / el, "unit": "rows/s", "cores": used, "kind": "oracle",
+            "sample": f"{calls} verify calls of the workload's batches ({rows} rows), "
+                      f"{el:.1f} s of oracle time, threads over sequences"}
+
+
+def other_workloads(args, device, l2, stream):
+    """The other logits workloads measured the same way (sub-results)."""
+    out = {}
+    for name in args.also:
+        if name == args.workload:
+            continue
+        try:
+            sets, set_bytes = workload_sets(name, device, l2)
+            steps = max(20, min(args.steps, 200))
+            step, out_n = time_device(sets, steps, args.warmup, stream)
+            graph = capture(step, args.warmup, steps, stream)
+            replay_ms(graph, stream)
+            ms = replay_ms(graph, stream)
+            n_all = out_n.cpu().numpy()
+            ba = sum(alg_bytes(sets[i % len(sets)], n_all[i])
+                     for i in range(args.warmup, args.warmup + steps))
+            B, K1, V = sets[0].target.shape
+            gbs = ba / (ms / 1e3) / 1e9
+            peak, _ = measured_peaks()
+            out[name] = {"workload": describe(name), "steps": steps,
+                         "rows_per_s": B * K1 * steps / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
+                         "hbm_gbs": gbs, "frac_of_measured_peak": gbs / peak,
+                         "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                         "input_sets": len(sets)}
+            del sets
+            torch.cuda.empty_cache()
+        except Exception as e:  # report, do not hide
+            out[name] = {"error": repr(e)}
+    return out
+
+
+# ----------------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores on this workload."""
+    import synth
+    from oracle import oracle as orc
+    from synth.workloads import to_numpy_logits
+
+    orc.build()
+    c = synth.make_workload(args.workload, seed=2, device="cpu", tau=1.0 if args.workload == "c2" else None)
+    tgt, drf = to_numpy_logits(c.target), to_numpy_logits(c.draft)
+    tok, modes = c.tokens.numpy(), c.modes.numpy()
+    B, K1, V = c.target.shape
+    cores = os.cpu_count() or 1
+    threads = min(cores, B)
+    # each step verifies a bounded sample of the batch so the run stays short
+    budget_s = 0.2
+    t0 = time.perf_counter()
+    orc.verify(tgt, drf, tok, c.temperature, modes, seed=0, threads=threads)
+    one = time.perf_counter() - t0
+    n_seq = B if one <= budget_s else max(1, int(B * budget_s / one))
+    rng = (0, n_seq)
+    for i in range(args.warmup):
+        orc.verify(tgt, drf, tok, c.temperature, modes, seed=i, threads=threads, seq_range=rng)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        orc.verify(tgt, drf, tok, c.temperature, modes, seed=i, threads=min(threads, n_seq),
+                   seq_range=rng)
+    el = time.perf_counter() - t0
+    value = n_seq * K1 * args.steps / el
+    sample = f"{n_seq} of {B} sequences per step ({n_seq * K1} rows), {args.steps} steps"
+    return {
+        "impl": "reference", "metric": "verify rows/s", "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators in synth/)",
+        "config": {"workload": f"{args.workload}: {describe(args.workload)}", "B": B,
+                   "K": K1 - 1, "V": V},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": min(threads, n_seq),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "note": "the reference arm is the plain C double-precision oracle (the pages print no "
+                "implementation of the verify step to install)",
+    }
+
+
+# ----------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--also", default="c3,c4", help="other workloads reported as sub-results")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.also = [a for a in args.also.split(",") if a]
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    result = run_ours(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

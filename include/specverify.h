@@ -1,0 +1,189 @@
+/*
+ * specverify.h - C ABI of libspecverify, the batched verify step of
+ * speculative decoding on one GPU (sm_103a).
+ *
+ * The verify step takes, for each of B sequences, the target model's
+ * distribution at the K draft positions plus one more after the last draft
+ * (K+1 rows of V logits), the draft model's K rows and the K draft tokens,
+ * checks the drafts left to right, and commits the accepted drafts followed
+ * by one target token (a correction at the first rejection, or a bonus token
+ * when every draft is accepted). Sources:
+ *   "Inference-4" (brunomaga.github.io), section "Draft-model speculative
+ *     decoding": the K+1 rows, the greedy rule (accept while the draft equals
+ *     the target's most likely token; correction or bonus from the target),
+ *     the sampling rule (accept x with probability min(1, P_t(x)/P_d(x)); on
+ *     rejection draw from the normalised residual max(0, P_t - P_d)), and the
+ *     note that sequences of a batch accept different numbers of tokens.
+ *   "Speculative decoding" (leoniemonigatti.com blog), section "Rejection
+ *     sampling": the same rule and the bonus token when all drafts pass.
+ *   "Speculative decoding" (denimpatel.github.io interactive course), section
+ *     "Memory-bound, not compute-bound": verification is a forward pass whose
+ *     query dimension is K (+1), the target's LM head included, which the
+ *     fused entry point spec_verify_lmhead covers.
+ *
+ * Conventions shared by every entry point:
+ *   - All array arguments are DEVICE pointers to caller-owned memory on the
+ *     current CUDA device; the library allocates nothing and frees nothing.
+ *   - Layouts are dense row-major: logits [B, K+1, V] and [B, K, V] with V
+ *     innermost; each row must start on a multiple of its element size.
+ *   - Calls are asynchronous and stream-ordered on `stream` (NULL = the
+ *     legacy default stream); no call synchronises the host. Buffers must
+ *     stay valid until the work on `stream` completes.
+ *   - Host-detectable errors return a status before anything is launched and
+ *     leave the outputs untouched. A failed launch returns SV_ERR_CUDA.
+ *   - Device-detectable errors never trap: a sequence whose draft token is
+ *     outside [0, V), or whose rows contain no finite maximum (all -inf, or a
+ *     NaN or +inf), gets n_accepted = -1 and every token -1, and the bits of
+ *     sv_device_flag are OR-ed into the optional status word.
+ *   - Temperature: both distributions are softmax(logits / T). Greedy mode
+ *     ignores T. -inf logits are allowed and mean probability zero.
+ *   - Random numbers: Philox4x32-10 (Salmon et al., SC'11) with counter
+ *     (pos, seq_lo, seq_hi, 0) and key (seed_lo, seed_hi); word 0 gives the
+ *     accept uniform u of draft position pos, word 1 the uniform u2 of the
+ *     residual or bonus draw at that position; each is (w >> 8) * 2^-24. A
+ *     draft x at position i is accepted iff u * P_d(x) < P_t(x).
+ *   - The draw is the inverse CDF in index order: the smallest token k whose
+ *     cumulative mass exceeds u2 times the total mass.
+ *   - The thread-safety of a call is that of its stream: concurrent calls on
+ *     different streams with disjoint outputs are safe.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* sv_stream_t;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+typedef enum { SV_GREEDY = 0, SV_SAMPLE = 1 } sv_mode;
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_NULL = 1,          /* a required pointer is NULL                     */
+    SV_ERR_SHAPE = 2,         /* B < 1, K outside [1, 31], V < 2, d bad, ...    */
+    SV_ERR_DTYPE = 3,         /* unknown dtype                                  */
+    SV_ERR_TEMPERATURE = 4,   /* sample mode with T not finite or T <= 0        */
+    SV_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than required        */
+    SV_ERR_ARCH = 6,          /* the current device is not compute capability 10.3 */
+    SV_ERR_CUDA = 7,          /* a CUDA runtime call or launch failed           */
+    SV_ERR_MODE = 8,          /* unknown mode                                   */
+    SV_ERR_ALIGN = 9,         /* a pointer is not aligned to its element size   */
+    SV_ERR_CONFIG = 10,       /* a requested launch parameter cannot be used    */
+    SV_ERR_NOT_IMPLEMENTED = 11
+} sv_status;
+
+/* Bits OR-ed into the optional device status word. */
+typedef enum {
+    SV_FLAG_BAD_TOKEN = 1u,        /* a draft token outside [0, V)                 */
+    SV_FLAG_BAD_ROW = 2u,          /* a row with no finite maximum                 */
+    SV_FLAG_RESIDUAL_FALLBACK = 4u,/* a residual summed to 0 in float; P_t used    */
+    SV_FLAG_DRAW_EDGE = 8u,        /* a draw landed past the summed mass (rounding)*/
+    SV_FLAG_BAD_MODE = 16u,        /* a per-sequence mode that is neither greedy nor
+                                      sample, or sample mode without draft logits  */
+    SV_FLAG_TIMEOUT = 32u          /* a bounded wait inside the kernel gave up; the
+                                      sequence is reported invalid                 */
+} sv_device_flag;
+
+/* Batched verify over logits already in device memory.
+ *   target_logits  [B, K+1, V] of `dtype` (device): the target's rows at the K
+ *                  draft positions and after the last draft.
+ *   draft_logits   [B, K, V] of `dtype` (device): the draft's rows; may be
+ *                  NULL in greedy mode (never read there).
+ *   draft_tokens   [B, K] int32 (device): the drafts x_0..x_{K-1}.
+ *   B >= 1, 1 <= K <= 31, V >= 2; dtype SV_F32 or SV_BF16.
+ *   temperature    T of both softmaxes in sample mode (finite, > 0).
+ *   mode           SV_GREEDY or SV_SAMPLE for the whole batch.
+ *   seed           Philox key; the sequence id of row b is b.
+ *   out_tokens     [B, K+1] int32 (device): x_0..x_{j-1}, then the correction
+ *                  or bonus token, then -1 padding.
+ *   out_n_accepted [B] int32 (device): j, the number of accepted drafts
+ *                  (0..K), or -1 for an invalid sequence.
+ * Returns SV_OK once the work is enqueued. */
+sv_status spec_verify(const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, int B, int K, int V,
+                      sv_dtype dtype, float temperature, sv_mode mode,
+                      uint64_t seed, int32_t* out_tokens,
+                      int32_t* out_n_accepted, sv_stream_t stream);
+
+/* Arguments of spec_verify_ex. Zero-initialise, then fill what is used. */
+typedef struct {
+    const void* target_logits;   /* [B, K+1, V] dtype (device)                    */
+    const void* draft_logits;    /* [B, K, V] dtype (device); NULL if all greedy  */
+    const int32_t* draft_tokens; /* [B, K] int32 (device)                         */
+    int B, K, V;
+    sv_dtype dtype;
+    float temperature;
+    sv_mode mode;                /* the mode of every sequence when modes == NULL */
+    const int32_t* modes;        /* [B] int32 (device) per-sequence SV_GREEDY or
+                                    SV_SAMPLE, or NULL; other values make the
+                                    sequence invalid                               */
+    uint64_t seed;
+    const uint64_t* seq_ids;     /* [B] uint64 (device) Philox sequence ids, or
+                                    NULL (id = b); lets a batch split across calls
+                                    keep each sequence's random stream            */
+    int32_t* out_tokens;         /* [B, K+1] int32 (device)                       */
+    int32_t* out_n_accepted;     /* [B] int32 (device)                            */
+    float* out_p_target;         /* [B, K] float (device) or NULL: P_t(x_i) at the
+                                    call's temperature (NaN for greedy sequences) */
+    float* out_p_draft;          /* [B, K] float (device) or NULL: P_d(x_i)       */
+    float* out_residual_mass;    /* [B] float (device) or NULL: total mass of the
+                                    final draw (residual after a rejection, P_t of
+                                    row K for the bonus); NaN when greedy         */
+    uint32_t* status_word;       /* device uint32 or NULL: sv_device_flag bits are
+                                    OR-ed in; never cleared by the library        */
+    int cluster_size;            /* CTAs that share one sequence: 0 = automatic,
+                                    else 1, 2, 4, 8 or 16                         */
+    sv_stream_t stream;
+} sv_verify_args;
+
+/* spec_verify with per-sequence modes, explicit sequence ids and optional
+ * probability outputs. Same conventions and errors as spec_verify. */
+sv_status spec_verify_ex(const sv_verify_args* args);
+
+/* Bytes of device workspace spec_verify_lmhead needs for these sizes. */
+size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V);
+
+/* Fused LM head + verify: the target rows are computed on the GPU as
+ * logits[B*(K+1), V] = hidden[B*(K+1), d] . W[d, V] (bf16 inputs, fp32
+ * accumulation on the tensor cores) and verified against the draft rows as
+ * spec_verify does.
+ *   hidden [B, K+1, d] bf16 (device), W [d, V] bf16 (device, V contiguous),
+ *   draft_logits [B, K, V] of draft_dtype (device; NULL in greedy mode),
+ *   d a positive multiple of 64, V a positive multiple of 8.
+ *   workspace: device buffer of at least
+ *   spec_verify_lmhead_workspace_bytes(B, K, d, V) bytes, 256-byte aligned;
+ *   it receives the fp32 target logits and per-tile partials and may be
+ *   reused once the call's work on `stream` has completed.
+ * Other arguments as in spec_verify. */
+sv_status spec_verify_lmhead(const void* hidden, const void* W,
+                             const void* draft_logits,
+                             const int32_t* draft_tokens, int B, int K, int d,
+                             int V, sv_dtype draft_dtype, float temperature,
+                             sv_mode mode, uint64_t seed, void* workspace,
+                             size_t workspace_bytes, int32_t* out_tokens,
+                             int32_t* out_n_accepted, sv_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+const char* sv_status_string(sv_status status);
+
+/* The CUDA error behind the last SV_ERR_CUDA on this host thread (0 if none). */
+int sv_last_cuda_error(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int sv_version(void);
+
+/* sizeof(sv_verify_args) as compiled into the library, so that bindings can
+ * check their copy of the struct layout. */
+size_t sv_verify_args_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,263 @@
+"""Thin ctypes binding of libspecverify (argument marshalling only).
+
+Every function takes torch tensors that already live on the current CUDA
+device, passes their data pointers and the current torch stream to the C ABI
+declared in include/specverify.h, and raises SpecVerifyError on a non-OK
+status. All of the verify arithmetic runs in the library's CUDA kernels; this
+module computes nothing. Missing outputs are allocated with torch.empty.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+SV_F32, SV_BF16 = 0, 1
+SV_GREEDY, SV_SAMPLE = 0, 1
+
+SV_FLAG_BAD_TOKEN = 1
+SV_FLAG_BAD_ROW = 2
+SV_FLAG_RESIDUAL_FALLBACK = 4
+SV_FLAG_DRAW_EDGE = 8
+SV_FLAG_BAD_MODE = 16
+SV_FLAG_TIMEOUT = 32
+
+STATUS_NAMES = {
+    0: "SV_OK", 1: "SV_ERR_NULL", 2: "SV_ERR_SHAPE", 3: "SV_ERR_DTYPE", 4: "SV_ERR_TEMPERATURE",
+    5: "SV_ERR_WORKSPACE", 6: "SV_ERR_ARCH", 7: "SV_ERR_CUDA", 8: "SV_ERR_MODE",
+    9: "SV_ERR_ALIGN", 10: "SV_ERR_CONFIG", 11: "SV_ERR_NOT_IMPLEMENTED",
+}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {STATUS_NAMES.get(status, status)} ({sv_status_string(status)})"
+        if status == 7:
+            msg += f"; cuda error {_load().sv_last_cuda_error()}"
+        super().__init__(msg)
+
+
+class sv_verify_args(ctypes.Structure):
+    """Mirror of sv_verify_args in include/specverify.h."""
+    _fields_ = [
+        ("target_logits", ctypes.c_void_p),
+        ("draft_logits", ctypes.c_void_p),
+        ("draft_tokens", ctypes.c_void_p),
+        ("B", ctypes.c_int),
+        ("K", ctypes.c_int),
+        ("V", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("temperature", ctypes.c_float),
+        ("mode", ctypes.c_int),
+        ("modes", ctypes.c_void_p),
+        ("seed", ctypes.c_uint64),
+        ("seq_ids", ctypes.c_void_p),
+        ("out_tokens", ctypes.c_void_p),
+        ("out_n_accepted", ctypes.c_void_p),
+        ("out_p_target", ctypes.c_void_p),
+        ("out_p_draft", ctypes.c_void_p),
+        ("out_residual_mass", ctypes.c_void_p),
+        ("status_word", ctypes.c_void_p),
+        ("cluster_size", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+# (name, restype, argtypes) of every symbol the header declares.
+P = ctypes.c_void_p
+I = ctypes.c_int
+SIGNATURES = [
+    ("spec_verify", I, [P, P, P, I, I, I, I, ctypes.c_float, I, ctypes.c_uint64, P, P, P]),
+    ("spec_verify_ex", I, [ctypes.POINTER(sv_verify_args)]),
+    ("spec_verify_lmhead_workspace_bytes", ctypes.c_size_t, [I, I, I, I]),
+    ("spec_verify_lmhead", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I, ctypes.c_uint64, P,
+                               ctypes.c_size_t, P, P, P]),
+    ("sv_status_string", ctypes.c_char_p, [I]),
+    ("sv_last_cuda_error", I, []),
+    ("sv_version", I, []),
+    ("sv_verify_args_size", ctypes.c_size_t, []),
+]
+
+
+def _load():
+    """Load the in-tree library; fail loudly when it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` (there is no fallback)")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, res, args in SIGNATURES:
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            if lib.sv_verify_args_size() != ctypes.sizeof(sv_verify_args):
+                raise ImportError("sv_verify_args layout differs between the binding and the library")
+            _lib = lib
+    return _lib
+
+
+def library():
+    return _load()
+
+
+def sv_status_string(status: int) -> str:
+    return _load().sv_status_string(int(status)).decode()
+
+
+def sv_version() -> int:
+    return int(_load().sv_version())
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise SpecVerifyError(int(status), where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SV_F32
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _mode_code(mode) -> int:
+    if mode in ("greedy", SV_GREEDY):
+        return SV_GREEDY
+    if mode in ("sample", SV_SAMPLE):
+        return SV_SAMPLE
+    raise ValueError(f"mode must be 'greedy' or 'sample', got {mode!r}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("every tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("every tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream, device):
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, temperature=1.0, mode="sample", seed=0,
+                out_tokens=None, out_n_accepted=None, stream=None):
+    """Verify a batch: returns (out_tokens [B, K+1] int32, out_n_accepted [B] int32)."""
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K1, dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().spec_verify(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, K, V,
+            _dtype_code(target_logits), float(temperature), _mode_code(mode),
+            ctypes.c_uint64(int(seed) & (2**64 - 1)), _ptr(out_tokens), _ptr(out_n_accepted),
+            _stream(stream, dev))
+    _check(st, "spec_verify")
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, modes="sample",
+                   seed=0, seq_ids=None, out_tokens=None, out_n_accepted=None, out_p_target=None,
+                   out_p_draft=None, out_residual_mass=None, status_word=None, cluster_size=0,
+                   stream=None, debug=False):
+    """Verify with per-sequence modes ([B] int32 tensor, or 'greedy'/'sample'
+    for all), explicit Philox sequence ids and optional debug outputs.
+    debug=True allocates out_p_target, out_p_draft, out_residual_mass and
+    status_word. Returns a dict of the output tensors."""
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    dev = target_logits.device
+    a = sv_verify_args()
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K1, dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if debug:
+        if out_p_target is None:
+            out_p_target = torch.empty(B, K, dtype=torch.float32, device=dev)
+        if out_p_draft is None:
+            out_p_draft = torch.empty(B, K, dtype=torch.float32, device=dev)
+        if out_residual_mass is None:
+            out_residual_mass = torch.empty(B, dtype=torch.float32, device=dev)
+        if status_word is None:
+            status_word = torch.zeros(1, dtype=torch.int32, device=dev)
+    a.target_logits = _ptr(target_logits)
+    a.draft_logits = _ptr(draft_logits)
+    a.draft_tokens = _ptr(draft_tokens)
+    a.B, a.K, a.V = B, K, V
+    a.dtype = _dtype_code(target_logits)
+    a.temperature = float(temperature)
+    if isinstance(modes, torch.Tensor):
+        a.mode = SV_SAMPLE
+        a.modes = _ptr(modes)
+    else:
+        a.mode = _mode_code(modes)
+        a.modes = None
+    a.seed = int(seed) & (2**64 - 1)
+    a.seq_ids = _ptr(seq_ids)
+    a.out_tokens = _ptr(out_tokens)
+    a.out_n_accepted = _ptr(out_n_accepted)
+    a.out_p_target = _ptr(out_p_target)
+    a.out_p_draft = _ptr(out_p_draft)
+    a.out_residual_mass = _ptr(out_residual_mass)
+    a.status_word = _ptr(status_word)
+    a.cluster_size = int(cluster_size)
+    with torch.cuda.device(dev):
+        a.stream = _stream(stream, dev)
+        st = _load().spec_verify_ex(ctypes.byref(a))
+    _check(st, "spec_verify_ex")
+    return {"tokens": out_tokens, "n_accepted": out_n_accepted, "p_target": out_p_target,
+            "p_draft": out_p_draft, "residual_mass": out_residual_mass,
+            "status_word": status_word}
+
+
+def spec_verify_lmhead_workspace_bytes(B: int, K: int, d: int, V: int) -> int:
+    return int(_load().spec_verify_lmhead_workspace_bytes(B, K, d, V))
+
+
+def spec_verify_lmhead(hidden, W, draft_logits, draft_tokens, temperature=1.0, mode="sample",
+                       seed=0, workspace=None, out_tokens=None, out_n_accepted=None, stream=None):
+    """Fused LM head + verify: hidden [B, K+1, d] bf16, W [d, V] bf16."""
+    B, K1, d = hidden.shape
+    K = K1 - 1
+    V = W.shape[1]
+    dev = hidden.device
+    need = spec_verify_lmhead_workspace_bytes(B, K, d, V)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K1, dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    ddt = _dtype_code(draft_logits) if draft_logits is not None else SV_BF16
+    with torch.cuda.device(dev):
+        st = _load().spec_verify_lmhead(
+            _ptr(hidden), _ptr(W), _ptr(draft_logits), _ptr(draft_tokens), B, K, d, V, ddt,
+            float(temperature), _mode_code(mode), ctypes.c_uint64(int(seed) & (2**64 - 1)),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out_tokens),
+            _ptr(out_n_accepted), _stream(stream, dev))
+    _check(st, "spec_verify_lmhead")
+    return out_tokens, out_n_accepted

@@ -1,0 +1,42 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+// Arguments of the logits-path verify kernel, validated by the C-ABI layer.
+struct VerifyParams {
+    const void* target;        // [B, K+1, V]
+    const void* draft;         // [B, K, V] or nullptr (greedy only)
+    const int32_t* tokens;     // [B, K]
+    const int32_t* modes;      // [B] or nullptr
+    const uint64_t* seq_ids;   // [B] or nullptr
+    int B, K, V;
+    int mode;                  // used when modes == nullptr
+    float c;                   // log2(e) / temperature
+    uint64_t seed;
+    int32_t* out_tokens;       // [B, K+1]
+    int32_t* out_n_accepted;   // [B]
+    float* out_p_target;       // [B, K] or nullptr
+    float* out_p_draft;        // [B, K] or nullptr
+    float* out_residual_mass;  // [B] or nullptr
+    uint32_t* status_word;     // or nullptr
+};
+
+// CTAs per cluster chosen from the shape when the caller asks for automatic.
+int auto_cluster_size(int B, int V, int esize, int num_sms);
+
+// Smallest cluster size whose per-CTA slice of a row fits the kernel's
+// bookkeeping (0: the row is too long for any cluster size).
+int min_cluster_size(int V, int esize);
+
+// Largest cluster size <= cs that can be resident for this dtype (0 if none).
+int usable_cluster_size(int dtype, int cs);
+
+cudaError_t launch_verify_logits(const VerifyParams& p, int dtype, int cs, cudaStream_t stream);
+
+}  // namespace sv

@@ -1,0 +1,1173 @@
+// Verify kernel over logits in HBM: one thread-block cluster per sequence.
+//
+// What it computes follows "Inference-4" (brunomaga.github.io), section
+// "Draft-model speculative decoding", and "Speculative decoding"
+// (leoniemonigatti.com blog), section "Rejection sampling":
+//   greedy  - accept drafts while x_i equals the argmax of target row i; emit
+//             the argmax of the first mismatching row (or of row K);
+//   sample  - accept x_i iff u_i * P_d,i(x_i) < P_t,i(x_i); at the first
+//             rejection j draw from norm(max(0, P_t,j - P_d,j)); if all K pass
+//             draw the bonus from P_t,K. Draws are inverse CDFs in index order.
+//
+// Layout of the work (one launch, no global scratch):
+//   pass 1  Each of the CS CTAs of a cluster owns a contiguous slice of V and
+//           streams that slice of every row the sequence needs (K+1 target
+//           rows; plus K draft rows in sample mode). The slices' 16-byte
+//           slots form one schedule cut into 4 KB chunks (a chunk may hold
+//           pieces of several short rows). Each of the 8 warps owns two
+//           shared-memory stages and streams every 8th chunk itself: bulk
+//           copies (cp.async.bulk, no multicast) complete on the stage's
+//           mbarrier; the warp copies the chunk into registers, refills the
+//           stage with its chunk 16 ahead, then reduces: (R, s) base-2
+//           softmax partials with packed fp32x2 arithmetic for sample rows,
+//           (max, lowest index) for greedy rows. Partial 16-byte slots at a
+//           row's two ends use plain loads.
+//   decide  Every CTA pushes its per-row partials into every CTA of the
+//           cluster (distributed shared memory); after one cluster barrier
+//           each CTA merges them in rank order (so all hold bit-identical
+//           statistics), gathers the logits at the draft tokens, draws its
+//           Philox uniforms and finds the first rejection with a warp ballot.
+//           CTA 0 writes the outputs.
+//   pass 2  Sample mode only: row j (target, and draft after a rejection)
+//           streams through the same stages in 128-slot chunks; a warp sums
+//           each chunk's draw mass in a fixed order (a warp scan per 32
+//           slots). CTA totals are pushed cluster-wide; the CTA holding
+//           u2 * total walks its chunk totals with a warp scan and one warp
+//           re-reads that chunk to find the token.
+//   Every mbarrier wait is bounded; a wait that gives up marks the sequence
+//   invalid (SV_FLAG_TIMEOUT), and every warp waits for its own copies
+//   before the CTA exits.
+#include <cooperative_groups.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+
+#include "sv_device.cuh"
+#include "sv_launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace sv {
+
+constexpr int MAX_K = 31;
+constexpr int MAX_ROWS = 2 * MAX_K + 1;
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+    static constexpr int E = 4;                       // elements per 16-byte slot
+    static constexpr int U1 = 8;                      // slots per lane per step, pass 1
+    static constexpr int U2 = 4;                      // slots per lane per step, pass 2
+    static constexpr uint32_t NEG_INF = 0xFF800000u;  // one -inf element word
+};
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int E = 8;
+    static constexpr int U1 = 8;
+    static constexpr int U2 = 2;
+    static constexpr uint32_t NEG_INF = 0xFF80FF80u;  // two -inf elements
+};
+
+// Element e of a 16-byte slot, widened to float.
+template <typename T>
+__device__ __forceinline__ float elem(const uint4& d, int e);
+template <>
+__device__ __forceinline__ float elem<float>(const uint4& d, int e) {
+    const uint32_t w = e == 0 ? d.x : e == 1 ? d.y : e == 2 ? d.z : d.w;
+    return __uint_as_float(w);
+}
+template <>
+__device__ __forceinline__ float elem<__nv_bfloat16>(const uint4& d, int e) {
+    const int k = e >> 1;
+    const uint32_t w = k == 0 ? d.x : k == 1 ? d.y : k == 2 ? d.z : d.w;
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+template <typename T>
+__device__ __forceinline__ float load_logit(const T* row, int i);
+template <>
+__device__ __forceinline__ float load_logit<float>(const float* row, int i) {
+    return __ldg(row + i);
+}
+template <>
+__device__ __forceinline__ float load_logit<__nv_bfloat16>(const __nv_bfloat16* row, int i) {
+    const unsigned short bits = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+    return __uint_as_float((uint32_t)bits << 16);
+}
+
+// A row seen as 16-byte slots: slot q holds elements q*E - head .. q*E - head
+// + E - 1; the first and last slots may hang over the row's ends.
+struct RowGeom {
+    const uint4* base;
+    int head;
+    int nslot;
+};
+
+template <typename T>
+__device__ __forceinline__ RowGeom row_geom(const T* row, int V) {
+    const uintptr_t p = reinterpret_cast<uintptr_t>(row);
+    const uintptr_t a = p & ~uintptr_t(15);
+    RowGeom g;
+    g.base = reinterpret_cast<const uint4*>(a);
+    g.head = (int)((p - a) / sizeof(T));
+    g.nslot = (int)((p - a + (uintptr_t)V * sizeof(T) + 15) >> 4);
+    return g;
+}
+
+// Slot of row elements starting at element index i0 (which may be negative or
+// run past V): elements outside [0, V) read as -inf.
+template <typename T>
+__device__ __forceinline__ uint4 load_partial_slot(const T* row, int V, int i0) {
+    constexpr int E = Elem<T>::E;
+    uint32_t w[4] = {Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF};
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = i0 + e;
+        if (i < 0 || i >= V) continue;
+        if constexpr (sizeof(T) == 4) {
+            w[e] = __ldg(reinterpret_cast<const uint32_t*>(row) + i);
+        } else {
+            const uint32_t bits = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+            const int k = e >> 1, sh = (e & 1) * 16;
+            w[k] = (w[k] & ~(0xFFFFu << sh)) | (bits << sh);
+        }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T>
+__device__ __forceinline__ bool slot_full(const RowGeom& g, int V, int q) {
+    constexpr int E = Elem<T>::E;
+    const int i0 = q * E - g.head;
+    return i0 >= 0 && i0 + E <= V;
+}
+
+// Any slot of a row, full or partial.
+template <typename T>
+__device__ __forceinline__ uint4 load_slot(const RowGeom& g, const T* row, int V, int q) {
+    constexpr int E = Elem<T>::E;
+    if (slot_full<T>(g, V, q)) return ld_stream(g.base + q);
+    return load_partial_slot<T>(row, V, q * E - g.head);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 neg_inf_slot() {
+    return make_uint4(Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF);
+}
+
+// Contiguous split of [0, n) into G parts; part g is [lo, hi). The host keeps
+// n * G below 2^31 (rows of at most 2^26 slots, G <= 16).
+__device__ __forceinline__ void split_range(int n, int g, int G, int& lo, int& hi) {
+    lo = (int)((unsigned)n * (unsigned)g / (unsigned)G);
+    hi = (int)((unsigned)n * (unsigned)(g + 1) / (unsigned)G);
+}
+
+// A warp's slots [qa, qb) of a row, split into the full interior [ia, ib) and
+// the partial slots at either end (only slot 0 and the row's last slot can be
+// partial), in index order: edge_lo, interior, edge_hi (-1 = none).
+struct WarpSlots {
+    int ia, ib, edge_lo, edge_hi;
+};
+
+template <typename T>
+__device__ __forceinline__ WarpSlots warp_slots(const RowGeom& g, int V, int qa, int qb) {
+    WarpSlots w{qa, qb, -1, -1};
+    if (w.ia < w.ib && !slot_full<T>(g, V, w.ia)) w.edge_lo = w.ia++;
+    if (w.ia < w.ib && !slot_full<T>(g, V, w.ib - 1)) w.edge_hi = --w.ib;
+    return w;
+}
+
+// NaN-propagating maximum of the valid elements of U slots.
+template <typename T, int U>
+__device__ __forceinline__ float group_max(const uint4 (&d)[U]) {
+    if constexpr (sizeof(T) == 2) {
+        uint32_t m = Elem<T>::NEG_INF;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            m = max_nan_bf16x2(m, d[u].x);
+            m = max_nan_bf16x2(m, d[u].y);
+            m = max_nan_bf16x2(m, d[u].z);
+            m = max_nan_bf16x2(m, d[u].w);
+        }
+        return max_nan(bf16_lo(m), bf16_hi(m));
+    } else {
+        float m = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            m = max_nan(m, __uint_as_float(d[u].x));
+            m = max_nan(m, __uint_as_float(d[u].y));
+            m = max_nan(m, __uint_as_float(d[u].z));
+            m = max_nan(m, __uint_as_float(d[u].w));
+        }
+        return m;
+    }
+}
+
+__device__ __forceinline__ float warp_incl_scan(float x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: per-lane accumulation of one group of U slots.
+// ---------------------------------------------------------------------------
+struct SoftAcc {
+    float R;
+    f32x2 a0, a1, a2, a3;  // eight running sums as four packed pairs
+};
+
+__device__ __forceinline__ SoftAcc soft_acc_empty() { return SoftAcc{-INFINITY, 0ull, 0ull, 0ull, 0ull}; }
+
+__device__ __forceinline__ float soft_acc_sum(const SoftAcc& a) {
+    const f32x2 t = add2(add2(a.a0, a.a1), add2(a.a2, a.a3));
+    float x0, x1;
+    unpack2(t, x0, x1);
+    return x0 + x1;
+}
+
+// The 16-byte slot as element pairs (fp32: two pairs, bf16: four pairs).
+template <typename T>
+__device__ __forceinline__ f32x2 slot_pair(const uint4& d, int k);
+template <>
+__device__ __forceinline__ f32x2 slot_pair<float>(const uint4& d, int k) {
+    return k == 0 ? pack2(__uint_as_float(d.x), __uint_as_float(d.y))
+                  : pack2(__uint_as_float(d.z), __uint_as_float(d.w));
+}
+template <>
+__device__ __forceinline__ f32x2 slot_pair<__nv_bfloat16>(const uint4& d, int k) {
+    const uint32_t w = k == 0 ? d.x : k == 1 ? d.y : k == 2 ? d.z : d.w;
+    return bf16x2_to_f32x2(w);
+}
+
+// Adds sum 2^(l * c - R) over U slots to the running partial. R is raised to
+// ceil(max * c) when the slots need it, by an exact power-of-two rescale of
+// the sums; every step is a select, not a branch. A NaN maximum makes R NaN
+// for good (the row is then reported invalid); an all -inf group adds zero.
+template <typename T, int U>
+__device__ __forceinline__ void soft_group(SoftAcc& a, const uint4 (&d)[U], float c) {
+    constexpr int PAIRS = Elem<T>::E / 2;
+    const float m = group_max<T, U>(d);
+    const float Rn = max_nan(a.R, ceilf(m * c));
+    const float sc = pow2_nonpos(fmaxf(a.R - Rn, -1000.0f));  // NaN (-inf - -inf) -> 0
+    const f32x2 sc2 = pack2(sc, sc);
+    a.a0 = mul2(a.a0, sc2);
+    a.a1 = mul2(a.a1, sc2);
+    a.a2 = mul2(a.a2, sc2);
+    a.a3 = mul2(a.a3, sc2);
+    a.R = Rn;
+    const float nR = Rn == -INFINITY ? 0.0f : -Rn;
+    const f32x2 c2 = pack2(c, c), nR2 = pack2(nR, nR);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int k = 0; k < PAIRS; ++k) {
+            const f32x2 e = ex2x2(fma2(slot_pair<T>(d[u], k), c2, nR2));
+            switch ((u * PAIRS + k) & 3) {
+                case 0: a.a0 = add2(a.a0, e); break;
+                case 1: a.a1 = add2(a.a1, e); break;
+                case 2: a.a2 = add2(a.a2, e); break;
+                default: a.a3 = add2(a.a3, e); break;
+            }
+        }
+    }
+}
+
+// q[u]: the slot index of d[u] for this lane (its elements start at
+// q[u] * E - head).
+template <typename T, int U>
+__device__ __forceinline__ void arg_group(ArgPart& best, const uint4 (&d)[U], const int (&q)[U],
+                                          int head) {
+    constexpr int E = Elem<T>::E;
+    const float m = group_max<T, U>(d);
+    if (m > best.v || (m == best.v && m != -INFINITY) || (is_nan(m) && !is_nan(best.v))) {
+        const bool want_nan = is_nan(m);
+        int idx = INT_MAX;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const float x = elem<T>(d[u], e);
+                const bool hit = want_nan ? is_nan(x) : (x == m);
+                const int i = q[u] * E + e - head;
+                if (hit && i < idx) idx = i;
+            }
+        }
+        if (idx != INT_MAX) best = merge_arg(best, ArgPart{m, idx});
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Ring, row table and chunk schedule.
+// ---------------------------------------------------------------------------
+constexpr int NCW = 8;                          // warps per CTA; each streams its own chunks
+constexpr int NTHREADS = NCW * 32;
+constexpr int STAGE_BYTES = 4096;               // one ring stage
+constexpr int NSTAGE = 2 * NCW;                 // warp w owns stages w and w + NCW
+constexpr int RING_BYTES = STAGE_BYTES * NSTAGE;
+constexpr int STAGE_SLOTS = STAGE_BYTES / 16;   // slots per pass-1 chunk (256)
+constexpr int LANE_SLOTS = 4;                   // slots per lane per reduction step
+constexpr int P2_SLOTS = STAGE_SLOTS / 2;       // target slots per pass-2 chunk (128)
+constexpr int P2_DRAFT_OFF = P2_SLOTS * 16;     // draft half of a pass-2 stage
+constexpr int MAX_P2_CHUNKS = 256;              // per CTA slice of one row
+constexpr int MAX_CS = 16;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;       // polls before a wait gives up
+
+// One row of the sequence as this CTA sees it: the 16-byte slots of its slice,
+// split into the full interior [ia, ib) and the partial end slots; `pre` is
+// the number of interior slots of the rows before it (the pass-1 schedule
+// concatenates every row's interior slots and cuts them into chunks).
+struct RowInfo {
+    const uint4* base;  // 16-byte aligned address of slot 0
+    int head;           // elements between base and the row's first element
+    int ia, ib, edge_lo, edge_hi;
+    int pre;
+};
+
+template <typename T>
+__device__ __forceinline__ const T* seq_row(const T* tgt, const T* drf, int b, int K, int V, int r) {
+    return r <= K ? tgt + ((size_t)b * (K + 1) + r) * V : drf + ((size_t)b * K + (r - K - 1)) * V;
+}
+
+template <typename T>
+__device__ __forceinline__ RowInfo make_row_info(const T* row, int V, int rank, int CS) {
+    const RowGeom g = row_geom(row, V);
+    int qa, qb;
+    split_range(g.nslot, rank, CS, qa, qb);
+    const WarpSlots sl = warp_slots<T>(g, V, qa, qb);
+    return RowInfo{g.base, g.head, sl.ia, sl.ib, sl.edge_lo, sl.edge_hi, 0};
+}
+
+// Pieces of pass-1 chunk c: global schedule slots [c * STAGE_SLOTS, end) split
+// at row boundaries. `r` is a running row cursor (chunks are visited in
+// order); next_piece returns false once the chunk is exhausted.
+struct PieceIter {
+    int r;       // current row
+    int g;       // next global schedule slot
+    int end;     // end of this chunk in schedule slots
+};
+
+__device__ __forceinline__ bool next_piece(PieceIter& it, const RowInfo* rows, int& row, int& q0,
+                                           int& n, int& off, int chunk_start) {
+    if (it.g >= it.end) return false;
+    while (rows[it.r].pre + (rows[it.r].ib - rows[it.r].ia) <= it.g) ++it.r;  // skip finished rows
+    const RowInfo& ri = rows[it.r];
+    const int row_end = ri.pre + (ri.ib - ri.ia);
+    row = it.r;
+    q0 = ri.ia + (it.g - ri.pre);
+    n = min(it.end, row_end) - it.g;
+    off = it.g - chunk_start;
+    it.g += n;
+    return true;
+}
+
+struct DrawRows {
+    float c;
+    float ntR, invSt;   // target row j: -R and 1/S
+    float ndR, invSd;   // draft row j (use_d only)
+    bool use_d;
+};
+
+__device__ __forceinline__ float draw_mass(const DrawRows& w, float lt, float ld) {
+    const float pt = ex2(fmaf(lt, w.c, w.ntR)) * w.invSt;
+    if (!w.use_d) return pt;
+    const float pd = ex2(fmaf(ld, w.c, w.ndR)) * w.invSd;
+    return fmaxf(pt - pd, 0.0f);
+}
+
+template <typename T>
+__device__ __forceinline__ float slot_mass(const DrawRows& w, const uint4& dt, const uint4& dd) {
+    constexpr int E = Elem<T>::E;
+    float ls = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ls += draw_mass(w, elem<T>(dt, e), elem<T>(dd, e));
+    return ls;
+}
+
+// The rows of the final draw: target row j and (use_d) draft row j.
+template <typename T>
+struct DrawSrc {
+    const T* trow;
+    const T* drow;
+    RowGeom gt, gd;
+    int V;
+};
+
+// Target slot q (target geometry) and the draft elements with the same
+// indices, from global memory; q < 0 gives empty slots.
+template <typename T>
+__device__ __forceinline__ void load_draw_slot(const DrawSrc<T>& src, bool use_d, int q, uint4& dt,
+                                               uint4& dd) {
+    constexpr int E = Elem<T>::E;
+    if (q < 0) {
+        dt = neg_inf_slot<T>();
+        dd = neg_inf_slot<T>();
+        return;
+    }
+    dt = load_slot<T>(src.gt, src.trow, src.V, q);
+    if (!use_d) dd = neg_inf_slot<T>();
+    else if (src.gd.head == src.gt.head) dd = load_slot<T>(src.gd, src.drow, src.V, q);
+    else dd = load_partial_slot<T>(src.drow, src.V, q * E - src.gt.head);
+}
+
+// Inverse CDF over the slots [q_begin, q_begin + n) of the target row, in
+// steps of 32 slots (one per lane) and batches of 4 steps loaded together from
+// global memory: the first element whose cumulative mass exceeds tw, or with
+// tw = +inf the last element with positive mass. Every lane returns the
+// element index. The summation order matches the pass-2 totals.
+template <typename T>
+__device__ int warp_draw_search(const DrawSrc<T>& src, const DrawRows& w, int q_begin, int n,
+                                double tw, int lane) {
+    constexpr int E = Elem<T>::E, BATCH = 4;
+    double run = 0.0;
+    int last_pos = -1;
+    for (int k0 = 0; k0 < n; k0 += 32 * BATCH) {
+        uint4 dt[BATCH], dd[BATCH];
+        int qs[BATCH];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const int i = k0 + k * 32 + lane;
+            qs[k] = i < n ? q_begin + i : -1;
+            load_draw_slot<T>(src, w.use_d, qs[k], dt[k], dd[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+            const float ls = slot_mass<T>(w, dt[k], dd[k]);
+            const float incl = warp_incl_scan(ls, lane);
+            const float prev = __shfl_up_sync(FULL, incl, 1);  // inclusive value of lane - 1
+            const int i0 = qs[k] * E - src.gt.head;
+            int lp = -1;
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                if (qs[k] >= 0 && draw_mass(w, elem<T>(dt[k], e), elem<T>(dd[k], e)) > 0.0f) lp = i0 + e;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
+            if (lp >= 0) last_pos = lp;
+            const unsigned hit = __ballot_sync(FULL, run + (double)incl > tw);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                int tok = -1;
+                if (lane == l) {
+                    double cum = run + (double)(l == 0 ? 0.0f : prev);
+                    int lastp = -1;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        const float r = draw_mass(w, elem<T>(dt[k], e), elem<T>(dd[k], e));
+                        if (r > 0.0f) {
+                            lastp = i0 + e;
+                            cum += (double)r;
+                            if (tok < 0 && cum > tw) tok = i0 + e;
+                        }
+                    }
+                    if (tok < 0) tok = lastp;  // rounding put tw past this lane's last mass
+                }
+                return __shfl_sync(FULL, tok, l);
+            }
+            run += (double)__shfl_sync(FULL, incl, 31);
+        }
+    }
+    return last_pos;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+struct SeqShared {
+    uint64_t full[NSTAGE];
+    RowInfo rows[MAX_ROWS];
+    float2 warp_part[NCW][MAX_ROWS];
+    float2 edge_part[MAX_ROWS];
+    float2 gathered[MAX_CS][MAX_ROWS];  // every CTA's partials, pushed by their owners
+    float2 merged[MAX_ROWS];
+    float p2_part[2][MAX_P2_CHUNKS];
+    float p2_edge[2][2];
+    double gathered_tot[2][MAX_CS];     // every CTA's draw mass, pushed by their owners
+    // decision (identical in every CTA of the cluster)
+    int j, valid, sample, use_d, err;
+    float u2;
+    SoftPart st, sd;
+    double total, tc;
+    int cstar;
+    int total_slots;
+};
+
+// The two ring stages a warp owns (w and w + NCW) and their phase counters.
+// Chunk number `seq` of this warp (over both passes) uses stage seq & 1; the
+// warp refills a stage itself once it has copied the stage into registers.
+struct WarpRing {
+    uint32_t fills[2], waits[2];
+    int warp;
+    __device__ __forceinline__ uint64_t* bar(SeqShared& sh, int b) const { return &sh.full[warp + NCW * b]; }
+    __device__ __forceinline__ char* stage(char* ring, int b) const {
+        return ring + (warp + NCW * b) * STAGE_BYTES;
+    }
+    // Lane 0 announces the bytes; the copies follow (also from lane 0).
+    __device__ __forceinline__ void begin_fill(SeqShared& sh, int b, uint32_t bytes, int lane) {
+        if (lane == 0) mbar_arrive_expect_tx(bar(sh, b), bytes);
+        ++fills[b];
+    }
+    __device__ __forceinline__ bool wait(SeqShared& sh, int b) {
+        const bool ok = mbar_wait(bar(sh, b), waits[b] & 1, WAIT_LIMIT);
+        ++waits[b];
+        return ok;
+    }
+    // Before the CTA exits: every copy this warp issued has landed (bounded).
+    __device__ __forceinline__ void drain(SeqShared& sh) {
+        for (int b = 0; b < 2; ++b)
+            while (waits[b] < fills[b]) (void)wait(sh, b);
+    }
+};
+
+template <bool SAMPLE>
+__device__ __forceinline__ void flush_row(SeqShared& sh, int warp, int lane, int row,
+                                          const SoftAcc& sa, ArgPart ag) {
+    if (SAMPLE) {
+        SoftPart pp{sa.R, soft_acc_sum(sa)};
+        if (sa.R == -INFINITY) pp.s = 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            pp = merge_soft(pp, SoftPart{__shfl_xor_sync(FULL, pp.R, o), __shfl_xor_sync(FULL, pp.s, o)});
+        if (lane == 0) sh.warp_part[warp][row] = pack(pp);
+    } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            ag = merge_arg(ag, ArgPart{__shfl_xor_sync(FULL, ag.v, o), __shfl_xor_sync(FULL, ag.i, o)});
+        if (lane == 0) sh.warp_part[warp][row] = pack(ag);
+    }
+}
+
+constexpr int CHUNK_LANE_SLOTS = STAGE_SLOTS / 32;  // 8 slots per lane
+
+template <typename T, bool SAMPLE>
+__device__ __forceinline__ void reduce_piece(SoftAcc& sa, ArgPart& ag, const uint4 (&d)[CHUNK_LANE_SLOTS],
+                                             int off, int n, int q0, int head, float c, int lane,
+                                             bool whole) {
+#pragma unroll
+    for (int g = 0; g < CHUNK_LANE_SLOTS / LANE_SLOTS; ++g) {
+        uint4 x[LANE_SLOTS];
+        int qs[LANE_SLOTS];
+#pragma unroll
+        for (int u = 0; u < LANE_SLOTS; ++u) {
+            const int i = (g * LANE_SLOTS + u) * 32 + lane;  // slot of the chunk
+            x[u] = (whole || (i >= off && i < off + n)) ? d[g * LANE_SLOTS + u] : neg_inf_slot<T>();
+            qs[u] = q0 + (i - off);
+        }
+        if (SAMPLE) soft_group<T, LANE_SLOTS>(sa, x, c);
+        else arg_group<T, LANE_SLOTS>(ag, x, qs, head);
+    }
+}
+
+// Issues the bulk copies of pass-1 chunk `chunk` into stage b (lane 0 issues,
+// every lane walks the pieces with the row cursor `r`).
+__device__ __forceinline__ void fill_pass1(SeqShared& sh, WarpRing& wr, char* ring, int b, int chunk,
+                                           int total_slots, int& r, int lane) {
+    const int cstart = chunk * STAGE_SLOTS;
+    const int cend = min(cstart + STAGE_SLOTS, total_slots);
+    wr.begin_fill(sh, b, (uint32_t)(cend - cstart) * 16u, lane);
+    char* stage = wr.stage(ring, b);
+    int g = cstart;
+    while (g < cend) {
+        while (sh.rows[r].pre + (sh.rows[r].ib - sh.rows[r].ia) <= g) ++r;
+        const RowInfo& ri = sh.rows[r];
+        const int n = min(cend, ri.pre + (ri.ib - ri.ia)) - g;
+        if (lane == 0)
+            bulk_g2s(stage + (g - cstart) * 16, ri.base + ri.ia + (g - ri.pre), (uint32_t)n * 16u,
+                     wr.bar(sh, b));
+        g += n;
+    }
+}
+
+// Pass 1 of one warp: chunks warp, warp + NCW, ... of the schedule, double
+// buffered in the warp's two stages. Writes one partial per row it saw.
+template <typename T, bool SAMPLE>
+__device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* ring, int total_slots,
+                                             float c, int warp, int lane, uint32_t& seq) {
+    const int nchunks = (total_slots + STAGE_SLOTS - 1) / STAGE_SLOTS;
+    int r_fill = 0, r_proc = 0;
+    for (int j = 0; j < 2; ++j) {
+        const int chunk = warp + NCW * j;
+        if (chunk < nchunks) fill_pass1(sh, wr, ring, (int)((seq + j) & 1), chunk, total_slots, r_fill, lane);
+    }
+    int cur_row = -1;
+    SoftAcc sa = soft_acc_empty();
+    ArgPart ag{-INFINITY, INT_MAX};
+    for (int chunk = warp; chunk < nchunks; chunk += NCW, ++seq) {
+        const int b = (int)(seq & 1);
+        if (!wr.wait(sh, b)) {
+            atomicExch(&sh.err, 1);
+            break;
+        }
+        const int cstart = chunk * STAGE_SLOTS;
+        const int cend = min(cstart + STAGE_SLOTS, total_slots);
+        const char* stage = wr.stage(ring, b);
+        uint4 d[CHUNK_LANE_SLOTS];
+#pragma unroll
+        for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) {
+            const int i = u * 32 + lane;
+            d[u] = i < cend - cstart ? lds128(stage + i * 16) : neg_inf_slot<T>();
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (chunk + 2 * NCW < nchunks) fill_pass1(sh, wr, ring, b, chunk + 2 * NCW, total_slots, r_fill, lane);
+        PieceIter it{r_proc, cstart, cend};
+        int row, q0, n, off;
+        while (next_piece(it, sh.rows, row, q0, n, off, cstart)) {
+            if (row != cur_row) {
+                if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
+                sa = soft_acc_empty();
+                ag = ArgPart{-INFINITY, INT_MAX};
+                cur_row = row;
+            }
+            const bool whole = off == 0 && n == STAGE_SLOTS;
+            if (whole) reduce_piece<T, SAMPLE>(sa, ag, d, 0, n, q0, sh.rows[row].head, c, lane, true);
+            else reduce_piece<T, SAMPLE>(sa, ag, d, off, n, q0, sh.rows[row].head, c, lane, false);
+        }
+        r_proc = it.r;
+    }
+    if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
+}
+
+// Partial slots at the two ends of this CTA's slices (warp 0).
+template <typename T, bool SAMPLE>
+__device__ __forceinline__ void edge_pass1(SeqShared& sh, const T* tgt, const T* drf, int b, int K,
+                                           int V, int nrows, float c, int lane) {
+    for (int r = 0; r < nrows; ++r) {
+        const RowInfo ri = sh.rows[r];
+        float2 part;
+        if (ri.edge_lo < 0 && ri.edge_hi < 0) {
+            part = SAMPLE ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+        } else {
+            const T* row = seq_row(tgt, drf, b, K, V, r);
+            const RowGeom g{ri.base, ri.head, 0};
+            uint4 d[1];
+            int qs[1];
+            qs[0] = lane == 0 ? ri.edge_lo : lane == 1 ? ri.edge_hi : -1;
+            d[0] = qs[0] >= 0 ? load_slot<T>(g, row, V, qs[0]) : neg_inf_slot<T>();
+            if (SAMPLE) {
+                SoftAcc ea = soft_acc_empty();
+                soft_group<T, 1>(ea, d, c);
+                SoftPart pp{ea.R, soft_acc_sum(ea)};
+                if (ea.R == -INFINITY) pp.s = 0.0f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    pp = merge_soft(pp, SoftPart{__shfl_xor_sync(FULL, pp.R, o),
+                                                 __shfl_xor_sync(FULL, pp.s, o)});
+                part = pack(pp);
+            } else {
+                ArgPart ea{-INFINITY, INT_MAX};
+                arg_group<T, 1>(ea, d, qs, ri.head);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    ea = merge_arg(ea, ArgPart{__shfl_xor_sync(FULL, ea.v, o),
+                                               __shfl_xor_sync(FULL, ea.i, o)});
+                part = pack(ea);
+            }
+        }
+        if (lane == 0) sh.edge_part[r] = part;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams p) {
+    extern __shared__ __align__(128) char ring[];
+    __shared__ SeqShared sh;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CS = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = (int)(blockIdx.x / CS);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = p.K, V = p.V;
+    const T* tgt = static_cast<const T*>(p.target);
+    const T* drf = static_cast<const T*>(p.draft);
+
+    const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
+    const bool mode_ok = (mode == 0 || mode == 1) && !(mode == 1 && drf == nullptr);
+    const bool sample = mode == 1 && mode_ok;
+    const int nrows = sample ? 2 * K + 1 : K + 1;
+    const float c = p.c;
+
+    if (tid == 0) {
+        for (int s = 0; s < NSTAGE; ++s) mbar_init(&sh.full[s], 1);
+        sh.err = 0;
+        sh.total_slots = 0;
+        fence_barrier_init();
+    }
+    if (mode_ok && tid < nrows) sh.rows[tid] = make_row_info<T>(seq_row(tgt, drf, b, K, V, tid), V, rank, CS);
+    for (int t = tid; t < NCW * MAX_ROWS; t += NTHREADS) {
+        const int w = t / MAX_ROWS, r = t % MAX_ROWS;
+        sh.warp_part[w][r] = sample ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+    }
+    __syncthreads();
+    if (mode_ok && warp == 0) {
+        // prefix sums of the rows' interior slot counts (the pass-1 schedule)
+        int cnt = 0;
+        for (int r0 = 0; r0 < nrows; r0 += 32) {
+            const int r = r0 + lane;
+            const int m = r < nrows ? sh.rows[r].ib - sh.rows[r].ia : 0;
+            int incl = m;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(FULL, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (r < nrows) sh.rows[r].pre = cnt + incl - m;
+            cnt += __shfl_sync(FULL, incl, 31);
+        }
+        if (lane == 0) sh.total_slots = cnt;
+    }
+    __syncthreads();
+    const int total_slots = mode_ok ? sh.total_slots : 0;
+
+    WarpRing wr{{0u, 0u}, {0u, 0u}, warp};
+    uint32_t seq = 0;  // chunks this warp has handled, over both passes
+
+    // ---------------- pass 1: row partials over this CTA's slice ----------------
+    if (mode_ok) {
+        if (sample) stream_pass1<T, true>(sh, wr, ring, total_slots, c, warp, lane, seq);
+        else stream_pass1<T, false>(sh, wr, ring, total_slots, c, warp, lane, seq);
+        if (warp == 0) {
+            if (sample) edge_pass1<T, true>(sh, tgt, drf, b, K, V, nrows, c, lane);
+            else edge_pass1<T, false>(sh, tgt, drf, b, K, V, nrows, c, lane);
+        }
+    }
+    __syncthreads();
+    // This CTA's partial of every row, pushed into every CTA of the cluster.
+    for (int t = tid; mode_ok && t < CS * nrows; t += NTHREADS) {
+        const int dst = t / nrows, r = t % nrows;
+        float2 acc = sh.edge_part[r];
+        for (int w = 0; w < NCW; ++w) {
+            acc = sample ? pack(merge_soft(as_soft(acc), as_soft(sh.warp_part[w][r])))
+                         : pack(merge_arg(as_arg(acc), as_arg(sh.warp_part[w][r])));
+        }
+        if (sh.err) acc = make_float2(__int_as_float(0x7fc00000), 0.0f);  // poison: invalid
+        cluster.map_shared_rank(&sh.gathered[0][0], dst)[rank * MAX_ROWS + r] = acc;
+    }
+    cluster.sync();
+
+    // ---------------- decide (redundantly in every CTA) ----------------
+    if (warp == 0) {
+        bool bad = !mode_ok;
+        if (mode_ok) {
+            for (int r = lane; r < nrows; r += 32) {
+                float2 acc = sh.gathered[0][r];
+                for (int cr = 1; cr < CS; ++cr) {
+                    const float2 o = sh.gathered[cr][r];
+                    acc = sample ? pack(merge_soft(as_soft(acc), as_soft(o)))
+                                 : pack(merge_arg(as_arg(acc), as_arg(o)));
+                }
+                sh.merged[r] = acc;
+                if (sample) {
+                    const SoftPart sp = as_soft(acc);
+                    bad |= !(isfinite(sp.R) && isfinite(sp.s) && sp.s > 0.0f);
+                } else {
+                    const ArgPart ap = as_arg(acc);
+                    bad |= !isfinite(ap.v) || ap.i < 0 || ap.i >= V;
+                }
+            }
+        }
+        __syncwarp();
+        const uint64_t seqid = p.seq_ids ? __ldg(p.seq_ids + b) : (uint64_t)b;
+        float u = 0.0f, u2 = 0.0f;
+        if (lane <= K) position_uniforms(p.seed, seqid, (uint32_t)lane, u, u2);
+        int x = -1;
+        bool bad_token = false, rej = false;
+        float pt = __int_as_float(0x7fc00000), pd = pt;
+        if (lane < K) {
+            x = __ldg(p.tokens + (size_t)b * K + lane);
+            bad_token = x < 0 || x >= V;
+            if (!bad_token && mode_ok) {
+                if (!sample) {
+                    rej = x != as_arg(sh.merged[lane]).i;
+                } else {
+                    const SoftPart st = as_soft(sh.merged[lane]);
+                    const SoftPart sd = as_soft(sh.merged[K + 1 + lane]);
+                    const float lt = load_logit<T>(tgt + ((size_t)b * (K + 1) + lane) * V, x);
+                    const float ld = load_logit<T>(drf + ((size_t)b * K + lane) * V, x);
+                    const float et = ex2(fmaf(lt, c, -st.R));
+                    const float ed = ex2(fmaf(ld, c, -sd.R));
+                    pt = et / st.s;
+                    pd = ed / sd.s;
+                    // u * P_d(x) < P_t(x)  <=>  u * e_d * S_t < e_t * S_d
+                    rej = !((double)u * (double)ed * (double)st.s < (double)et * (double)sd.s);
+                }
+            }
+        }
+        const bool any_bad_token = __any_sync(FULL, bad_token);
+        const bool invalid = __any_sync(FULL, bad) || any_bad_token;
+        const unsigned rejm = __ballot_sync(FULL, rej);
+        const int j = rejm ? __ffs(rejm) - 1 : K;
+        const float u2j = __shfl_sync(FULL, u2, j);
+        if (lane == 0) {
+            sh.j = j;
+            sh.valid = !invalid;
+            sh.sample = sample;
+            sh.u2 = u2j;
+            if (sample && !invalid) {
+                sh.st = as_soft(sh.merged[j]);
+                sh.use_d = j < K;
+                sh.sd = j < K ? as_soft(sh.merged[K + 1 + j]) : SoftPart{-INFINITY, 0.0f};
+            }
+        }
+        if (rank == 0) {
+            const int greedy_tok = (!sample && !invalid) ? as_arg(sh.merged[j]).i : -1;
+            if (lane <= K) {
+                int tok = -1;
+                if (!invalid) tok = lane < j ? x : (lane == j ? greedy_tok : -1);
+                // in sample mode position j belongs to the CTA that finds the draw
+                if (!(sample && !invalid && lane == j))
+                    p.out_tokens[(size_t)b * (K + 1) + lane] = tok;
+            }
+            if (lane == 0) p.out_n_accepted[b] = invalid ? -1 : j;
+            if (lane < K) {
+                const float qnan = __int_as_float(0x7fc00000);
+                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = (sample && !invalid) ? pt : qnan;
+                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = (sample && !invalid) ? pd : qnan;
+            }
+            if (lane == 0 && (!sample || invalid) && p.out_residual_mass)
+                p.out_residual_mass[b] = __int_as_float(0x7fc00000);
+            if (lane == 0 && p.status_word && invalid)
+                atomicOr(p.status_word, !mode_ok       ? (unsigned)SV_FLAG_BAD_MODE
+                                        : any_bad_token ? (unsigned)SV_FLAG_BAD_TOKEN
+                                                        : (unsigned)SV_FLAG_BAD_ROW);
+            if (lane == 0 && p.status_word && sh.err) atomicOr(p.status_word, (unsigned)SV_FLAG_TIMEOUT);
+        }
+    }
+    __syncthreads();
+
+    if (!(sh.sample && sh.valid)) {
+        wr.drain(sh);
+        return;  // every remote access of this CTA's shared memory happened before the barrier
+    }
+
+    // ---------------- pass 2: mass of the final draw over row j ----------------
+    const int j = sh.j;
+    DrawSrc<T> src;
+    src.trow = tgt + ((size_t)b * (K + 1) + j) * V;
+    src.drow = sh.use_d ? drf + ((size_t)b * K + j) * V : src.trow;
+    src.gt = row_geom(src.trow, V);
+    src.gd = row_geom(src.drow, V);
+    src.V = V;
+    int qa, qb;
+    split_range(src.gt.nslot, rank, CS, qa, qb);
+    const WarpSlots sl = warp_slots<T>(src.gt, V, qa, qb);
+    const bool draft_in_ring = src.gd.head == src.gt.head;
+    DrawRows w;
+    w.c = c;
+    w.ntR = -sh.st.R;
+    w.invSt = 1.0f / sh.st.s;
+    w.ndR = -sh.sd.R;
+    w.invSd = sh.use_d ? 1.0f / sh.sd.s : 0.0f;
+    const int n_chunks = (sl.ib - sl.ia + P2_SLOTS - 1) / P2_SLOTS;
+    constexpr int STEPS = P2_SLOTS / 32;
+
+    int attempt = 0;
+    for (;; ++attempt) {
+        w.use_d = sh.use_d && attempt == 0;
+        const bool ring_d = w.use_d && draft_in_ring;
+        auto fill2 = [&](int bsl, int ci) {
+            const int q = sl.ia + ci * P2_SLOTS;
+            const int n = min(P2_SLOTS, sl.ib - q);
+            wr.begin_fill(sh, bsl, (uint32_t)n * 16u * (ring_d ? 2u : 1u), lane);
+            if (lane == 0) {
+                char* stage = wr.stage(ring, bsl);
+                bulk_g2s(stage, src.gt.base + q, (uint32_t)n * 16u, wr.bar(sh, bsl));
+                if (ring_d) bulk_g2s(stage + P2_DRAFT_OFF, src.gd.base + q, (uint32_t)n * 16u, wr.bar(sh, bsl));
+            }
+        };
+        if (!sh.err) {
+            for (int jj = 0; jj < 2; ++jj) {
+                const int ci = warp + NCW * jj;
+                if (ci < n_chunks) fill2((int)((seq + jj) & 1), ci);
+            }
+            for (int ci = warp; ci < n_chunks; ci += NCW, ++seq) {
+                const int bsl = (int)(seq & 1);
+                if (!wr.wait(sh, bsl)) {
+                    atomicExch(&sh.err, 1);
+                    break;
+                }
+                const int q = sl.ia + ci * P2_SLOTS;
+                const int n = min(P2_SLOTS, sl.ib - q);
+                const char* stage = wr.stage(ring, bsl);
+                uint4 dt[STEPS], dd[STEPS];
+#pragma unroll
+                for (int kk = 0; kk < STEPS; ++kk) {
+                    const int i = kk * 32 + lane;
+                    dt[kk] = neg_inf_slot<T>();
+                    dd[kk] = neg_inf_slot<T>();
+                    if (i < n) {
+                        dt[kk] = lds128(stage + i * 16);
+                        if (ring_d) dd[kk] = lds128(stage + P2_DRAFT_OFF + i * 16);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (ci + 2 * NCW < n_chunks) fill2(bsl, ci + 2 * NCW);
+                float part = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < STEPS; ++kk) {
+                    const int i = kk * 32 + lane;
+                    if (w.use_d && !draft_in_ring && i < n)
+                        dd[kk] = load_partial_slot<T>(src.drow, V, (q + i) * Elem<T>::E - src.gt.head);
+                    const float incl = warp_incl_scan(slot_mass<T>(w, dt[kk], dd[kk]), lane);
+                    part += __shfl_sync(FULL, incl, 31);
+                }
+                if (lane == 0) sh.p2_part[attempt][ci] = part;
+            }
+        }
+        if (warp == 0) {
+            // the partial slots at the two ends of this CTA's slice
+            float e_lo = 0.0f, e_hi = 0.0f;
+            if (sl.edge_lo >= 0 || sl.edge_hi >= 0) {
+                uint4 dt, dd;
+                const int q = lane == 0 ? sl.edge_lo : lane == 1 ? sl.edge_hi : -1;
+                load_draw_slot<T>(src, w.use_d, q, dt, dd);
+                const float m = slot_mass<T>(w, dt, dd);
+                e_lo = __shfl_sync(FULL, m, 0);
+                e_hi = __shfl_sync(FULL, m, 1);
+            }
+            if (lane == 0) {
+                sh.p2_edge[attempt][0] = e_lo;
+                sh.p2_edge[attempt][1] = e_hi;
+            }
+        }
+        __syncthreads();
+        // this CTA's draw mass, in the canonical order, pushed to every CTA
+        if (warp == 0) {
+            double t = 0.0;
+            for (int i = lane; i < n_chunks; i += 32) t += (double)sh.p2_part[attempt][i];
+            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
+            t += (double)sh.p2_edge[attempt][0] + (double)sh.p2_edge[attempt][1];
+            if (sh.err) t = 0.0;
+            t = __shfl_sync(FULL, t, 0);  // one value for every destination CTA
+            if (lane < CS) cluster.map_shared_rank(&sh.gathered_tot[0][0], lane)[attempt * MAX_CS + rank] = t;
+        }
+        cluster.sync();
+        if (tid == 0) {
+            double S = 0.0;
+            for (int cr = 0; cr < CS; ++cr) S += sh.gathered_tot[attempt][cr];
+            sh.total = S;
+        }
+        __syncthreads();
+        if (sh.total > 0.0 || !w.use_d) break;
+        // The residual summed to zero in float: fall back to P_t of row j.
+        if (rank == 0 && tid == 0 && p.status_word)
+            atomicOr(p.status_word, (unsigned)SV_FLAG_RESIDUAL_FALLBACK);
+    }
+
+    if (tid == 0) {
+        const double S = sh.total;
+        const double t = (double)sh.u2 * S;
+        double cum = 0.0;
+        int cstar = -1, last_pos = -1;
+        double tc = 0.0;
+        for (int cr = 0; cr < CS; ++cr) {
+            const double tot = sh.gathered_tot[attempt][cr];
+            if (tot > 0.0) last_pos = cr;
+            if (cstar < 0 && cum + tot > t) {
+                cstar = cr;
+                tc = t - cum;
+            }
+            cum += tot;
+        }
+        if (cstar < 0) {  // t at or past the summed mass: take the last positive element
+            cstar = last_pos;
+            tc = INFINITY;
+            if (rank == 0 && p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_DRAW_EDGE);
+        }
+        if (cstar < 0 && rank == 0) {
+            // No mass at all (cannot happen for a valid row): report the
+            // sequence as invalid rather than leave a slot unwritten.
+            p.out_tokens[(size_t)b * (K + 1) + j] = -1;
+            p.out_n_accepted[b] = -1;
+            if (p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_BAD_ROW);
+        }
+        sh.cstar = cstar;
+        sh.tc = tc;
+        if (rank == 0 && p.out_residual_mass) p.out_residual_mass[b] = (float)S;
+    }
+    __syncthreads();
+
+    if (rank == sh.cstar && warp == 0) {
+        // Walk down this CTA's parts in index order (low edge slot, the chunk
+        // parts, high edge slot): each lane sums a contiguous run of parts, a
+        // warp scan finds the run holding tc, its lane walks the run.
+        const int P = n_chunks + 2;
+        auto part_val = [&](int i) -> double {
+            if (i == 0) return (double)sh.p2_edge[attempt][0];
+            if (i == P - 1) return (double)sh.p2_edge[attempt][1];
+            return (double)sh.p2_part[attempt][i - 1];
+        };
+        const int per = (P + 31) / 32;
+        const int i0 = min(P, lane * per), i1 = min(P, i0 + per);
+        double mine = 0.0;
+        int last_pos = -1;
+        for (int i = i0; i < i1; ++i) {
+            const double v = part_val(i);
+            mine += v;
+            if (v > 0.0) last_pos = i;
+        }
+        double incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const double tc = sh.tc;
+        const unsigned hit = __ballot_sync(FULL, incl > tc);
+        int found = -1;
+        double tw = INFINITY;
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            if (lane == l) {
+                double t = tc - (incl - mine);
+                for (int i = i0; i < i1; ++i) {
+                    const double v = part_val(i);
+                    if (v > t) { found = i; tw = t; break; }
+                    t -= v;
+                }
+                if (found < 0) found = last_pos;  // rounding: this run's last positive part
+            }
+            found = __shfl_sync(FULL, found, l);
+            tw = __shfl_sync(FULL, tw, l);
+        }
+        if (found < 0) {  // rounding put tc past every part: the last positive part
+            int lp = last_pos;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
+            found = lp;
+            tw = INFINITY;
+        }
+        if (found >= 0) {
+            int q0, n;
+            if (found == 0) { q0 = sl.edge_lo; n = 1; }
+            else if (found == P - 1) { q0 = sl.edge_hi; n = 1; }
+            else {
+                q0 = sl.ia + (found - 1) * P2_SLOTS;
+                n = min(P2_SLOTS, sl.ib - q0);
+            }
+            const int token = warp_draw_search<T>(src, w, q0, n, tw, lane);
+            if (lane == 0) p.out_tokens[(size_t)b * (K + 1) + j] = token;
+        }
+    }
+    wr.drain(sh);
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+// Function attributes are per device; set them once per device and dtype.
+static std::atomic<int> g_attr_done[64][2];
+
+template <typename T>
+static cudaError_t prepare_kernel() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int di = sizeof(T) == 4 ? 0 : 1;
+    if (dev >= 0 && dev < 64 && g_attr_done[dev][di].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(verify_logits_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             RING_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(verify_logits_kernel<T>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) g_attr_done[dev][di].store(1, std::memory_order_release);
+    return cudaSuccess;
+}
+
+template <typename T>
+static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, unsigned grid, int cs,
+                        cudaStream_t stream) {
+    cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = RING_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+}
+
+template <typename T>
+static cudaError_t launch_typed(const VerifyParams& p, int cs, cudaStream_t stream) {
+    cudaError_t e = prepare_kernel<T>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config<T>(cfg, attr, (unsigned)(p.B * cs), cs, stream);
+    return cudaLaunchKernelEx(&cfg, verify_logits_kernel<T>, p);
+}
+
+template <typename T>
+static int max_active_clusters(int cs) {
+    if (prepare_kernel<T>() != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config<T>(cfg, attr, (unsigned)cs, cs, 0);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, verify_logits_kernel<T>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// Per device, dtype and log2(cluster size): 0 unknown, 1 usable, 2 not.
+static std::atomic<int> g_cluster_ok[64][2][5];
+
+int usable_cluster_size(int dtype, int cs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int di = dtype == SV_F32 ? 0 : 1;
+    for (; cs >= 1; cs >>= 1) {
+        const int lg = cs >= 16 ? 4 : cs >= 8 ? 3 : cs >= 4 ? 2 : cs >= 2 ? 1 : 0;
+        int state = g_cluster_ok[dev][di][lg].load(std::memory_order_acquire);
+        if (state == 0) {
+            const int n = di == 0 ? max_active_clusters<float>(cs)
+                                  : max_active_clusters<__nv_bfloat16>(cs);
+            state = n > 0 ? 1 : 2;
+            g_cluster_ok[dev][di][lg].store(state, std::memory_order_release);
+        }
+        if (state == 1) return cs;
+    }
+    return 0;
+}
+
+int min_cluster_size(int V, int esize) {
+    const long long nslot = ((long long)V * esize + 15) / 16 + 1;
+    if (nslot > (1LL << 26)) return 0;  // keeps the slot arithmetic inside 32 bits
+    const long long cap = (long long)MAX_P2_CHUNKS * P2_SLOTS;  // slots per CTA slice
+    int cs = 1;
+    while (cs < MAX_CS && (nslot + cs - 1) / cs > cap) cs *= 2;
+    return (nslot + cs - 1) / cs > cap ? 0 : cs;
+}
+
+// The smallest power of two that gives every SM a CTA, while each CTA keeps at
+// least two chunks of every row (measured best on GB300 for the workloads).
+int auto_cluster_size(int B, int V, int esize, int num_sms) {
+    const long long nslot = ((long long)V * esize + 15) / 16;
+    int cs = 1;
+    while (cs < MAX_CS && (long long)B * cs < num_sms && nslot / (2LL * cs) >= STAGE_SLOTS) cs *= 2;
+    const int lo = min_cluster_size(V, esize);
+    return cs < lo ? lo : cs;
+}
+
+cudaError_t launch_verify_logits(const VerifyParams& p, int dtype, int cs, cudaStream_t stream) {
+    if (dtype == SV_F32) return launch_typed<float>(p, cs, stream);
+    return launch_typed<__nv_bfloat16>(p, cs, stream);
+}
+
+}  // namespace sv

@@ -1,0 +1,114 @@
+"""The C ABI library loads, exports every symbol include/*.h declares, and
+rejects bad arguments on the host (CPU only: no call here reaches the GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_24_gb300 import binding
+from speculative_decoding_verification_24_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.library()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", text):
+            name = m.group(1)
+            # a function declaration: identifier followed by '(' at file scope
+            line_start = text.rfind("\n", 0, m.start()) + 1
+            prefix = text[line_start:m.start()]
+            if name in {"defined", "if", "sizeof"} or prefix.strip().startswith("#"):
+                continue
+            if re.search(r"[;{}]\s*$", prefix) or prefix.strip() == "":
+                continue
+            names.add(name)
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("spec_verify", "spec_verify_ex", "spec_verify_lmhead",
+                     "spec_verify_lmhead_workspace_bytes", "sv_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert names
+    so = ctypes.CDLL(binding.LIB_PATH)
+    for name in sorted(names):
+        assert hasattr(so, name), f"{name} declared but not exported"
+    bound = {n for n, _, _ in binding.SIGNATURES}
+    assert names <= bound, f"binding misses {sorted(names - bound)}"
+
+
+def test_struct_layout_matches(lib):
+    assert lib.sv_verify_args_size() == ctypes.sizeof(binding.sv_verify_args)
+    assert lib.sv_version() >= 100
+    assert lib.sv_status_string(0).decode() == "ok"
+    for code in range(12):
+        assert lib.sv_status_string(code)
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def call(lib, target=FAKE, draft=FAKE, tokens=FAKE, B=2, K=4, V=100, dtype=0, T=1.0, mode=1,
+         out_tokens=FAKE, out_n=FAKE):
+    return lib.spec_verify(target, draft, tokens, B, K, V, dtype, T, mode, 0, out_tokens, out_n,
+                           None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(target=None), 1), (dict(tokens=None), 1), (dict(out_tokens=None), 1),
+    (dict(out_n=None), 1), (dict(draft=None, mode=1), 1),
+    (dict(B=0), 2), (dict(K=0), 2), (dict(K=32), 2), (dict(V=1), 2),
+    (dict(dtype=7), 3),
+    (dict(T=0.0), 4), (dict(T=-1.0), 4), (dict(T=float("nan")), 4), (dict(T=float("inf")), 4),
+    (dict(T=1e-40), 4),
+    (dict(mode=5), 8),
+    (dict(target=FAKE + 2, dtype=0), 9), (dict(draft=FAKE + 1, dtype=1), 9),
+    (dict(tokens=FAKE + 2), 9),
+])
+def test_host_validation(lib, kwargs, code):
+    assert call(lib, **kwargs) == code
+
+
+def test_greedy_ignores_temperature_and_draft_validation_order(lib):
+    # greedy with a NULL draft and a bad temperature is valid up to the device
+    # check; here a bad shape still comes first
+    assert call(lib, draft=None, mode=0, T=float("nan"), B=0) == 2
+
+
+def test_ex_validation(lib):
+    a = binding.sv_verify_args()
+    assert lib.spec_verify_ex(None) == 1
+    assert lib.spec_verify_ex(ctypes.byref(a)) == 1
+    a.target_logits = a.draft_logits = a.draft_tokens = a.out_tokens = a.out_n_accepted = FAKE
+    a.B, a.K, a.V, a.dtype, a.temperature, a.mode = 2, 3, 64, 0, 1.0, 1
+    a.cluster_size = 3
+    assert lib.spec_verify_ex(ctypes.byref(a)) == 10
+    a.cluster_size = 32
+    assert lib.spec_verify_ex(ctypes.byref(a)) == 10
+    a.cluster_size = 0
+    a.seq_ids = FAKE + 4
+    assert lib.spec_verify_ex(ctypes.byref(a)) == 9
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ImportError):
+        binding.library()
