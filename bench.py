@@ -206,6 +206,17 @@ def min_bytes(case) -> int:
 # ----------------------------------------------------------------- our arm
 
 
+def uniform_mode(modes: torch.Tensor):
+    """'sample' / 'greedy' when every sequence shares the mode (no per-sequence
+    array to read), else the per-sequence tensor."""
+    m = modes.cpu()
+    if bool((m == 1).all()):
+        return "sample"
+    if bool((m == 0).all()):
+        return "greedy"
+    return modes
+
+
 def time_device(sets, steps, warmup, stream, seed0=0):
     from speculative_decoding_verification_24_gb300 import spec_verify_ex
 
@@ -214,10 +225,12 @@ def time_device(sets, steps, warmup, stream, seed0=0):
     out_tok = torch.empty(steps + warmup, B, K1, dtype=torch.int32, device=dev)
     out_n = torch.empty(steps + warmup, B, dtype=torch.int32, device=dev)
 
+    modes = [uniform_mode(c.modes) for c in sets]
+
     def step(i):
         c = sets[i % len(sets)]
-        spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=c.modes, seed=seed0 + i,
-                       out_tokens=out_tok[i], out_n_accepted=out_n[i], stream=stream)
+        spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=modes[i % len(sets)],
+                       seed=seed0 + i, out_tokens=out_tok[i], out_n_accepted=out_n[i], stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -382,6 +395,9 @@ def run_e2e(args, sets, device, stream, world):
     out_n = torch.empty(B, dtype=torch.int32, device=device)
     res_t = torch.empty(B, K1, dtype=torch.int32).pin_memory()
     res_n = torch.empty(B, dtype=torch.int32).pin_memory()
+    mode0 = uniform_mode(c0.modes)
+    if isinstance(mode0, torch.Tensor):
+        mode0 = dev_m
     h2d = sum(t.numel() * t.element_size() for t in host[0])
     d2h = res_t.numel() * 4 + res_n.numel() * 4
 
@@ -391,7 +407,7 @@ def run_e2e(args, sets, device, stream, world):
         dev_d.copy_(hd, non_blocking=True)
         dev_x.copy_(hx, non_blocking=True)
         dev_m.copy_(hm, non_blocking=True)
-        spec_verify_ex(dev_t, dev_d, dev_x, c0.temperature, modes=dev_m, seed=i,
+        spec_verify_ex(dev_t, dev_d, dev_x, c0.temperature, modes=mode0, seed=i,
                        out_tokens=out_t, out_n_accepted=out_n, stream=stream)
         res_t.copy_(out_t, non_blocking=True)
         res_n.copy_(out_n, non_blocking=True)
@@ -427,21 +443,20 @@ def cpu_baseline(sets, seconds):
     cores = os.cpu_count() or 1
     rows = 0
     used = 1
-    t0 = time.perf_counter()
+    host = [(to_numpy_logits(c.target), to_numpy_logits(c.draft), c.tokens.cpu().numpy(),
+             c.modes.cpu().numpy(), c.temperature) for c in sets[:8]]
     calls = 0
-    for k, c in enumerate(sets):
-        B, K1, _ = c.target.shape
+    el = 0.0
+    while el < seconds:  # cycle over the input sets until the sample is long enough
+        tgt, drf, tok, modes, T = host[calls % len(host)]
+        B, K1, _ = tgt.shape
         threads = min(cores, B)
         used = max(used, threads)
-        tgt, drf = to_numpy_logits(c.target), to_numpy_logits(c.draft)
-        tok, modes = c.tokens.cpu().numpy(), c.modes.cpu().numpy()
         t1 = time.perf_counter()
-        orc.verify(tgt, drf, tok, c.temperature, modes, seed=k, threads=threads)
+        orc.verify(tgt, drf, tok, T, modes, seed=calls, threads=threads)
+        el += time.perf_counter() - t1
         rows += B * K1
         calls += 1
-        if time.perf_counter() - t0 > seconds:
-            break
-    el = time.perf_counter() - t0
     return {"value": rows / el, "unit": "rows/s", "cores": used, "kind": "oracle",
             "sample": f"{calls} verify calls of the workload's batches ({rows} rows), "
                       f"{el:.1f} s of oracle time, threads over sequences"}

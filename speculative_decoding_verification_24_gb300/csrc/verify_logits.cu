@@ -87,6 +87,19 @@ __device__ __forceinline__ float elem<__nv_bfloat16>(const uint4& d, int e) {
     return (e & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 
+// Element e (a runtime index, 0..E-1) of a 16-byte slot.
+template <typename T>
+__device__ __forceinline__ float elem_rt(const uint4& d, int e) {
+    if constexpr (sizeof(T) == 4) {
+        const uint32_t w = e == 0 ? d.x : e == 1 ? d.y : e == 2 ? d.z : d.w;
+        return __uint_as_float(w);
+    } else {
+        const int k = e >> 1;
+        const uint32_t w = k == 0 ? d.x : k == 1 ? d.y : k == 2 ? d.z : d.w;
+        return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ float load_logit(const T* row, int i);
 template <>
@@ -310,7 +323,8 @@ __device__ __forceinline__ void arg_group(ArgPart& best, const uint4 (&d)[U], co
 constexpr int NCW = 8;                          // warps per CTA; each streams its own chunks
 constexpr int NTHREADS = NCW * 32;
 constexpr int STAGE_BYTES = 4096;               // one ring stage
-constexpr int NSTAGE = 2 * NCW;                 // warp w owns stages w and w + NCW
+constexpr int NBUF = 3;                         // stages per warp
+constexpr int NSTAGE = NBUF * NCW;              // warp w owns stages w, w + NCW, w + 2 NCW
 constexpr int RING_BYTES = STAGE_BYTES * NSTAGE;
 constexpr int STAGE_SLOTS = STAGE_BYTES / 16;   // slots per pass-1 chunk (256)
 constexpr int LANE_SLOTS = 4;                   // slots per lane per reduction step
@@ -373,7 +387,26 @@ struct DrawRows {
     float ntR, invSt;   // target row j: -R and 1/S
     float ndR, invSd;   // draft row j (use_d only)
     bool use_d;
+    f32x2 c2, ntR2, invSt2, ndR2, invSd2;  // the same, packed for fp32x2 arithmetic
 };
+
+__device__ __forceinline__ void pack_draw_rows(DrawRows& w) {
+    w.c2 = pack2(w.c, w.c);
+    w.ntR2 = pack2(w.ntR, w.ntR);
+    w.invSt2 = pack2(w.invSt, w.invSt);
+    w.ndR2 = pack2(w.ndR, w.ndR);
+    w.invSd2 = pack2(w.invSd, w.invSd);
+}
+
+// The draw mass of an element pair, bit-identical to draw_mass on each half.
+__device__ __forceinline__ f32x2 draw_mass2(const DrawRows& w, f32x2 lt, f32x2 ld) {
+    const f32x2 pt = mul2(ex2x2(fma2(lt, w.c2, w.ntR2)), w.invSt2);
+    if (!w.use_d) return pt;
+    const f32x2 pd = mul2(ex2x2(fma2(ld, w.c2, w.ndR2)), w.invSd2);
+    float a, b;
+    unpack2(fma2(pd, pack2(-1.0f, -1.0f), pt), a, b);  // pt - pd, rounded once
+    return pack2(fmaxf(a, 0.0f), fmaxf(b, 0.0f));
+}
 
 __device__ __forceinline__ float draw_mass(const DrawRows& w, float lt, float ld) {
     const float pt = ex2(fmaf(lt, w.c, w.ntR)) * w.invSt;
@@ -486,8 +519,10 @@ struct SeqShared {
     float2 edge_part[MAX_ROWS];
     float2 gathered[MAX_CS][MAX_ROWS];  // every CTA's partials, pushed by their owners
     float2 merged[MAX_ROWS];
-    float p2_part[2][MAX_P2_CHUNKS];
-    float p2_edge[2][2];
+    float p2_part[MAX_P2_CHUNKS];
+    float p2_edge[2];
+    int x_tok[MAX_K];                   // draft tokens, and the logits at them
+    float lt_x[MAX_K], ld_x[MAX_K];     // (prefetched at the start)
     double gathered_tot[2][MAX_CS];     // every CTA's draw mass, pushed by their owners
     // decision (identical in every CTA of the cluster)
     int j, valid, sample, use_d, err;
@@ -498,30 +533,34 @@ struct SeqShared {
     int total_slots;
 };
 
-// The two ring stages a warp owns (w and w + NCW) and their phase counters.
-// Chunk number `seq` of this warp (over both passes) uses stage seq & 1; the
-// warp refills a stage itself once it has copied the stage into registers.
+// The NBUF ring stages a warp owns (w, w + NCW, ...). Chunk number `seq` of
+// this warp (counted over both passes) lives in stage seq % NBUF and is that
+// stage's (seq / NBUF)-th fill, so its mbarrier phase parity is
+// (seq / NBUF) & 1. Fills are issued in seq order; `filled` and `waited`
+// count them. The warp refills a stage itself once it has copied the stage
+// into registers.
 struct WarpRing {
-    uint32_t fills[2], waits[2];
     int warp;
-    __device__ __forceinline__ uint64_t* bar(SeqShared& sh, int b) const { return &sh.full[warp + NCW * b]; }
-    __device__ __forceinline__ char* stage(char* ring, int b) const {
-        return ring + (warp + NCW * b) * STAGE_BYTES;
+    uint32_t filled, waited;
+    __device__ __forceinline__ uint64_t* bar(SeqShared& sh, uint32_t seq) const {
+        return &sh.full[warp + NCW * (int)(seq % NBUF)];
     }
-    // Lane 0 announces the bytes; the copies follow (also from lane 0).
-    __device__ __forceinline__ void begin_fill(SeqShared& sh, int b, uint32_t bytes, int lane) {
-        if (lane == 0) mbar_arrive_expect_tx(bar(sh, b), bytes);
-        ++fills[b];
+    __device__ __forceinline__ char* stage(char* ring, uint32_t seq) const {
+        return ring + (warp + NCW * (int)(seq % NBUF)) * STAGE_BYTES;
     }
-    __device__ __forceinline__ bool wait(SeqShared& sh, int b) {
-        const bool ok = mbar_wait(bar(sh, b), waits[b] & 1, WAIT_LIMIT);
-        ++waits[b];
-        return ok;
+    // Lane 0 announces the bytes of fill `seq`; its copies follow (also lane 0).
+    __device__ __forceinline__ void begin_fill(SeqShared& sh, uint32_t seq, uint32_t bytes, int lane) {
+        if (lane == 0) mbar_arrive_expect_tx(bar(sh, seq), bytes);
+        filled = seq + 1;
+    }
+    __device__ __forceinline__ bool wait(SeqShared& sh, uint32_t seq) {
+        waited = seq + 1;
+        return mbar_wait(bar(sh, seq), (seq / NBUF) & 1, WAIT_LIMIT);
     }
     // Before the CTA exits: every copy this warp issued has landed (bounded).
     __device__ __forceinline__ void drain(SeqShared& sh) {
-        for (int b = 0; b < 2; ++b)
-            while (waits[b] < fills[b]) (void)wait(sh, b);
+        for (uint32_t q = waited; q < filled; ++q) (void)mbar_wait(bar(sh, q), (q / NBUF) & 1, WAIT_LIMIT);
+        waited = filled;
     }
 };
 
@@ -566,12 +605,12 @@ __device__ __forceinline__ void reduce_piece(SoftAcc& sa, ArgPart& ag, const uin
 
 // Issues the bulk copies of pass-1 chunk `chunk` into stage b (lane 0 issues,
 // every lane walks the pieces with the row cursor `r`).
-__device__ __forceinline__ void fill_pass1(SeqShared& sh, WarpRing& wr, char* ring, int b, int chunk,
+__device__ __forceinline__ void fill_pass1(SeqShared& sh, WarpRing& wr, char* ring, uint32_t fseq, int chunk,
                                            int total_slots, int& r, int lane) {
     const int cstart = chunk * STAGE_SLOTS;
     const int cend = min(cstart + STAGE_SLOTS, total_slots);
-    wr.begin_fill(sh, b, (uint32_t)(cend - cstart) * 16u, lane);
-    char* stage = wr.stage(ring, b);
+    wr.begin_fill(sh, fseq, (uint32_t)(cend - cstart) * 16u, lane);
+    char* stage = wr.stage(ring, fseq);
     int g = cstart;
     while (g < cend) {
         while (sh.rows[r].pre + (sh.rows[r].ib - sh.rows[r].ia) <= g) ++r;
@@ -579,43 +618,89 @@ __device__ __forceinline__ void fill_pass1(SeqShared& sh, WarpRing& wr, char* ri
         const int n = min(cend, ri.pre + (ri.ib - ri.ia)) - g;
         if (lane == 0)
             bulk_g2s(stage + (g - cstart) * 16, ri.base + ri.ia + (g - ri.pre), (uint32_t)n * 16u,
-                     wr.bar(sh, b));
+                     wr.bar(sh, fseq));
         g += n;
     }
 }
 
-// Pass 1 of one warp: chunks warp, warp + NCW, ... of the schedule, double
-// buffered in the warp's two stages. Writes one partial per row it saw.
+// The logit at the draft token of row r, if this piece of the row holds it,
+// read from the stage before it is refilled: lane 0 writes it into every CTA
+// of the cluster (exactly one CTA's slice holds any given element, so each
+// value has one writer). Row r is target row r (r < K) or draft row r - K - 1;
+// row K has no draft token. x_reg: lane i holds draft token x_i.
+template <typename T>
+__device__ __forceinline__ void capture_logit(SeqShared& sh, cg::cluster_group& cluster, int CS,
+                                              const char* stage, int r, int K, int x_reg, int q0,
+                                              int n, int off, int head, int lane) {
+    constexpr int E = Elem<T>::E;
+    if (r == K) return;
+    const int i = r < K ? r : r - K - 1;
+    const int x = __shfl_sync(FULL, x_reg, i);
+    const int slot = (x + head) / E;  // x + head >= 0 for a valid token
+    if (lane != 0 || x < 0 || slot < q0 || slot >= q0 + n) return;
+    const char* at = stage + (slot - q0 + off) * 16 + ((x + head) % E) * (int)sizeof(T);
+    float v;
+    if constexpr (sizeof(T) == 4) v = *reinterpret_cast<const float*>(at);
+    else v = __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short*>(at)) << 16);
+    float* dst = r < K ? sh.lt_x : sh.ld_x;
+    for (int cr = 0; cr < CS; ++cr) cluster.map_shared_rank(dst, cr)[i] = v;
+}
+
+// As capture_logit for the partial edge slots: each lane holds one slot q
+// (q < 0: none).
+template <typename T>
+__device__ __forceinline__ void capture_edge_logit(SeqShared& sh, cg::cluster_group& cluster, int CS,
+                                                   const uint4& d, int q, int r, int K, int x_reg,
+                                                   int head, int lane) {
+    constexpr int E = Elem<T>::E;
+    if (r == K) return;
+    const int i = r < K ? r : r - K - 1;
+    const int x = __shfl_sync(FULL, x_reg, i);
+    if (x < 0 || q < 0 || (x + head) / E != q) return;
+    const float v = elem_rt<T>(d, (x + head) % E);
+    float* dst = r < K ? sh.lt_x : sh.ld_x;
+    for (int cr = 0; cr < CS; ++cr) cluster.map_shared_rank(dst, cr)[i] = v;
+}
+
+// Pass 1 of one warp: chunks warp, warp + NCW, ... of the schedule, buffered
+// in the warp's NBUF stages. Writes one partial per row it saw.
 template <typename T, bool SAMPLE>
 __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* ring, int total_slots,
-                                             float c, int warp, int lane, uint32_t& seq) {
+                                             float c, int warp, int lane, uint32_t& seq,
+                                             cg::cluster_group& cluster, int CS, int K, int x_reg) {
     const int nchunks = (total_slots + STAGE_SLOTS - 1) / STAGE_SLOTS;
     int r_fill = 0, r_proc = 0;
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < NBUF; ++j) {
         const int chunk = warp + NCW * j;
-        if (chunk < nchunks) fill_pass1(sh, wr, ring, (int)((seq + j) & 1), chunk, total_slots, r_fill, lane);
+        if (chunk < nchunks) fill_pass1(sh, wr, ring, seq + j, chunk, total_slots, r_fill, lane);
     }
     int cur_row = -1;
     SoftAcc sa = soft_acc_empty();
     ArgPart ag{-INFINITY, INT_MAX};
     for (int chunk = warp; chunk < nchunks; chunk += NCW, ++seq) {
-        const int b = (int)(seq & 1);
-        if (!wr.wait(sh, b)) {
+        if (!wr.wait(sh, seq)) {
             atomicExch(&sh.err, 1);
             break;
         }
         const int cstart = chunk * STAGE_SLOTS;
         const int cend = min(cstart + STAGE_SLOTS, total_slots);
-        const char* stage = wr.stage(ring, b);
+        const char* stage = wr.stage(ring, seq);
         uint4 d[CHUNK_LANE_SLOTS];
 #pragma unroll
         for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) {
             const int i = u * 32 + lane;
             d[u] = i < cend - cstart ? lds128(stage + i * 16) : neg_inf_slot<T>();
         }
+        if (SAMPLE) {
+            PieceIter ic{r_proc, cstart, cend};
+            int row, q0, n, off;
+            while (next_piece(ic, sh.rows, row, q0, n, off, cstart))
+                capture_logit<T>(sh, cluster, CS, stage, row, K, x_reg, q0, n, off, sh.rows[row].head, lane);
+        }
         fence_proxy_async_smem();
         __syncwarp();
-        if (chunk + 2 * NCW < nchunks) fill_pass1(sh, wr, ring, b, chunk + 2 * NCW, total_slots, r_fill, lane);
+        if (chunk + NBUF * NCW < nchunks)
+            fill_pass1(sh, wr, ring, seq + NBUF, chunk + NBUF * NCW, total_slots, r_fill, lane);
         PieceIter it{r_proc, cstart, cend};
         int row, q0, n, off;
         while (next_piece(it, sh.rows, row, q0, n, off, cstart)) {
@@ -634,10 +719,27 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
     if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
 }
 
+// Issues pass-2 chunk ci (target slots, and the draft slots when they share
+// the target's alignment) as fill `fseq` of the warp.
+template <typename T>
+__device__ __forceinline__ void fill_pass2(SeqShared& sh, WarpRing& wr, char* ring, uint32_t fseq,
+                                           const DrawSrc<T>& src, int ia, int ib, int ci, bool ring_d,
+                                           int lane) {
+    const int q = ia + ci * P2_SLOTS;
+    const int n = min(P2_SLOTS, ib - q);
+    wr.begin_fill(sh, fseq, (uint32_t)n * 16u * (ring_d ? 2u : 1u), lane);
+    if (lane == 0) {
+        char* stage = wr.stage(ring, fseq);
+        bulk_g2s(stage, src.gt.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
+        if (ring_d) bulk_g2s(stage + P2_DRAFT_OFF, src.gd.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
+    }
+}
+
 // Partial slots at the two ends of this CTA's slices (warp 0).
 template <typename T, bool SAMPLE>
 __device__ __forceinline__ void edge_pass1(SeqShared& sh, const T* tgt, const T* drf, int b, int K,
-                                           int V, int nrows, float c, int lane) {
+                                           int V, int nrows, float c, int lane,
+                                           cg::cluster_group& cluster, int CS, int x_reg) {
     for (int r = 0; r < nrows; ++r) {
         const RowInfo ri = sh.rows[r];
         float2 part;
@@ -651,6 +753,7 @@ __device__ __forceinline__ void edge_pass1(SeqShared& sh, const T* tgt, const T*
             qs[0] = lane == 0 ? ri.edge_lo : lane == 1 ? ri.edge_hi : -1;
             d[0] = qs[0] >= 0 ? load_slot<T>(g, row, V, qs[0]) : neg_inf_slot<T>();
             if (SAMPLE) {
+                capture_edge_logit<T>(sh, cluster, CS, d[0], qs[0], r, K, x_reg, ri.head, lane);
                 SoftAcc ea = soft_acc_empty();
                 soft_group<T, 1>(ea, d, c);
                 SoftPart pp{ea.R, soft_acc_sum(ea)};
@@ -725,16 +828,19 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     __syncthreads();
     const int total_slots = mode_ok ? sh.total_slots : 0;
 
-    WarpRing wr{{0u, 0u}, {0u, 0u}, warp};
+    WarpRing wr{warp, 0u, 0u};
     uint32_t seq = 0;  // chunks this warp has handled, over both passes
+    // Lane i of every warp holds draft token x_i (first used after the
+    // warp's first chunk has arrived, so the load overlaps the copies).
+    const int x_reg = lane < K ? __ldg(p.tokens + (size_t)b * K + lane) : -1;
 
     // ---------------- pass 1: row partials over this CTA's slice ----------------
     if (mode_ok) {
-        if (sample) stream_pass1<T, true>(sh, wr, ring, total_slots, c, warp, lane, seq);
-        else stream_pass1<T, false>(sh, wr, ring, total_slots, c, warp, lane, seq);
+        if (sample) stream_pass1<T, true>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
+        else stream_pass1<T, false>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
         if (warp == 0) {
-            if (sample) edge_pass1<T, true>(sh, tgt, drf, b, K, V, nrows, c, lane);
-            else edge_pass1<T, false>(sh, tgt, drf, b, K, V, nrows, c, lane);
+            if (sample) edge_pass1<T, true>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
+            else edge_pass1<T, false>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
         }
     }
     __syncthreads();
@@ -780,7 +886,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         bool bad_token = false, rej = false;
         float pt = __int_as_float(0x7fc00000), pd = pt;
         if (lane < K) {
-            x = __ldg(p.tokens + (size_t)b * K + lane);
+            x = x_reg;
             bad_token = x < 0 || x >= V;
             if (!bad_token && mode_ok) {
                 if (!sample) {
@@ -788,8 +894,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 } else {
                     const SoftPart st = as_soft(sh.merged[lane]);
                     const SoftPart sd = as_soft(sh.merged[K + 1 + lane]);
-                    const float lt = load_logit<T>(tgt + ((size_t)b * (K + 1) + lane) * V, x);
-                    const float ld = load_logit<T>(drf + ((size_t)b * K + lane) * V, x);
+                    // the logits at x, captured during pass 1 by the CTA holding them
+                    const float lt = sh.lt_x[lane];
+                    const float ld = sh.ld_x[lane];
                     const float et = ex2(fmaf(lt, c, -st.R));
                     const float ed = ex2(fmaf(ld, c, -sd.R));
                     pt = et / st.s;
@@ -864,6 +971,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     w.invSt = 1.0f / sh.st.s;
     w.ndR = -sh.sd.R;
     w.invSd = sh.use_d ? 1.0f / sh.sd.s : 0.0f;
+    pack_draw_rows(w);
     const int n_chunks = (sl.ib - sl.ia + P2_SLOTS - 1) / P2_SLOTS;
     constexpr int STEPS = P2_SLOTS / 32;
 
@@ -871,30 +979,19 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     for (;; ++attempt) {
         w.use_d = sh.use_d && attempt == 0;
         const bool ring_d = w.use_d && draft_in_ring;
-        auto fill2 = [&](int bsl, int ci) {
-            const int q = sl.ia + ci * P2_SLOTS;
-            const int n = min(P2_SLOTS, sl.ib - q);
-            wr.begin_fill(sh, bsl, (uint32_t)n * 16u * (ring_d ? 2u : 1u), lane);
-            if (lane == 0) {
-                char* stage = wr.stage(ring, bsl);
-                bulk_g2s(stage, src.gt.base + q, (uint32_t)n * 16u, wr.bar(sh, bsl));
-                if (ring_d) bulk_g2s(stage + P2_DRAFT_OFF, src.gd.base + q, (uint32_t)n * 16u, wr.bar(sh, bsl));
-            }
-        };
         if (!sh.err) {
-            for (int jj = 0; jj < 2; ++jj) {
+            for (int jj = 0; jj < NBUF; ++jj) {
                 const int ci = warp + NCW * jj;
-                if (ci < n_chunks) fill2((int)((seq + jj) & 1), ci);
+                if (ci < n_chunks) fill_pass2<T>(sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, lane);
             }
             for (int ci = warp; ci < n_chunks; ci += NCW, ++seq) {
-                const int bsl = (int)(seq & 1);
-                if (!wr.wait(sh, bsl)) {
+                if (!wr.wait(sh, seq)) {
                     atomicExch(&sh.err, 1);
                     break;
                 }
                 const int q = sl.ia + ci * P2_SLOTS;
                 const int n = min(P2_SLOTS, sl.ib - q);
-                const char* stage = wr.stage(ring, bsl);
+                const char* stage = wr.stage(ring, seq);
                 uint4 dt[STEPS], dd[STEPS];
 #pragma unroll
                 for (int kk = 0; kk < STEPS; ++kk) {
@@ -908,17 +1005,25 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (ci + 2 * NCW < n_chunks) fill2(bsl, ci + 2 * NCW);
-                float part = 0.0f;
+                if (ci + NBUF * NCW < n_chunks)
+                    fill_pass2<T>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, lane);
+                // the chunk's draw mass: per lane over its slots, then one warp sum
+                f32x2 acc = 0ull;
 #pragma unroll
                 for (int kk = 0; kk < STEPS; ++kk) {
                     const int i = kk * 32 + lane;
                     if (w.use_d && !draft_in_ring && i < n)
                         dd[kk] = load_partial_slot<T>(src.drow, V, (q + i) * Elem<T>::E - src.gt.head);
-                    const float incl = warp_incl_scan(slot_mass<T>(w, dt[kk], dd[kk]), lane);
-                    part += __shfl_sync(FULL, incl, 31);
+#pragma unroll
+                    for (int k2 = 0; k2 < Elem<T>::E / 2; ++k2)
+                        acc = add2(acc, draw_mass2(w, slot_pair<T>(dt[kk], k2), slot_pair<T>(dd[kk], k2)));
                 }
-                if (lane == 0) sh.p2_part[attempt][ci] = part;
+                float a0, a1;
+                unpack2(acc, a0, a1);
+                float part = a0 + a1;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
+                if (lane == 0) sh.p2_part[ci] = part;
             }
         }
         if (warp == 0) {
@@ -933,17 +1038,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 e_hi = __shfl_sync(FULL, m, 1);
             }
             if (lane == 0) {
-                sh.p2_edge[attempt][0] = e_lo;
-                sh.p2_edge[attempt][1] = e_hi;
+                sh.p2_edge[0] = e_lo;
+                sh.p2_edge[1] = e_hi;
             }
         }
         __syncthreads();
         // this CTA's draw mass, in the canonical order, pushed to every CTA
         if (warp == 0) {
             double t = 0.0;
-            for (int i = lane; i < n_chunks; i += 32) t += (double)sh.p2_part[attempt][i];
+            for (int i = lane; i < n_chunks; i += 32) t += (double)sh.p2_part[i];
             for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
-            t += (double)sh.p2_edge[attempt][0] + (double)sh.p2_edge[attempt][1];
+            t += (double)sh.p2_edge[0] + (double)sh.p2_edge[1];
             if (sh.err) t = 0.0;
             t = __shfl_sync(FULL, t, 0);  // one value for every destination CTA
             if (lane < CS) cluster.map_shared_rank(&sh.gathered_tot[0][0], lane)[attempt * MAX_CS + rank] = t;
@@ -1000,9 +1105,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         // warp scan finds the run holding tc, its lane walks the run.
         const int P = n_chunks + 2;
         auto part_val = [&](int i) -> double {
-            if (i == 0) return (double)sh.p2_edge[attempt][0];
-            if (i == P - 1) return (double)sh.p2_edge[attempt][1];
-            return (double)sh.p2_part[attempt][i - 1];
+            if (i == 0) return (double)sh.p2_edge[0];
+            if (i == P - 1) return (double)sh.p2_edge[1];
+            return (double)sh.p2_part[i - 1];
         };
         const int per = (P + 31) / 32;
         const int i0 = min(P, lane * per), i1 = min(P, i0 + per);
