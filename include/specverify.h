@@ -155,7 +155,8 @@ size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V);
  * spec_verify does.
  *   hidden [B, K+1, d] bf16 (device), W [d, V] bf16 (device, V contiguous),
  *   draft_logits [B, K, V] of draft_dtype (device; NULL in greedy mode),
- *   d a positive multiple of 64, V a positive multiple of 8.
+ *   d a positive multiple of 64, V a positive multiple of 8, B * (K+1) <= 256;
+ *   hidden and W 16-byte aligned. Greedy mode ignores draft_dtype.
  *   workspace: device buffer of at least
  *   spec_verify_lmhead_workspace_bytes(B, K, d, V) bytes, 256-byte aligned;
  *   it receives the fp32 target logits and per-tile partials and may be
@@ -168,6 +169,15 @@ sv_status spec_verify_lmhead(const void* hidden, const void* W,
                              sv_mode mode, uint64_t seed, void* workspace,
                              size_t workspace_bytes, int32_t* out_tokens,
                              int32_t* out_n_accepted, sv_stream_t stream);
+
+/* The LM head alone: logits[M, V] = hidden[M, d] . W[d, V] with bf16 inputs
+ * and fp32 accumulation on the tensor cores (the first half of
+ * spec_verify_lmhead, exposed for callers that verify in a separate step).
+ *   hidden [M, d] bf16 (device, d contiguous), W [d, V] bf16 (device, V
+ *   contiguous), out [M, V] fp32 (device). 1 <= M <= 256, d a positive
+ *   multiple of 64, V a positive multiple of 8; hidden and W 16-byte aligned. */
+sv_status spec_lmhead_logits(const void* hidden, const void* W, int M, int d, int V, float* out,
+                             sv_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char* sv_status_string(sv_status status);

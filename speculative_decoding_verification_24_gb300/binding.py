@@ -81,6 +81,7 @@ SIGNATURES = [
     ("spec_verify_lmhead_workspace_bytes", ctypes.c_size_t, [I, I, I, I]),
     ("spec_verify_lmhead", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I, ctypes.c_uint64, P,
                                ctypes.c_size_t, P, P, P]),
+    ("spec_lmhead_logits", I, [P, P, I, I, I, P, P]),
     ("sv_status_string", ctypes.c_char_p, [I]),
     ("sv_last_cuda_error", I, []),
     ("sv_version", I, []),
@@ -232,6 +233,20 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     return {"tokens": out_tokens, "n_accepted": out_n_accepted, "p_target": out_p_target,
             "p_draft": out_p_draft, "residual_mass": out_residual_mass,
             "status_word": status_word}
+
+
+def spec_lmhead_logits(hidden, W, out=None, stream=None):
+    """fp32 logits [M, V] = hidden [M, d] (bf16) . W [d, V] (bf16) on the tensor cores."""
+    hidden = hidden.reshape(-1, hidden.shape[-1])
+    M, d = hidden.shape
+    V = W.shape[1]
+    dev = hidden.device
+    if out is None:
+        out = torch.empty(M, V, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().spec_lmhead_logits(_ptr(hidden), _ptr(W), M, d, V, _ptr(out), _stream(stream, dev))
+    _check(st, "spec_lmhead_logits")
+    return out
 
 
 def spec_verify_lmhead_workspace_bytes(B: int, K: int, d: int, V: int) -> int:

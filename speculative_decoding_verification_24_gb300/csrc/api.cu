@@ -56,12 +56,17 @@ bool valid_cluster_request(int cs) { return cs == 0 || cs == 1 || cs == 2 || cs 
 
 }  // namespace
 
-extern "C" sv_status spec_verify_ex(const sv_verify_args* a) {
+// The verify step over logits in device memory; the target rows have type
+// dtype_t and the draft rows type dtype_d (equal, or fp32 target with bf16
+// draft rows for the LM-head path).
+static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype dtype_d) {
     if (!a) return SV_ERR_NULL;
     if (!a->target_logits || !a->draft_tokens || !a->out_tokens || !a->out_n_accepted)
         return SV_ERR_NULL;
     if (a->B < 1 || a->K < 1 || a->K > 31 || a->V < 2) return SV_ERR_SHAPE;
-    if (a->dtype != SV_F32 && a->dtype != SV_BF16) return SV_ERR_DTYPE;
+    if ((dtype_t != SV_F32 && dtype_t != SV_BF16) || (dtype_d != SV_F32 && dtype_d != SV_BF16) ||
+        !sv::supported_dtypes(dtype_t, dtype_d))
+        return SV_ERR_DTYPE;
     if (!a->modes && a->mode != SV_GREEDY && a->mode != SV_SAMPLE) return SV_ERR_MODE;
     if (!a->modes && a->mode == SV_SAMPLE && !a->draft_logits) return SV_ERR_NULL;
     const bool may_sample = a->modes != nullptr || a->mode == SV_SAMPLE;
@@ -72,8 +77,8 @@ extern "C" sv_status spec_verify_ex(const sv_verify_args* a) {
         c = 1.4426950408889634 / T;  // log2(e) / T
         if (!std::isfinite((float)c)) return SV_ERR_TEMPERATURE;
     }
-    const size_t es = (size_t)esize_of(a->dtype);
-    if (!aligned(a->target_logits, es) || (a->draft_logits && !aligned(a->draft_logits, es)) ||
+    const size_t es_t = (size_t)esize_of(dtype_t), es_d = (size_t)esize_of(dtype_d);
+    if (!aligned(a->target_logits, es_t) || (a->draft_logits && !aligned(a->draft_logits, es_d)) ||
         !aligned(a->draft_tokens, 4) || !aligned(a->out_tokens, 4) || !aligned(a->out_n_accepted, 4) ||
         (a->modes && !aligned(a->modes, 4)) || (a->seq_ids && !aligned(a->seq_ids, 8)) ||
         (a->out_p_target && !aligned(a->out_p_target, 4)) ||
@@ -89,12 +94,12 @@ extern "C" sv_status spec_verify_ex(const sv_verify_args* a) {
     sv_status st = check_device(&sms);
     if (st != SV_OK) return st;
 
-    const int cs_min = sv::min_cluster_size(a->V, (int)es);
+    const int cs_min = sv::min_cluster_size(a->V, (int)es_t);
     if (cs_min == 0) return SV_ERR_SHAPE;
     if (a->cluster_size && a->cluster_size < cs_min) return SV_ERR_CONFIG;
     int cs = a->cluster_size ? a->cluster_size
-                             : sv::auto_cluster_size(a->B, a->V, (int)es, sms);
-    const int usable = sv::usable_cluster_size((int)a->dtype, cs);
+                             : sv::auto_cluster_size(a->B, a->V, (int)es_t, sms);
+    const int usable = sv::usable_cluster_size((int)dtype_t, (int)dtype_d, cs);
     if (usable == 0) return fail_cuda(cudaGetLastError());
     if (a->cluster_size && usable != cs) return SV_ERR_CONFIG;
     cs = usable;
@@ -117,9 +122,14 @@ extern "C" sv_status spec_verify_ex(const sv_verify_args* a) {
     p.out_p_draft = a->out_p_draft;
     p.out_residual_mass = a->out_residual_mass;
     p.status_word = a->status_word;
-    cudaError_t e = sv::launch_verify_logits(p, (int)a->dtype, cs, (cudaStream_t)a->stream);
+    cudaError_t e = sv::launch_verify_logits(p, (int)dtype_t, (int)dtype_d, cs, (cudaStream_t)a->stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return SV_OK;
+}
+
+extern "C" sv_status spec_verify_ex(const sv_verify_args* a) {
+    if (!a) return SV_ERR_NULL;
+    return verify_impl(a, a->dtype, a->dtype);
 }
 
 extern "C" sv_status spec_verify(const void* target_logits, const void* draft_logits,
@@ -167,9 +177,34 @@ extern "C" int sv_version(void) { return 100; }
 
 extern "C" size_t sv_verify_args_size(void) { return sizeof(sv_verify_args); }
 
+static size_t lmhead_logits_bytes(long long M, long long V) {
+    return (size_t)(((M * V * 4) + 255) / 256 * 256);
+}
+
+static sv_status check_lmhead_shape(const void* hidden, const void* W, long long M, int d, int V) {
+    if (!hidden || !W) return SV_ERR_NULL;
+    if (M < 1 || M > 256 || d < 64 || d % 64 != 0 || V < 8 || V % 8 != 0) return SV_ERR_SHAPE;
+    if (!aligned(hidden, 16) || !aligned(W, 16)) return SV_ERR_ALIGN;
+    return SV_OK;
+}
+
+extern "C" sv_status spec_lmhead_logits(const void* hidden, const void* W, int M, int d, int V,
+                                        float* out, sv_stream_t stream) {
+    sv_status st = check_lmhead_shape(hidden, W, M, d, V);
+    if (st != SV_OK) return st;
+    if (!out) return SV_ERR_NULL;
+    if (!aligned(out, 4)) return SV_ERR_ALIGN;
+    int sms = 0;
+    if ((st = check_device(&sms)) != SV_OK) return st;
+    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, M, d, V, out, nullptr, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return SV_OK;
+}
+
 extern "C" size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V) {
-    (void)B; (void)K; (void)d; (void)V;
-    return 0;
+    (void)d;
+    if (B < 1 || K < 1 || V < 1) return 0;
+    return lmhead_logits_bytes((long long)B * (K + 1), V);
 }
 
 extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const void* draft_logits,
@@ -178,8 +213,40 @@ extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const
                                         uint64_t seed, void* workspace, size_t workspace_bytes,
                                         int32_t* out_tokens, int32_t* out_n_accepted,
                                         sv_stream_t stream) {
-    (void)hidden; (void)W; (void)draft_logits; (void)draft_tokens; (void)B; (void)K; (void)d;
-    (void)V; (void)draft_dtype; (void)temperature; (void)mode; (void)seed; (void)workspace;
-    (void)workspace_bytes; (void)out_tokens; (void)out_n_accepted; (void)stream;
-    return SV_ERR_NOT_IMPLEMENTED;
+    if (B < 1 || K < 1 || K > 31) return SV_ERR_SHAPE;
+    const long long M = (long long)B * (K + 1);
+    sv_status st = check_lmhead_shape(hidden, W, M, d, V);
+    if (st != SV_OK) return st;
+    if (draft_dtype != SV_F32 && draft_dtype != SV_BF16) return SV_ERR_DTYPE;
+    if (!workspace) return SV_ERR_WORKSPACE;
+    if (workspace_bytes < lmhead_logits_bytes(M, V)) return SV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return SV_ERR_ALIGN;
+    // validate the verify half before anything is launched
+    sv_verify_args a = {};
+    a.target_logits = workspace;
+    a.draft_logits = draft_logits;
+    a.draft_tokens = draft_tokens;
+    a.B = B;
+    a.K = K;
+    a.V = V;
+    a.dtype = SV_F32;
+    a.temperature = temperature;
+    a.mode = mode;
+    a.seed = seed;
+    a.out_tokens = out_tokens;
+    a.out_n_accepted = out_n_accepted;
+    a.stream = stream;
+    if (!draft_tokens || !out_tokens || !out_n_accepted) return SV_ERR_NULL;
+    if (mode != SV_GREEDY && mode != SV_SAMPLE) return SV_ERR_MODE;
+    if (mode == SV_SAMPLE) {
+        if (!draft_logits) return SV_ERR_NULL;
+        if (!std::isfinite(temperature) || !(temperature > 0.0f)) return SV_ERR_TEMPERATURE;
+    }
+    int sms = 0;
+    if ((st = check_device(&sms)) != SV_OK) return st;
+    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, (int)M, d, V, static_cast<float*>(workspace),
+                                           nullptr, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return verify_impl(&a, SV_F32, mode == SV_SAMPLE ? draft_dtype : SV_F32);
 }
+

@@ -1,0 +1,300 @@
+// LM head on the 5th-generation tensor cores: logits[M, V] = hidden[M, d] .
+// W[d, V] with bf16 inputs and fp32 accumulation, written to an fp32 buffer.
+//
+// The verify step's target rows are the target model's output head applied
+// to the K+1 positions of every sequence ("Speculative decoding",
+// denimpatel.github.io interactive course, section "Memory-bound, not
+// compute-bound": verification is a forward pass whose query dimension is the
+// number of positions, so the head's weights are read once for all of them).
+// M = B * (K+1) is small, so the product is computed transposed (swap-AB):
+//   D^T[v, m] = sum_k W[k, v] * hidden[m, k]
+// with a 128-wide slice of V as the MMA's M dimension (A = W^T, read from the
+// V-contiguous W as an MN-major operand) and the M rows of hidden as the MMA's
+// N dimension (B = hidden, K-major), N = M rounded up to 16 (at most 256).
+//
+// One CTA per 128-column slice of V:
+//   warp 0  TMA producer: per 64-wide step of d, two 64x64 boxes of W and one
+//           64 x N box of hidden (128-byte swizzle) into a 4-stage ring whose
+//           stages complete on mbarriers;
+//   warp 1  allocates the TMEM accumulator (128 lanes x 256 columns) and one
+//           thread issues tcgen05.mma (kind::f16, 4 per stage, K = 16 each),
+//           committing each stage back to the producer and the last one to
+//           the epilogue;
+//   warps 4-7  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
+//           32(w-4)...), one coalesced 128-byte store per column and warp.
+// Every mbarrier wait is bounded; a wait that gives up sets SV_FLAG_TIMEOUT,
+// the CTA skips the remaining work, waits for what it issued and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "sv_device.cuh"
+#include "sv_launch.h"
+
+namespace sv {
+
+constexpr int LM_BLOCK_V = 128;                       // slice of V per CTA (MMA M)
+constexpr int LM_BLOCK_K = 64;                        // d per stage (one 128-byte row of bf16)
+constexpr int LM_STAGES = 4;
+constexpr int LM_A_BYTES = LM_BLOCK_V * LM_BLOCK_K * 2;  // 16 KB: two 64 x 64 boxes of W
+constexpr int LM_BOX_BYTES = 64 * LM_BLOCK_K * 2;        // 8 KB: one box of W
+constexpr int LM_MAX_N = 256;
+constexpr int LM_B_STAGE_MAX = LM_MAX_N * LM_BLOCK_K * 2;  // 32 KB
+constexpr int LM_THREADS = 256;
+constexpr int LM_TMEM_COLS = 256;
+constexpr uint32_t LM_WAIT_LIMIT = 1u << 24;
+
+struct LmParams {
+    int M, d, V, N;     // N: M rounded up to 16
+    float* out;         // [M, V]
+    uint32_t* status;   // optional
+};
+
+// tcgen05 shared-memory matrix descriptor: start address, leading and stride
+// byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
+// A MN-major, B K-major, N x M shape.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int n, int m) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(LM_THREADS, 1)
+    lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
+                       LmParams p) {
+    extern __shared__ __align__(1024) char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    char* a_stage = smem;                                   // LM_STAGES x 16 KB
+    char* b_stage = smem + LM_STAGES * LM_A_BYTES;          // LM_STAGES x N*128 B
+    const int b_bytes = p.N * LM_BLOCK_K * 2;
+    __shared__ __align__(8) uint64_t full[LM_STAGES], empty[LM_STAGES], accum_full;
+    __shared__ uint32_t tmem_base;
+    __shared__ int err;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int v0 = blockIdx.x * LM_BLOCK_V;
+    const int ksteps = p.d / LM_BLOCK_K;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < LM_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&accum_full, 1);
+        err = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&tmem_base)), "r"(LM_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem = tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_h)) : "memory");
+        // A slice whose second 64 columns lie wholly past V loads only the
+        // first box; the MMA rows of the other half are never stored.
+        const bool second_box = v0 + 64 < p.V;
+        const uint32_t stage_tx = (uint32_t)((second_box ? LM_A_BYTES : LM_BOX_BYTES) + b_bytes);
+        int issued = 0;
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int s = ks % LM_STAGES, k = ks / LM_STAGES;
+            if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, LM_WAIT_LIMIT)) {
+                atomicExch(&err, 1);
+                break;
+            }
+            mbar_arrive_expect_tx(&full[s], stage_tx);
+            char* a = a_stage + s * LM_A_BYTES;
+            tma_load_2d(a, &tm_w, v0, ks * LM_BLOCK_K, &full[s]);
+            if (second_box) tma_load_2d(a + LM_BOX_BYTES, &tm_w, v0 + 64, ks * LM_BLOCK_K, &full[s]);
+            tma_load_2d(b_stage + s * LM_B_STAGE_MAX, &tm_h, ks * LM_BLOCK_K, 0, &full[s]);
+            ++issued;
+        }
+        // every load issued has landed before this thread leaves the loop
+        for (int q = issued - LM_STAGES > 0 ? issued - LM_STAGES : 0; q < issued; ++q)
+            (void)mbar_wait(&full[q % LM_STAGES], (q / LM_STAGES) & 1, LM_WAIT_LIMIT);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        const uint32_t idesc = umma_idesc_bf16(p.N, LM_BLOCK_V);
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const int s = ks % LM_STAGES, k = ks / LM_STAGES;
+            if (!mbar_wait(&full[s], k & 1, LM_WAIT_LIMIT)) {
+                atomicExch(&err, 1);
+                break;
+            }
+            tmem_fence_after();
+            const uint32_t a0 = smem_u32(a_stage + s * LM_A_BYTES);
+            const uint32_t b0 = smem_u32(b_stage + s * LM_B_STAGE_MAX);
+#pragma unroll
+            for (int kk = 0; kk < LM_BLOCK_K / 16; ++kk) {
+                // A (MN-major): 16 rows of d = two 8-row swizzle atoms (2 KB);
+                //   LBO = the second 64-wide block of V (the second box), SBO = 8 rows.
+                // B (K-major): 16 elements of d = 32 bytes inside the 128-byte row.
+                const uint64_t ad = umma_desc_sw128(a0 + kk * 2048, LM_BOX_BYTES, 1024);
+                const uint64_t bd = umma_desc_sw128(b0 + kk * 32, 16, 1024);
+                umma_bf16(tmem, ad, bd, idesc, (ks | kk) != 0);
+            }
+            umma_commit(&empty[s]);  // the stage is free once these MMAs completed
+        }
+        umma_commit(&accum_full);
+    } else if (warp >= 4) {
+        // ---- epilogue: TMEM -> registers -> global (coalesced per column)
+        const int q = warp - 4;
+        bool ok = mbar_wait(&accum_full, 0, LM_WAIT_LIMIT);
+        tmem_fence_after();
+        if (!ok) atomicExch(&err, 1);
+        // tcgen05.ld is warp-collective: the whole warp reads or none of it
+        ok = __all_sync(0xffffffffu, ok && *(volatile int*)&err == 0);
+        const int v = v0 + 32 * q + lane;
+        if (ok) {
+            for (int c0 = 0; c0 < p.N; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int m = c0 + c;
+                    if (m < p.M && v < p.V) p.out[(size_t)m * p.V + v] = __uint_as_float(r[c]);
+                }
+            }
+        }
+        tmem_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LM_TMEM_COLS)
+                     : "memory");
+    }
+    if (threadIdx.x == 0 && err && p.status) atomicOr(p.status, (unsigned)SV_FLAG_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static std::atomic<void*> fn{nullptr};
+    void* f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box [box_rows, 64]
+// (64 bf16 = 128 bytes inner), 128-byte swizzle, zero fill out of bounds.
+static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
+    if (!encode) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int lmhead_smem_bytes(int N) {
+    (void)N;
+    return 1024 + LM_STAGES * (LM_A_BYTES + LM_B_STAGE_MAX);
+}
+
+cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
+                               uint32_t* status, cudaStream_t stream) {
+    static std::atomic<int> attr_done{0};
+    const int smem = lmhead_smem_bytes(0);
+    if (!attr_done.load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_done.store(1, std::memory_order_release);
+    }
+    LmParams p;
+    p.M = M;
+    p.d = d;
+    p.V = V;
+    p.N = (M + 15) / 16 * 16;
+    p.out = out;
+    p.status = status;
+    CUtensorMap tm_w, tm_h;
+    if (!encode_bf16_2d(&tm_w, W, (uint64_t)d, (uint64_t)V, 64) ||
+        !encode_bf16_2d(&tm_h, hidden, (uint64_t)M, (uint64_t)d, (uint32_t)p.N))
+        return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((V + LM_BLOCK_V - 1) / LM_BLOCK_V));
+    lmhead_gemm_kernel<<<grid, LM_THREADS, smem, stream>>>(tm_w, tm_h, p);
+    return cudaGetLastError();
+}
+
+}  // namespace sv

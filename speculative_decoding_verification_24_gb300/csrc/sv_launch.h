@@ -34,9 +34,20 @@ int auto_cluster_size(int B, int V, int esize, int num_sms);
 // bookkeeping (0: the row is too long for any cluster size).
 int min_cluster_size(int V, int esize);
 
-// Largest cluster size <= cs that can be resident for this dtype (0 if none).
-int usable_cluster_size(int dtype, int cs);
+// Whether the verify kernel is built for this (target, draft) pair of types:
+// both fp32, both bf16, or fp32 target rows with bf16 draft rows.
+bool supported_dtypes(int dtype_target, int dtype_draft);
 
-cudaError_t launch_verify_logits(const VerifyParams& p, int dtype, int cs, cudaStream_t stream);
+// Largest cluster size <= cs that can be resident for these types (0 if none).
+int usable_cluster_size(int dtype_target, int dtype_draft, int cs);
+
+cudaError_t launch_verify_logits(const VerifyParams& p, int dtype_target, int dtype_draft, int cs,
+                                 cudaStream_t stream);
+
+// LM head: logits[M, V] (fp32) = hidden[M, d] . W[d, V] (bf16) on the tensor
+// cores; 1 <= M <= 256, d a multiple of 64, V a multiple of 8, 16-byte
+// aligned bases.
+cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
+                               uint32_t* status, cudaStream_t stream);
 
 }  // namespace sv

@@ -43,6 +43,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "sv_device.cuh"
 #include "sv_launch.h"
@@ -345,9 +346,35 @@ struct RowInfo {
     int pre;
 };
 
-template <typename T>
-__device__ __forceinline__ const T* seq_row(const T* tgt, const T* drf, int b, int K, int V, int r) {
-    return r <= K ? tgt + ((size_t)b * (K + 1) + r) * V : drf + ((size_t)b * K + (r - K - 1)) * V;
+// Row r of sequence b: target row r (r <= K) or draft row r - K - 1.
+template <typename TT>
+__device__ __forceinline__ const TT* target_row(const TT* tgt, int b, int K, int V, int r) {
+    return tgt + ((size_t)b * (K + 1) + r) * V;
+}
+template <typename TD>
+__device__ __forceinline__ const TD* draft_row(const TD* drf, int b, int K, int V, int r) {
+    return drf + ((size_t)b * K + (r - K - 1)) * V;
+}
+
+// E_TT consecutive elements of a TD row starting at element i0, in the slot
+// format of TT (elements outside [0, V) read as -inf). The mixed case widens
+// bf16 draft elements exactly into fp32 words.
+template <typename TT, typename TD>
+__device__ __forceinline__ uint4 load_elems_as(const TD* row, int V, int i0) {
+    if constexpr (std::is_same<TT, TD>::value) {
+        return load_partial_slot<TT>(row, V, i0);
+    } else {
+        static_assert(sizeof(TT) == 4 && sizeof(TD) == 2, "mixed rows: fp32 target, bf16 draft");
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int i = i0 + e;
+            w[e] = (i >= 0 && i < V)
+                       ? ((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(row) + i) << 16)
+                       : 0xFF800000u;
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
 }
 
 template <typename T>
@@ -424,30 +451,33 @@ __device__ __forceinline__ float slot_mass(const DrawRows& w, const uint4& dt, c
     return ls;
 }
 
-// The rows of the final draw: target row j and (use_d) draft row j.
-template <typename T>
+// The rows of the final draw: target row j and (use_d) draft row j. The
+// draft shares the target's 16-byte slots only when both have the same type
+// and alignment; otherwise its elements are read one by one.
+template <typename TT, typename TD>
 struct DrawSrc {
-    const T* trow;
-    const T* drow;
+    const TT* trow;
+    const TD* drow;
     RowGeom gt, gd;
     int V;
+    bool same_slots;
 };
 
 // Target slot q (target geometry) and the draft elements with the same
 // indices, from global memory; q < 0 gives empty slots.
-template <typename T>
-__device__ __forceinline__ void load_draw_slot(const DrawSrc<T>& src, bool use_d, int q, uint4& dt,
+template <typename TT, typename TD>
+__device__ __forceinline__ void load_draw_slot(const DrawSrc<TT, TD>& src, bool use_d, int q, uint4& dt,
                                                uint4& dd) {
-    constexpr int E = Elem<T>::E;
+    constexpr int E = Elem<TT>::E;
     if (q < 0) {
-        dt = neg_inf_slot<T>();
-        dd = neg_inf_slot<T>();
+        dt = neg_inf_slot<TT>();
+        dd = neg_inf_slot<TT>();
         return;
     }
-    dt = load_slot<T>(src.gt, src.trow, src.V, q);
-    if (!use_d) dd = neg_inf_slot<T>();
-    else if (src.gd.head == src.gt.head) dd = load_slot<T>(src.gd, src.drow, src.V, q);
-    else dd = load_partial_slot<T>(src.drow, src.V, q * E - src.gt.head);
+    dt = load_slot<TT>(src.gt, src.trow, src.V, q);
+    if (!use_d) dd = neg_inf_slot<TT>();
+    else if (src.same_slots) dd = load_slot<TT>(src.gd, reinterpret_cast<const TT*>(src.drow), src.V, q);
+    else dd = load_elems_as<TT, TD>(src.drow, src.V, q * E - src.gt.head);
 }
 
 // Inverse CDF over the slots [q_begin, q_begin + n) of the target row, in
@@ -455,9 +485,10 @@ __device__ __forceinline__ void load_draw_slot(const DrawSrc<T>& src, bool use_d
 // global memory: the first element whose cumulative mass exceeds tw, or with
 // tw = +inf the last element with positive mass. Every lane returns the
 // element index. The summation order matches the pass-2 totals.
-template <typename T>
-__device__ int warp_draw_search(const DrawSrc<T>& src, const DrawRows& w, int q_begin, int n,
+template <typename TT, typename TD>
+__device__ int warp_draw_search(const DrawSrc<TT, TD>& src, const DrawRows& w, int q_begin, int n,
                                 double tw, int lane) {
+    using T = TT;
     constexpr int E = Elem<T>::E, BATCH = 4;
     double run = 0.0;
     int last_pos = -1;
@@ -468,7 +499,7 @@ __device__ int warp_draw_search(const DrawSrc<T>& src, const DrawRows& w, int q_
         for (int k = 0; k < BATCH; ++k) {
             const int i = k0 + k * 32 + lane;
             qs[k] = i < n ? q_begin + i : -1;
-            load_draw_slot<T>(src, w.use_d, qs[k], dt[k], dd[k]);
+            load_draw_slot<TT, TD>(src, w.use_d, qs[k], dt[k], dd[k]);
         }
 #pragma unroll
         for (int k = 0; k < BATCH; ++k) {
@@ -664,7 +695,7 @@ __device__ __forceinline__ void capture_edge_logit(SeqShared& sh, cg::cluster_gr
 
 // Pass 1 of one warp: chunks warp, warp + NCW, ... of the schedule, buffered
 // in the warp's NBUF stages. Writes one partial per row it saw.
-template <typename T, bool SAMPLE>
+template <typename TT, typename TD, bool SAMPLE>
 __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* ring, int total_slots,
                                              float c, int warp, int lane, uint32_t& seq,
                                              cg::cluster_group& cluster, int CS, int K, int x_reg) {
@@ -689,13 +720,15 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
 #pragma unroll
         for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) {
             const int i = u * 32 + lane;
-            d[u] = i < cend - cstart ? lds128(stage + i * 16) : neg_inf_slot<T>();
+            d[u] = i < cend - cstart ? lds128(stage + i * 16) : neg_inf_slot<TT>();
         }
         if (SAMPLE) {
             PieceIter ic{r_proc, cstart, cend};
             int row, q0, n, off;
-            while (next_piece(ic, sh.rows, row, q0, n, off, cstart))
-                capture_logit<T>(sh, cluster, CS, stage, row, K, x_reg, q0, n, off, sh.rows[row].head, lane);
+            while (next_piece(ic, sh.rows, row, q0, n, off, cstart)) {
+                if (row <= K) capture_logit<TT>(sh, cluster, CS, stage, row, K, x_reg, q0, n, off, sh.rows[row].head, lane);
+                else capture_logit<TD>(sh, cluster, CS, stage, row, K, x_reg, q0, n, off, sh.rows[row].head, lane);
+            }
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -711,8 +744,14 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
                 cur_row = row;
             }
             const bool whole = off == 0 && n == STAGE_SLOTS;
-            if (whole) reduce_piece<T, SAMPLE>(sa, ag, d, 0, n, q0, sh.rows[row].head, c, lane, true);
-            else reduce_piece<T, SAMPLE>(sa, ag, d, off, n, q0, sh.rows[row].head, c, lane, false);
+            const int head = sh.rows[row].head;
+            if (std::is_same<TT, TD>::value || row <= K) {
+                if (whole) reduce_piece<TT, SAMPLE>(sa, ag, d, 0, n, q0, head, c, lane, true);
+                else reduce_piece<TT, SAMPLE>(sa, ag, d, off, n, q0, head, c, lane, false);
+            } else {
+                if (whole) reduce_piece<TD, SAMPLE>(sa, ag, d, 0, n, q0, head, c, lane, true);
+                else reduce_piece<TD, SAMPLE>(sa, ag, d, off, n, q0, head, c, lane, false);
+            }
         }
         r_proc = it.r;
     }
@@ -721,9 +760,9 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
 
 // Issues pass-2 chunk ci (target slots, and the draft slots when they share
 // the target's alignment) as fill `fseq` of the warp.
-template <typename T>
+template <typename TT, typename TD>
 __device__ __forceinline__ void fill_pass2(SeqShared& sh, WarpRing& wr, char* ring, uint32_t fseq,
-                                           const DrawSrc<T>& src, int ia, int ib, int ci, bool ring_d,
+                                           const DrawSrc<TT, TD>& src, int ia, int ib, int ci, bool ring_d,
                                            int lane) {
     const int q = ia + ci * P2_SLOTS;
     const int n = min(P2_SLOTS, ib - q);
@@ -736,8 +775,40 @@ __device__ __forceinline__ void fill_pass2(SeqShared& sh, WarpRing& wr, char* ri
 }
 
 // Partial slots at the two ends of this CTA's slices (warp 0).
+// One partial edge slot per lane (lane 0: the low end, lane 1: the high end of
+// this CTA's slice of row r), reduced like the chunks.
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ void edge_pass1(SeqShared& sh, const T* tgt, const T* drf, int b, int K,
+__device__ __forceinline__ float2 edge_row(SeqShared& sh, const T* row, const RowInfo& ri, int r,
+                                           int K, int V, float c, int lane, cg::cluster_group& cluster,
+                                           int CS, int x_reg) {
+    const RowGeom g{ri.base, ri.head, 0};
+    uint4 d[1];
+    int qs[1];
+    qs[0] = lane == 0 ? ri.edge_lo : lane == 1 ? ri.edge_hi : -1;
+    d[0] = qs[0] >= 0 ? load_slot<T>(g, row, V, qs[0]) : neg_inf_slot<T>();
+    if (SAMPLE) {
+        capture_edge_logit<T>(sh, cluster, CS, d[0], qs[0], r, K, x_reg, ri.head, lane);
+        SoftAcc ea = soft_acc_empty();
+        soft_group<T, 1>(ea, d, c);
+        SoftPart pp{ea.R, soft_acc_sum(ea)};
+        if (ea.R == -INFINITY) pp.s = 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            pp = merge_soft(pp, SoftPart{__shfl_xor_sync(FULL, pp.R, o), __shfl_xor_sync(FULL, pp.s, o)});
+        return pack(pp);
+    } else {
+        ArgPart ea{-INFINITY, INT_MAX};
+        arg_group<T, 1>(ea, d, qs, ri.head);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            ea = merge_arg(ea, ArgPart{__shfl_xor_sync(FULL, ea.v, o), __shfl_xor_sync(FULL, ea.i, o)});
+        return pack(ea);
+    }
+}
+
+// Partial slots at the two ends of this CTA's slices (warp 0).
+template <typename TT, typename TD, bool SAMPLE>
+__device__ __forceinline__ void edge_pass1(SeqShared& sh, const TT* tgt, const TD* drf, int b, int K,
                                            int V, int nrows, float c, int lane,
                                            cg::cluster_group& cluster, int CS, int x_reg) {
     for (int r = 0; r < nrows; ++r) {
@@ -745,39 +816,16 @@ __device__ __forceinline__ void edge_pass1(SeqShared& sh, const T* tgt, const T*
         float2 part;
         if (ri.edge_lo < 0 && ri.edge_hi < 0) {
             part = SAMPLE ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+        } else if (r <= K) {
+            part = edge_row<TT, SAMPLE>(sh, target_row(tgt, b, K, V, r), ri, r, K, V, c, lane, cluster, CS, x_reg);
         } else {
-            const T* row = seq_row(tgt, drf, b, K, V, r);
-            const RowGeom g{ri.base, ri.head, 0};
-            uint4 d[1];
-            int qs[1];
-            qs[0] = lane == 0 ? ri.edge_lo : lane == 1 ? ri.edge_hi : -1;
-            d[0] = qs[0] >= 0 ? load_slot<T>(g, row, V, qs[0]) : neg_inf_slot<T>();
-            if (SAMPLE) {
-                capture_edge_logit<T>(sh, cluster, CS, d[0], qs[0], r, K, x_reg, ri.head, lane);
-                SoftAcc ea = soft_acc_empty();
-                soft_group<T, 1>(ea, d, c);
-                SoftPart pp{ea.R, soft_acc_sum(ea)};
-                if (ea.R == -INFINITY) pp.s = 0.0f;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    pp = merge_soft(pp, SoftPart{__shfl_xor_sync(FULL, pp.R, o),
-                                                 __shfl_xor_sync(FULL, pp.s, o)});
-                part = pack(pp);
-            } else {
-                ArgPart ea{-INFINITY, INT_MAX};
-                arg_group<T, 1>(ea, d, qs, ri.head);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    ea = merge_arg(ea, ArgPart{__shfl_xor_sync(FULL, ea.v, o),
-                                               __shfl_xor_sync(FULL, ea.i, o)});
-                part = pack(ea);
-            }
+            part = edge_row<TD, SAMPLE>(sh, draft_row(drf, b, K, V, r), ri, r, K, V, c, lane, cluster, CS, x_reg);
         }
         if (lane == 0) sh.edge_part[r] = part;
     }
 }
 
-template <typename T>
+template <typename TT, typename TD>
 __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams p) {
     extern __shared__ __align__(128) char ring[];
     __shared__ SeqShared sh;
@@ -787,8 +835,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const int b = (int)(blockIdx.x / CS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int K = p.K, V = p.V;
-    const T* tgt = static_cast<const T*>(p.target);
-    const T* drf = static_cast<const T*>(p.draft);
+    const TT* tgt = static_cast<const TT*>(p.target);
+    const TD* drf = static_cast<const TD*>(p.draft);
 
     const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
     const bool mode_ok = (mode == 0 || mode == 1) && !(mode == 1 && drf == nullptr);
@@ -802,7 +850,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         sh.total_slots = 0;
         fence_barrier_init();
     }
-    if (mode_ok && tid < nrows) sh.rows[tid] = make_row_info<T>(seq_row(tgt, drf, b, K, V, tid), V, rank, CS);
+    if (mode_ok && tid < nrows)
+        sh.rows[tid] = tid <= K ? make_row_info<TT>(target_row(tgt, b, K, V, tid), V, rank, CS)
+                                : make_row_info<TD>(draft_row(drf, b, K, V, tid), V, rank, CS);
     for (int t = tid; t < NCW * MAX_ROWS; t += NTHREADS) {
         const int w = t / MAX_ROWS, r = t % MAX_ROWS;
         sh.warp_part[w][r] = sample ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
@@ -836,11 +886,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 
     // ---------------- pass 1: row partials over this CTA's slice ----------------
     if (mode_ok) {
-        if (sample) stream_pass1<T, true>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
-        else stream_pass1<T, false>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
+        if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
+        else stream_pass1<TT, TD, false>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
         if (warp == 0) {
-            if (sample) edge_pass1<T, true>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
-            else edge_pass1<T, false>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
+            if (sample) edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
+            else edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
         }
     }
     __syncthreads();
@@ -955,16 +1005,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 
     // ---------------- pass 2: mass of the final draw over row j ----------------
     const int j = sh.j;
-    DrawSrc<T> src;
+    DrawSrc<TT, TD> src;
     src.trow = tgt + ((size_t)b * (K + 1) + j) * V;
-    src.drow = sh.use_d ? drf + ((size_t)b * K + j) * V : src.trow;
+    src.drow = sh.use_d ? drf + ((size_t)b * K + j) * V : reinterpret_cast<const TD*>(src.trow);
     src.gt = row_geom(src.trow, V);
     src.gd = row_geom(src.drow, V);
     src.V = V;
+    src.same_slots = std::is_same<TT, TD>::value && src.gd.head == src.gt.head;
     int qa, qb;
     split_range(src.gt.nslot, rank, CS, qa, qb);
-    const WarpSlots sl = warp_slots<T>(src.gt, V, qa, qb);
-    const bool draft_in_ring = src.gd.head == src.gt.head;
+    const WarpSlots sl = warp_slots<TT>(src.gt, V, qa, qb);
+    const bool draft_in_ring = src.same_slots;
     DrawRows w;
     w.c = c;
     w.ntR = -sh.st.R;
@@ -982,7 +1033,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         if (!sh.err) {
             for (int jj = 0; jj < NBUF; ++jj) {
                 const int ci = warp + NCW * jj;
-                if (ci < n_chunks) fill_pass2<T>(sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, lane);
+                if (ci < n_chunks) fill_pass2<TT, TD>(sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, lane);
             }
             for (int ci = warp; ci < n_chunks; ci += NCW, ++seq) {
                 if (!wr.wait(sh, seq)) {
@@ -996,8 +1047,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 #pragma unroll
                 for (int kk = 0; kk < STEPS; ++kk) {
                     const int i = kk * 32 + lane;
-                    dt[kk] = neg_inf_slot<T>();
-                    dd[kk] = neg_inf_slot<T>();
+                    dt[kk] = neg_inf_slot<TT>();
+                    dd[kk] = neg_inf_slot<TT>();
                     if (i < n) {
                         dt[kk] = lds128(stage + i * 16);
                         if (ring_d) dd[kk] = lds128(stage + P2_DRAFT_OFF + i * 16);
@@ -1006,17 +1057,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (ci + NBUF * NCW < n_chunks)
-                    fill_pass2<T>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, lane);
+                    fill_pass2<TT, TD>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, lane);
                 // the chunk's draw mass: per lane over its slots, then one warp sum
                 f32x2 acc = 0ull;
 #pragma unroll
                 for (int kk = 0; kk < STEPS; ++kk) {
                     const int i = kk * 32 + lane;
                     if (w.use_d && !draft_in_ring && i < n)
-                        dd[kk] = load_partial_slot<T>(src.drow, V, (q + i) * Elem<T>::E - src.gt.head);
+                        dd[kk] = load_elems_as<TT, TD>(src.drow, V, (q + i) * Elem<TT>::E - src.gt.head);
 #pragma unroll
-                    for (int k2 = 0; k2 < Elem<T>::E / 2; ++k2)
-                        acc = add2(acc, draw_mass2(w, slot_pair<T>(dt[kk], k2), slot_pair<T>(dd[kk], k2)));
+                    for (int k2 = 0; k2 < Elem<TT>::E / 2; ++k2)
+                        acc = add2(acc, draw_mass2(w, slot_pair<TT>(dt[kk], k2), slot_pair<TT>(dd[kk], k2)));
                 }
                 float a0, a1;
                 unpack2(acc, a0, a1);
@@ -1032,8 +1083,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             if (sl.edge_lo >= 0 || sl.edge_hi >= 0) {
                 uint4 dt, dd;
                 const int q = lane == 0 ? sl.edge_lo : lane == 1 ? sl.edge_hi : -1;
-                load_draw_slot<T>(src, w.use_d, q, dt, dd);
-                const float m = slot_mass<T>(w, dt, dd);
+                load_draw_slot<TT, TD>(src, w.use_d, q, dt, dd);
+                const float m = slot_mass<TT>(w, dt, dd);
                 e_lo = __shfl_sync(FULL, m, 0);
                 e_hi = __shfl_sync(FULL, m, 1);
             }
@@ -1157,7 +1208,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 q0 = sl.ia + (found - 1) * P2_SLOTS;
                 n = min(P2_SLOTS, sl.ib - q0);
             }
-            const int token = warp_draw_search<T>(src, w, q0, n, tw, lane);
+            const int token = warp_draw_search<TT, TD>(src, w, q0, n, tw, lane);
             if (lane == 0) p.out_tokens[(size_t)b * (K + 1) + j] = token;
         }
     }
@@ -1167,27 +1218,34 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 // ---------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------
-// Function attributes are per device; set them once per device and dtype.
-static std::atomic<int> g_attr_done[64][2];
+// Type pairs (target, draft): 0 = fp32/fp32, 1 = bf16/bf16, 2 = fp32/bf16.
+constexpr int N_COMBOS = 3;
 
-template <typename T>
+// Function attributes are per device; set them once per device and pair.
+static std::atomic<int> g_attr_done[64][N_COMBOS];
+
+template <typename TT, typename TD>
+static constexpr int combo_of() {
+    return std::is_same<TT, TD>::value ? (sizeof(TT) == 4 ? 0 : 1) : 2;
+}
+
+template <typename TT, typename TD>
 static cudaError_t prepare_kernel() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int di = sizeof(T) == 4 ? 0 : 1;
-    if (dev >= 0 && dev < 64 && g_attr_done[dev][di].load(std::memory_order_acquire)) return cudaSuccess;
-    e = cudaFuncSetAttribute(verify_logits_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    constexpr int ci = combo_of<TT, TD>();
+    if (dev >= 0 && dev < 64 && g_attr_done[dev][ci].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              RING_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(verify_logits_kernel<T>,
+    e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) g_attr_done[dev][di].store(1, std::memory_order_release);
+    if (dev >= 0 && dev < 64) g_attr_done[dev][ci].store(1, std::memory_order_release);
     return cudaSuccess;
 }
 
-template <typename T>
 static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, unsigned grid, int cs,
                         cudaStream_t stream) {
     cfg = {};
@@ -1203,48 +1261,61 @@ static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, unsi
     cfg.numAttrs = 1;
 }
 
-template <typename T>
+template <typename TT, typename TD>
 static cudaError_t launch_typed(const VerifyParams& p, int cs, cudaStream_t stream) {
-    cudaError_t e = prepare_kernel<T>();
+    cudaError_t e = prepare_kernel<TT, TD>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    fill_config<T>(cfg, attr, (unsigned)(p.B * cs), cs, stream);
-    return cudaLaunchKernelEx(&cfg, verify_logits_kernel<T>, p);
+    fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream);
+    return cudaLaunchKernelEx(&cfg, verify_logits_kernel<TT, TD>, p);
 }
 
-template <typename T>
+template <typename TT, typename TD>
 static int max_active_clusters(int cs) {
-    if (prepare_kernel<T>() != cudaSuccess) {
+    if (prepare_kernel<TT, TD>() != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    fill_config<T>(cfg, attr, (unsigned)cs, cs, 0);
+    fill_config(cfg, attr, (unsigned)cs, cs, 0);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, verify_logits_kernel<T>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, verify_logits_kernel<TT, TD>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-// Per device, dtype and log2(cluster size): 0 unknown, 1 usable, 2 not.
-static std::atomic<int> g_cluster_ok[64][2][5];
+static int combo_index(int dtype_target, int dtype_draft) {
+    if (dtype_target == SV_F32 && dtype_draft == SV_F32) return 0;
+    if (dtype_target == SV_BF16 && dtype_draft == SV_BF16) return 1;
+    if (dtype_target == SV_F32 && dtype_draft == SV_BF16) return 2;
+    return -1;
+}
 
-int usable_cluster_size(int dtype, int cs) {
+bool supported_dtypes(int dtype_target, int dtype_draft) {
+    return combo_index(dtype_target, dtype_draft) >= 0;
+}
+
+// Per device, type pair and log2(cluster size): 0 unknown, 1 usable, 2 not.
+static std::atomic<int> g_cluster_ok[64][N_COMBOS][5];
+
+int usable_cluster_size(int dtype_target, int dtype_draft, int cs) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    const int di = dtype == SV_F32 ? 0 : 1;
+    const int ci = combo_index(dtype_target, dtype_draft);
+    if (ci < 0) return 0;
     for (; cs >= 1; cs >>= 1) {
         const int lg = cs >= 16 ? 4 : cs >= 8 ? 3 : cs >= 4 ? 2 : cs >= 2 ? 1 : 0;
-        int state = g_cluster_ok[dev][di][lg].load(std::memory_order_acquire);
+        int state = g_cluster_ok[dev][ci][lg].load(std::memory_order_acquire);
         if (state == 0) {
-            const int n = di == 0 ? max_active_clusters<float>(cs)
-                                  : max_active_clusters<__nv_bfloat16>(cs);
+            const int n = ci == 0   ? max_active_clusters<float, float>(cs)
+                          : ci == 1 ? max_active_clusters<__nv_bfloat16, __nv_bfloat16>(cs)
+                                    : max_active_clusters<float, __nv_bfloat16>(cs);
             state = n > 0 ? 1 : 2;
-            g_cluster_ok[dev][di][lg].store(state, std::memory_order_release);
+            g_cluster_ok[dev][ci][lg].store(state, std::memory_order_release);
         }
         if (state == 1) return cs;
     }
@@ -1270,9 +1341,14 @@ int auto_cluster_size(int B, int V, int esize, int num_sms) {
     return cs < lo ? lo : cs;
 }
 
-cudaError_t launch_verify_logits(const VerifyParams& p, int dtype, int cs, cudaStream_t stream) {
-    if (dtype == SV_F32) return launch_typed<float>(p, cs, stream);
-    return launch_typed<__nv_bfloat16>(p, cs, stream);
+cudaError_t launch_verify_logits(const VerifyParams& p, int dtype_target, int dtype_draft, int cs,
+                                 cudaStream_t stream) {
+    switch (combo_index(dtype_target, dtype_draft)) {
+        case 0: return launch_typed<float, float>(p, cs, stream);
+        case 1: return launch_typed<__nv_bfloat16, __nv_bfloat16>(p, cs, stream);
+        case 2: return launch_typed<float, __nv_bfloat16>(p, cs, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace sv

@@ -112,3 +112,39 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(ImportError):
         binding.library()
+
+
+def test_lmhead_workspace_size(lib):
+    # fp32 logits of B * (K+1) rows, rounded up to 256 bytes
+    assert lib.spec_verify_lmhead_workspace_bytes(32, 5, 4096, 128256) == 32 * 6 * 128256 * 4
+    assert lib.spec_verify_lmhead_workspace_bytes(1, 1, 64, 8) == 256
+    assert lib.spec_verify_lmhead_workspace_bytes(0, 1, 64, 8) == 0
+
+
+def lm_call(lib, hidden=FAKE, W=FAKE, draft=FAKE, tokens=FAKE, B=2, K=3, d=128, V=256, ddt=1,
+            T=1.0, mode=1, ws=FAKE, ws_bytes=1 << 30, out_tokens=FAKE, out_n=FAKE):
+    return lib.spec_verify_lmhead(hidden, W, draft, tokens, B, K, d, V, ddt, T, mode, 0, ws,
+                                  ws_bytes, out_tokens, out_n, None)
+
+
+@pytest.mark.parametrize("kwargs,code", [
+    (dict(hidden=None), 1), (dict(W=None), 1), (dict(tokens=None), 1), (dict(out_n=None), 1),
+    (dict(draft=None, mode=1), 1),
+    (dict(B=0), 2), (dict(K=32), 2), (dict(d=100), 2), (dict(d=0), 2), (dict(V=100), 2),
+    (dict(B=64, K=4), 2),  # 256 rows fit, 320 do not
+    (dict(ddt=4), 3), (dict(T=0.0), 4), (dict(mode=3), 8),
+    (dict(ws=None), 5), (dict(ws_bytes=1000), 5),
+    (dict(hidden=FAKE + 8), 9), (dict(W=FAKE + 2), 9), (dict(ws=FAKE + 16), 9),
+])
+def test_lmhead_host_validation(lib, kwargs, code):
+    assert lm_call(lib, **kwargs) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, FAKE, 4, 64, 8, FAKE), 1), ((FAKE, FAKE, 4, 64, 8, None), 1),
+    ((FAKE, FAKE, 0, 64, 8, FAKE), 2), ((FAKE, FAKE, 257, 64, 8, FAKE), 2),
+    ((FAKE, FAKE, 4, 96, 8, FAKE), 2), ((FAKE, FAKE, 4, 64, 12, FAKE), 2),
+    ((FAKE + 4, FAKE, 4, 64, 8, FAKE), 9), ((FAKE, FAKE, 4, 64, 8, FAKE + 2), 9),
+])
+def test_lmhead_logits_host_validation(lib, args, code):
+    assert lib.spec_lmhead_logits(*args, None) == code
