@@ -159,8 +159,9 @@ size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V);
  *   hidden and W 16-byte aligned. Greedy mode ignores draft_dtype.
  *   workspace: device buffer of at least
  *   spec_verify_lmhead_workspace_bytes(B, K, d, V) bytes, 256-byte aligned;
- *   it receives the fp32 target logits and per-tile partials and may be
- *   reused once the call's work on `stream` has completed.
+ *   it receives the fp32 target logits [B*(K+1), V] (every byte the call
+ *   reads there it wrote first, so no initial contents are needed) and may
+ *   be reused once the call's work on `stream` has completed.
  * Other arguments as in spec_verify. */
 sv_status spec_verify_lmhead(const void* hidden, const void* W,
                              const void* draft_logits,
