@@ -75,7 +75,8 @@ typedef enum {
     SV_ERR_MODE = 8,          /* unknown mode                                   */
     SV_ERR_ALIGN = 9,         /* a pointer is not aligned to its element size   */
     SV_ERR_CONFIG = 10,       /* a requested launch parameter cannot be used    */
-    SV_ERR_NOT_IMPLEMENTED = 11
+    SV_ERR_NOT_IMPLEMENTED = 11,
+    SV_ERR_SCRATCH_LIMIT = 12 /* needs more than SV_LMHEAD_SCRATCH_BYTES     */
 } sv_status;
 
 /* Bits OR-ed into the optional device status word. */
@@ -170,6 +171,39 @@ sv_status spec_verify_lmhead(const void* hidden, const void* W,
                              sv_mode mode, uint64_t seed, void* workspace,
                              size_t workspace_bytes, int32_t* out_tokens,
                              int32_t* out_n_accepted, sv_stream_t stream);
+
+/* Capacity of the library's own device scratch used by
+ * spec_verify_lmhead_noalloc: 32 MiB, i.e. B*(K+1)*V*4 <= 33554432 bytes of
+ * fp32 target logits (V = 128256 allows B*(K+1) <= 65). */
+#define SV_LMHEAD_SCRATCH_BYTES (32u << 20)
+
+/* spec_verify_lmhead without a workspace argument: it allocates nothing.
+ * The pages describe no such variant; it exists for callers that cannot
+ * allocate device memory when they verify (a C host runtime linked without
+ * an allocator of its own, or a serving loop that must not call cudaMalloc
+ * or cudaFree between steps, since either may synchronise the whole device).
+ * The target logits go to one fixed scratch array that the library's device
+ * image holds (SV_LMHEAD_SCRATCH_BYTES, 256-byte aligned, one copy per
+ * device); its address is looked up once per device with that device current.
+ *   Arguments as in spec_verify_lmhead, minus the workspace.
+ *   Nothing in the scratch needs to start at zero: the call writes every
+ *   byte it reads there before reading it.
+ *   Sizes whose logits exceed SV_LMHEAD_SCRATCH_BYTES return
+ *   SV_ERR_SCRATCH_LIMIT before any work is enqueued.
+ *   All calls on one device share the one scratch array: calls whose work
+ *   may overlap (other streams, other host threads, another call before this
+ *   one's work on `stream` has completed unless both are on the same stream)
+ *   race on it and corrupt each other's results. Order them.
+ *   The first call on each device may load the library's device image to
+ *   look the address up; make that first call outside any stream capture. */
+sv_status spec_verify_lmhead_noalloc(const void* hidden, const void* W,
+                                     const void* draft_logits,
+                                     const int32_t* draft_tokens, int B, int K,
+                                     int d, int V, sv_dtype draft_dtype,
+                                     float temperature, sv_mode mode,
+                                     uint64_t seed, int32_t* out_tokens,
+                                     int32_t* out_n_accepted,
+                                     sv_stream_t stream);
 
 /* The LM head alone: logits[M, V] = hidden[M, d] . W[d, V] with bf16 inputs
  * and fp32 accumulation on the tensor cores (the first half of

@@ -26,6 +26,8 @@ SV_FLAG_RESIDUAL_FALLBACK = 4
 SV_FLAG_DRAW_EDGE = 8
 SV_FLAG_BAD_MODE = 16
 SV_FLAG_TIMEOUT = 32
+SV_ERR_SCRATCH_LIMIT = 12
+SV_LMHEAD_SCRATCH_BYTES = 32 << 20  # include/specverify.h
 
 STATUS_NAMES = {
     0: "SV_OK", 1: "SV_ERR_NULL", 2: "SV_ERR_SHAPE", 3: "SV_ERR_DTYPE", 4: "SV_ERR_TEMPERATURE",
@@ -82,6 +84,8 @@ SIGNATURES = [
     ("spec_verify_lmhead", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I, ctypes.c_uint64, P,
                                ctypes.c_size_t, P, P, P]),
     ("spec_lmhead_logits", I, [P, P, I, I, I, P, P]),
+    ("spec_verify_lmhead_noalloc", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I,
+                                       ctypes.c_uint64, P, P, P]),
     ("sv_status_string", ctypes.c_char_p, [I]),
     ("sv_last_cuda_error", I, []),
     ("sv_version", I, []),
@@ -275,4 +279,28 @@ def spec_verify_lmhead(hidden, W, draft_logits, draft_tokens, temperature=1.0, m
             _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out_tokens),
             _ptr(out_n_accepted), _stream(stream, dev))
     _check(st, "spec_verify_lmhead")
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_lmhead_noalloc(hidden, W, draft_logits, draft_tokens, temperature=1.0,
+                               mode="sample", seed=0, out_tokens=None, out_n_accepted=None,
+                               stream=None):
+    """spec_verify_lmhead with the logits in the library's own static device
+    scratch (SV_LMHEAD_SCRATCH_BYTES): the C call allocates nothing. Calls
+    that may overlap on one device race on that scratch; order them."""
+    B, K1, d = hidden.shape
+    K = K1 - 1
+    V = W.shape[1]
+    dev = hidden.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, K1, dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    ddt = _dtype_code(draft_logits) if draft_logits is not None else SV_BF16
+    with torch.cuda.device(dev):
+        st = _load().spec_verify_lmhead_noalloc(
+            _ptr(hidden), _ptr(W), _ptr(draft_logits), _ptr(draft_tokens), B, K, d, V, ddt,
+            float(temperature), _mode_code(mode), ctypes.c_uint64(int(seed) & (2**64 - 1)),
+            _ptr(out_tokens), _ptr(out_n_accepted), _stream(stream, dev))
+    _check(st, "spec_verify_lmhead_noalloc")
     return out_tokens, out_n_accepted

@@ -167,6 +167,8 @@ extern "C" const char* sv_status_string(sv_status s) {
         case SV_ERR_ALIGN: return "pointer not aligned to its element size";
         case SV_ERR_CONFIG: return "requested launch configuration cannot be used";
         case SV_ERR_NOT_IMPLEMENTED: return "not implemented";
+        case SV_ERR_SCRATCH_LIMIT:
+            return "the logits B*(K+1)*V*4 bytes exceed the static scratch (SV_LMHEAD_SCRATCH_BYTES)";
     }
     return "unknown status";
 }
@@ -250,3 +252,60 @@ extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const
     return verify_impl(&a, SV_F32, mode == SV_SAMPLE ? draft_dtype : SV_F32);
 }
 
+// ---------------------------------------------------------------------------
+// LM-head verify with no allocation at all.
+//
+// Callers that cannot allocate device memory at verify time (a C host runtime
+// without an allocator of its own; a serving loop that avoids cudaMalloc and
+// cudaFree between steps because either may synchronise the whole device)
+// get the fp32 target logits written to this fixed array instead of a
+// workspace. It lives in this translation unit's device image, one copy per
+// device, loaded with it; no call below allocates anything.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_lmhead_scratch[SV_LMHEAD_SCRATCH_BYTES];
+
+static std::atomic<void*> g_scratch_addr[kMaxDevices];
+
+// The scratch's device address on the current device, looked up once per
+// device (with that device current) and cached.
+static sv_status scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return SV_ERR_ARCH;
+    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_lmhead_scratch);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (!p) return fail_cuda(cudaErrorInvalidSymbol);
+        g_scratch_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return SV_OK;
+}
+
+extern "C" sv_status spec_verify_lmhead_noalloc(const void* hidden, const void* W,
+                                                const void* draft_logits, const int32_t* draft_tokens,
+                                                int B, int K, int d, int V, sv_dtype draft_dtype,
+                                                float temperature, sv_mode mode, uint64_t seed,
+                                                int32_t* out_tokens, int32_t* out_n_accepted,
+                                                sv_stream_t stream) {
+    if (B < 1 || K < 1 || K > 31 || V < 1) return SV_ERR_SHAPE;
+    // B*(K+1) <= 256 is checked by the callee; bound the product here first
+    if ((long long)B * (K + 1) > 256) return SV_ERR_SHAPE;
+    if (lmhead_logits_bytes((long long)B * (K + 1), V) > (size_t)SV_LMHEAD_SCRATCH_BYTES)
+        return SV_ERR_SCRATCH_LIMIT;
+    // every other argument is validated by spec_verify_lmhead before launching;
+    // validate the cheap host-side ones first so that a bad call never loads
+    // the device image
+    sv_status st = check_lmhead_shape(hidden, W, (long long)B * (K + 1), d, V);
+    if (st != SV_OK) return st;
+    if (!draft_tokens || !out_tokens || !out_n_accepted) return SV_ERR_NULL;
+    void* scratch = nullptr;
+    int sms = 0;
+    if ((st = check_device(&sms)) != SV_OK) return st;
+    if ((st = scratch_address(&scratch)) != SV_OK) return st;
+    return spec_verify_lmhead(hidden, W, draft_logits, draft_tokens, B, K, d, V, draft_dtype,
+                              temperature, mode, seed, scratch, (size_t)SV_LMHEAD_SCRATCH_BYTES,
+                              out_tokens, out_n_accepted, stream);
+}

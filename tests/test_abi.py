@@ -58,7 +58,7 @@ def test_struct_layout_matches(lib):
     assert lib.sv_verify_args_size() == ctypes.sizeof(binding.sv_verify_args)
     assert lib.sv_version() >= 100
     assert lib.sv_status_string(0).decode() == "ok"
-    for code in range(12):
+    for code in range(13):
         assert lib.sv_status_string(code)
 
 
