@@ -468,6 +468,12 @@ def other_workloads(args, device, l2, stream):
     for name in args.also:
         if name == args.workload:
             continue
+        if name == "c5":
+            try:
+                out[name] = lmhead_workload(args, device, stream)
+            except Exception as e:  # report, do not hide
+                out[name] = {"error": repr(e)}
+            continue
         try:
             sets, set_bytes = workload_sets(name, device, l2)
             steps = max(20, min(args.steps, 200))
@@ -481,7 +487,10 @@ def other_workloads(args, device, l2, stream):
             B, K1, V = sets[0].target.shape
             gbs = ba / (ms / 1e3) / 1e9
             peak, _ = measured_peaks()
+            traffic, traffic_note = profiled_traffic(name)
             out[name] = {"workload": describe(name), "steps": steps,
+                         "traffic": traffic, "traffic_note": traffic_note,
+                         "algorithmic_bytes_per_launch": ba / steps,
                          "rows_per_s": B * K1 * steps / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
                          "hbm_gbs": gbs, "frac_of_measured_peak": gbs / peak,
                          "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
@@ -491,6 +500,87 @@ def other_workloads(args, device, l2, stream):
         except Exception as e:  # report, do not hide
             out[name] = {"error": repr(e)}
     return out
+
+
+def lmhead_workload(args, device, stream, n_sets=4):
+    """The fused LM-head workload (hidden [32, 6, 4096] bf16, W [4096, 128256]
+    bf16): spec_verify_lmhead per step, and the tensor-core GEMM alone. W
+    (1.05 GB) is far larger than L2, so every step streams it from HBM."""
+    import synth
+    from speculative_decoding_verification_24_gb300 import (spec_lmhead_logits, spec_verify_lmhead,
+                                                            spec_verify_lmhead_workspace_bytes)
+    from synth.workloads import WORKLOADS
+
+    w = WORKLOADS["c5"]
+    base = synth.make_workload("c5", seed=5, device=device)
+    sets = [base] + [synth.make_lmhead_case(B=w["B"], K=w["K"], V=w["V"], d=w["d"], seed=5 + k,
+                                            device=device) for k in range(1, n_sets)]
+    W = base.W  # one head, as in serving: the hidden states and drafts change per step
+    B, K1, d = base.hidden.shape
+    K, V = K1 - 1, W.shape[1]
+    M = B * K1
+    steps = max(20, min(args.steps, 100))
+    ws = torch.empty(spec_verify_lmhead_workspace_bytes(B, K, d, V), dtype=torch.uint8, device=device)
+    out_t = torch.empty(steps + args.warmup, B, K1, dtype=torch.int32, device=device)
+    out_n = torch.empty(steps + args.warmup, B, dtype=torch.int32, device=device)
+    logits = torch.empty(M, V, dtype=torch.float32, device=device)
+    hid2d = [c.hidden.reshape(M, d) for c in sets]
+
+    def fused(i):
+        c = sets[i % n_sets]
+        spec_verify_lmhead(c.hidden, W, c.draft, c.tokens, c.temperature, seed=i, workspace=ws,
+                           out_tokens=out_t[i], out_n_accepted=out_n[i], stream=stream)
+
+    def gemm(i):
+        spec_lmhead_logits(hid2d[i % n_sets], W, out=logits, stream=stream)
+
+    res = {"workload": "c5: fused LM head + verify, hidden [B=32, K+1=6, d=4096] bf16 ~ N(0,1), "
+                       "W [4096, 128256] bf16 ~ N(0, 0.02^2), draft = hidden.W + N(0,1) (bf16), "
+                       "T=1, sample mode",
+           "steps": steps, "l2": f"W of {d * V * 2 / 2**30:.2f} GiB streams from HBM every step; "
+                                 f"hidden and draft rotate over {n_sets} sets"}
+    timings = {}
+    for name, fn in (("fused", fused), ("gemm", gemm)):
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                fn(i)
+        torch.cuda.synchronize()
+        g = capture(fn, args.warmup, steps, stream)
+        replay_ms(g, stream)
+        timings[name] = replay_ms(g, stream) / steps
+        del g
+    peak, peak_src = measured_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_peak = float(json.load(f)["bf16_tflops"])
+        tf_src = "measured (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)"
+    except Exception:
+        tf_peak, tf_src = 1900.0, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
+    g_ms, f_ms = timings["gemm"], timings["fused"]
+    w_bytes = d * V * 2
+    io_bytes = w_bytes + M * d * 2 + M * V * 4
+    flops = 2.0 * M * d * V
+    n_all = out_n[args.warmup:args.warmup + steps].cpu().numpy()
+    res.update({
+        "rows_per_s": M / (f_ms / 1e3), "us_per_step": f_ms * 1e3,
+        "gemm_us": g_ms * 1e3, "verify_us": (f_ms - g_ms) * 1e3,
+        "mean_tokens_per_verify": float((n_all + 1).mean()),
+        "roofline": {
+            "bound": "hbm", "kernel": "sv::lmhead_gemm_kernel",
+            "achieved": w_bytes / (g_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": w_bytes / (g_ms / 1e3) / 1e9 / peak, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": w_bytes,
+            "what": "W-streaming roofline: the head's weights (d*V*2 bytes) once per launch",
+            "all_io_gbs": io_bytes / (g_ms / 1e3) / 1e9,
+        },
+        "tensor": {"achieved_tflops": flops / (g_ms / 1e3) / 1e12, "peak_tflops": tf_peak,
+                   "frac": flops / (g_ms / 1e3) / 1e12 / tf_peak, "peak_source": tf_src,
+                   "note": "M = B*(K+1) = 192 rows make the product HBM-bound by design"},
+        "gpu_launches_per_step": 2,
+    })
+    del sets, ws, logits
+    torch.cuda.empty_cache()
+    return res
 
 
 # ----------------------------------------------------------------- reference arm
@@ -541,6 +631,36 @@ def run_reference(args):
     }
 
 
+def profile_run(args, device):
+    """--profile NAME: warmup + steps eager calls of one workload and no bench
+    line, for ncu (every launch of the verify kernel, or for c5 the LM-head
+    GEMM then the verify kernel, on inputs larger than L2)."""
+    from speculative_decoding_verification_24_gb300 import (spec_verify_ex, spec_verify_lmhead,
+                                                            spec_verify_lmhead_workspace_bytes)
+    from speculative_decoding_verification_24_gb300.build import build
+
+    build()
+    n = args.warmup + args.steps
+    if args.profile == "c5":
+        import synth
+        c = synth.make_workload("c5", seed=5, device=device)
+        B, K1, d = c.hidden.shape
+        ws = torch.empty(spec_verify_lmhead_workspace_bytes(B, K1 - 1, d, c.W.shape[1]),
+                         dtype=torch.uint8, device=device)
+        for i in range(n):
+            spec_verify_lmhead(c.hidden, c.W, c.draft, c.tokens, c.temperature, seed=i, workspace=ws)
+    else:
+        props = torch.cuda.get_device_properties(device)
+        l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
+        sets, _ = workload_sets(args.profile, device, l2)
+        for i in range(n):
+            c = sets[i % len(sets)]
+            spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=uniform_mode(c.modes),
+                           seed=i)
+    torch.cuda.synchronize()
+    print(f"profile run: {args.profile}, {n} steps", flush=True)
+
+
 # ----------------------------------------------------------------- main
 
 
@@ -551,10 +671,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4"])
-    ap.add_argument("--also", default="c3,c4", help="other workloads reported as sub-results")
+    ap.add_argument("--also", default="c3,c4,c5", help="other workloads reported as sub-results")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5"],
+                    help="run warmup+steps calls of one workload for ncu; no bench line")
     args = ap.parse_args()
     args.also = [a for a in args.also.split(",") if a]
     args.warmup = max(3, args.warmup)
@@ -570,6 +692,9 @@ def main():
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.profile:
+        profile_run(args, device)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     result = run_ours(args, rank, world, device)
