@@ -67,12 +67,6 @@ __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 2^n for an integer-valued n <= 0 (or -inf), built from the exponent bits so
-// that rescaling a partial sum by it is exact; below 2^-126 it flushes to 0.
-__device__ __forceinline__ float pow2_nonpos(float n) {
-    return n < -126.0f ? 0.0f : __int_as_float(((int)n + 127) << 23);
-}
-
 __device__ __forceinline__ bool is_nan(float x) { return x != x; }
 
 // --------------------------------------------------------------------------
@@ -97,14 +91,17 @@ struct SoftPart {
     float R, s;
 };
 
+// 2^d for the integer differences d <= 0 of two partials' R (or -inf): the
+// ex2 instruction returns exact powers of two for integer arguments (checked
+// on sm_103a for every integer in [-160, 95]; below 2^-126 it flushes to 0).
+// Every step is a select, not a branch: a merge sits on the critical path of
+// the warp, CTA and cluster reductions.
 __device__ __forceinline__ SoftPart merge_soft(SoftPart a, SoftPart b) {
-    if (is_nan(a.R) || is_nan(b.R)) return SoftPart{__int_as_float(0x7fc00000), 0.0f};
-    float R = fmaxf(a.R, b.R);
-    if (R == -INFINITY) return SoftPart{-INFINITY, 0.0f};
-    if (R == INFINITY) return SoftPart{INFINITY, __int_as_float(0x7fc00000)};
-    float sa = a.R == -INFINITY ? 0.0f : a.s * pow2_nonpos(a.R - R);
-    float sb = b.R == -INFINITY ? 0.0f : b.s * pow2_nonpos(b.R - R);
-    return SoftPart{R, sa + sb};
+    const float R = fmaxf(a.R, b.R);
+    const float sa = a.R == -INFINITY ? 0.0f : a.s * ex2(a.R - R);
+    const float sb = b.R == -INFINITY ? 0.0f : b.s * ex2(b.R - R);  // +inf: inf - inf = NaN
+    const bool nan = is_nan(a.R) || is_nan(b.R);
+    return SoftPart{nan ? __int_as_float(0x7fc00000) : R, nan ? 0.0f : sa + sb};
 }
 
 // Greedy partial: the largest logit and its lowest index (NaN is sticky).
@@ -114,13 +111,66 @@ struct ArgPart {
 };
 
 __device__ __forceinline__ ArgPart merge_arg(ArgPart a, ArgPart b) {
-    bool an = is_nan(a.v), bn = is_nan(b.v);
-    if (an || bn) {
-        if (an && bn) return a.i <= b.i ? a : b;
-        return an ? a : b;
-    }
-    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
-    return a;
+    const bool an = is_nan(a.v), bn = is_nan(b.v);
+    const bool take_b = bn ? (!an || b.i < a.i) : (!an && (b.v > a.v || (b.v == a.v && b.i < a.i)));
+    return take_b ? b : a;
+}
+
+// --------------------------------------------------------------------------
+// Float-float sums (hi + lo, about 48 significant bits) for the draw's
+// cumulative masses: the same role double would play, at fp32 latency (fp64
+// is a slow, long-latency path on this part).
+// --------------------------------------------------------------------------
+struct ff {
+    float hi, lo;
+};
+
+__device__ __forceinline__ ff ff_from(float x) { return ff{x, 0.0f}; }
+
+// s + e = a + b exactly (Knuth's two-sum).
+__device__ __forceinline__ ff two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return ff{s, e};
+}
+
+// Renormalise hi + lo with |hi| >= |lo| (Dekker's fast two-sum).
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    return ff{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    const ff s = two_sum(a.hi, b.hi);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ ff ff_add(ff a, float b) { return ff_add(a, ff{b, 0.0f}); }
+
+__device__ __forceinline__ ff ff_neg(ff a) { return ff{-a.hi, -a.lo}; }
+
+// a * u for a float u.
+__device__ __forceinline__ ff ff_mul(ff a, float u) {
+    const float p = __fmul_rn(a.hi, u);
+    const float e = __fmaf_rn(a.hi, u, -p);
+    return fast_two_sum(p, __fmaf_rn(a.lo, u, e));
+}
+
+// a > b, decided on the float-float difference.
+__device__ __forceinline__ bool ff_gt(ff a, ff b) {
+    const ff d = ff_add(a, ff_neg(b));
+    return d.hi > 0.0f || (d.hi == 0.0f && d.lo > 0.0f);
+}
+
+__device__ __forceinline__ ff ff_shfl_xor(ff a, int o) {
+    return ff{__shfl_xor_sync(0xFFFFFFFFu, a.hi, o), __shfl_xor_sync(0xFFFFFFFFu, a.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl_up(ff a, int o) {
+    return ff{__shfl_up_sync(0xFFFFFFFFu, a.hi, o), __shfl_up_sync(0xFFFFFFFFu, a.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl(ff a, int l) {
+    return ff{__shfl_sync(0xFFFFFFFFu, a.hi, l), __shfl_sync(0xFFFFFFFFu, a.lo, l)};
 }
 
 // Rows of one sequence share one 8-byte slot per row in shared memory; the

@@ -195,29 +195,31 @@ __device__ __forceinline__ WarpSlots warp_slots(const RowGeom& g, int V, int qa,
     return w;
 }
 
-// NaN-propagating maximum of the valid elements of U slots.
+// NaN-propagating maximum of the valid elements of U slots, as a tree (the
+// dependent chain is log2 of the element count long).
 template <typename T, int U>
 __device__ __forceinline__ float group_max(const uint4 (&d)[U]) {
     if constexpr (sizeof(T) == 2) {
-        uint32_t m = Elem<T>::NEG_INF;
+        uint32_t m[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            m = max_nan_bf16x2(m, d[u].x);
-            m = max_nan_bf16x2(m, d[u].y);
-            m = max_nan_bf16x2(m, d[u].z);
-            m = max_nan_bf16x2(m, d[u].w);
-        }
-        return max_nan(bf16_lo(m), bf16_hi(m));
+        for (int u = 0; u < U; ++u)
+            m[u] = max_nan_bf16x2(max_nan_bf16x2(d[u].x, d[u].y), max_nan_bf16x2(d[u].z, d[u].w));
+#pragma unroll
+        for (int st = 1; st < U; st *= 2)
+#pragma unroll
+            for (int u = 0; u + st < U; u += 2 * st) m[u] = max_nan_bf16x2(m[u], m[u + st]);
+        return max_nan(bf16_lo(m[0]), bf16_hi(m[0]));
     } else {
-        float m = -INFINITY;
+        float m[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            m = max_nan(m, __uint_as_float(d[u].x));
-            m = max_nan(m, __uint_as_float(d[u].y));
-            m = max_nan(m, __uint_as_float(d[u].z));
-            m = max_nan(m, __uint_as_float(d[u].w));
-        }
-        return m;
+        for (int u = 0; u < U; ++u)
+            m[u] = max_nan(max_nan(__uint_as_float(d[u].x), __uint_as_float(d[u].y)),
+                           max_nan(__uint_as_float(d[u].z), __uint_as_float(d[u].w)));
+#pragma unroll
+        for (int st = 1; st < U; st *= 2)
+#pragma unroll
+            for (int u = 0; u + st < U; u += 2 * st) m[u] = max_nan(m[u], m[u + st]);
+        return m[0];
     }
 }
 
@@ -270,7 +272,7 @@ __device__ __forceinline__ void soft_group(SoftAcc& a, const uint4 (&d)[U], floa
     constexpr int PAIRS = Elem<T>::E / 2;
     const float m = group_max<T, U>(d);
     const float Rn = max_nan(a.R, ceilf(m * c));
-    const float sc = pow2_nonpos(fmaxf(a.R - Rn, -1000.0f));  // NaN (-inf - -inf) -> 0
+    const float sc = ex2(fmaxf(a.R - Rn, -1000.0f));  // exact 2^n; NaN (-inf - -inf) -> 0
     const f32x2 sc2 = pack2(sc, sc);
     a.a0 = mul2(a.a0, sc2);
     a.a1 = mul2(a.a1, sc2);
@@ -328,7 +330,6 @@ constexpr int NBUF = 3;                         // stages per warp
 constexpr int NSTAGE = NBUF * NCW;              // warp w owns stages w, w + NCW, w + 2 NCW
 constexpr int RING_BYTES = STAGE_BYTES * NSTAGE;
 constexpr int STAGE_SLOTS = STAGE_BYTES / 16;   // slots per pass-1 chunk (256)
-constexpr int LANE_SLOTS = 4;                   // slots per lane per reduction step
 constexpr int P2_SLOTS = STAGE_SLOTS / 2;       // target slots per pass-2 chunk (128)
 constexpr int P2_DRAFT_OFF = P2_SLOTS * 16;     // draft half of a pass-2 stage
 constexpr int MAX_P2_CHUNKS = 256;              // per CTA slice of one row
@@ -336,15 +337,19 @@ constexpr int MAX_CS = 16;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;       // polls before a wait gives up
 
 // One row of the sequence as this CTA sees it: the 16-byte slots of its slice,
-// split into the full interior [ia, ib) and the partial end slots; `pre` is
-// the number of interior slots of the rows before it (the pass-1 schedule
-// concatenates every row's interior slots and cuts them into chunks).
+// split into the full interior [ia, ib) and the partial end slots. The pass-1
+// schedule cuts every row's interior into chunks of STAGE_SLOTS slots (the
+// last one of a row may be shorter) and numbers them row after row: row r
+// owns chunks [c1 of row r - 1 (0 for row 0), c1), its k-th chunk holding
+// slots ia + k * STAGE_SLOTS ...
 struct RowInfo {
     const uint4* base;  // 16-byte aligned address of slot 0
     int head;           // elements between base and the row's first element
     int ia, ib, edge_lo, edge_hi;
-    int pre;
+    int c1;
 };
+
+__device__ __forceinline__ int row_c0(const RowInfo* rows, int r) { return r == 0 ? 0 : rows[r - 1].c1; }
 
 // Row r of sequence b: target row r (r <= K) or draft row r - K - 1.
 template <typename TT>
@@ -384,29 +389,6 @@ __device__ __forceinline__ RowInfo make_row_info(const T* row, int V, int rank, 
     split_range(g.nslot, rank, CS, qa, qb);
     const WarpSlots sl = warp_slots<T>(g, V, qa, qb);
     return RowInfo{g.base, g.head, sl.ia, sl.ib, sl.edge_lo, sl.edge_hi, 0};
-}
-
-// Pieces of pass-1 chunk c: global schedule slots [c * STAGE_SLOTS, end) split
-// at row boundaries. `r` is a running row cursor (chunks are visited in
-// order); next_piece returns false once the chunk is exhausted.
-struct PieceIter {
-    int r;       // current row
-    int g;       // next global schedule slot
-    int end;     // end of this chunk in schedule slots
-};
-
-__device__ __forceinline__ bool next_piece(PieceIter& it, const RowInfo* rows, int& row, int& q0,
-                                           int& n, int& off, int chunk_start) {
-    if (it.g >= it.end) return false;
-    while (rows[it.r].pre + (rows[it.r].ib - rows[it.r].ia) <= it.g) ++it.r;  // skip finished rows
-    const RowInfo& ri = rows[it.r];
-    const int row_end = ri.pre + (ri.ib - ri.ia);
-    row = it.r;
-    q0 = ri.ia + (it.g - ri.pre);
-    n = min(it.end, row_end) - it.g;
-    off = it.g - chunk_start;
-    it.g += n;
-    return true;
 }
 
 struct DrawRows {
@@ -487,10 +469,11 @@ __device__ __forceinline__ void load_draw_slot(const DrawSrc<TT, TD>& src, bool 
 // element index. The summation order matches the pass-2 totals.
 template <typename TT, typename TD>
 __device__ int warp_draw_search(const DrawSrc<TT, TD>& src, const DrawRows& w, int q_begin, int n,
-                                double tw, int lane) {
+                                ff tw, int lane) {
     using T = TT;
     constexpr int E = Elem<T>::E, BATCH = 4;
-    double run = 0.0;
+    const bool tw_inf = isinf(tw.hi);
+    ff run = ff_from(0.0f);
     int last_pos = -1;
     for (int k0 = 0; k0 < n; k0 += 32 * BATCH) {
         uint4 dt[BATCH], dd[BATCH];
@@ -514,30 +497,52 @@ __device__ int warp_draw_search(const DrawSrc<TT, TD>& src, const DrawRows& w, i
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
             if (lp >= 0) last_pos = lp;
-            const unsigned hit = __ballot_sync(FULL, run + (double)incl > tw);
+            const unsigned hit = __ballot_sync(FULL, !tw_inf && ff_gt(ff_add(run, incl), tw));
             if (hit) {
                 const int l = __ffs(hit) - 1;
                 int tok = -1;
                 if (lane == l) {
-                    double cum = run + (double)(l == 0 ? 0.0f : prev);
+                    ff cum = ff_add(run, l == 0 ? 0.0f : prev);
                     int lastp = -1;
 #pragma unroll
                     for (int e = 0; e < E; ++e) {
                         const float r = draw_mass(w, elem<T>(dt[k], e), elem<T>(dd[k], e));
                         if (r > 0.0f) {
                             lastp = i0 + e;
-                            cum += (double)r;
-                            if (tok < 0 && cum > tw) tok = i0 + e;
+                            cum = ff_add(cum, r);
+                            if (tok < 0 && ff_gt(cum, tw)) tok = i0 + e;
                         }
                     }
                     if (tok < 0) tok = lastp;  // rounding put tw past this lane's last mass
                 }
                 return __shfl_sync(FULL, tok, l);
             }
-            run += (double)__shfl_sync(FULL, incl, 31);
+            run = ff_add(run, __shfl_sync(FULL, incl, 31));
         }
     }
     return last_pos;
+}
+
+// The accept test u * P_d(x) < P_t(x) with P = e / S, i.e. u * e_d * S_t <
+// e_t * S_d, decided as if in exact arithmetic on these float inputs. The
+// float products carry relative errors below 2^-23 (left, two roundings) and
+// 2^-24 (right) while they stay far above the float underflow range; outside
+// a 2^-21 band around equality they decide it, inside it (or near underflow)
+// the products are formed in double, where u * e_d and e_t * S_d are exact.
+__device__ __noinline__ bool accept_draft_exact(float u, float ed, float St, float et, float Sd) {
+    return (double)u * (double)ed * (double)St < (double)et * (double)Sd;
+}
+
+__device__ __forceinline__ bool accept_draft(float u, float ed, float St, float et, float Sd) {
+    const float ue = u * ed;
+    const float l = ue * St, r = et * Sd;
+    const float tiny = 0x1p-100f;
+    const bool normal = ue >= tiny && l >= tiny && r >= tiny;
+    const bool sure_accept = normal && l < r * (1.0f - 0x1p-21f);
+    const bool sure_reject = normal && l > r * (1.0f + 0x1p-21f);
+    if (sure_accept) return true;
+    if (sure_reject) return false;
+    return accept_draft_exact(u, ed, St, et, Sd);
 }
 
 // ---------------------------------------------------------------------------
@@ -554,15 +559,20 @@ struct SeqShared {
     float p2_edge[2];
     int x_tok[MAX_K];                   // draft tokens, and the logits at them
     float lt_x[MAX_K], ld_x[MAX_K];     // (prefetched at the start)
-    double gathered_tot[2][MAX_CS];     // every CTA's draw mass, pushed by their owners
+    float2 gathered_tot[2][MAX_CS];     // every CTA's draw mass (float-float), pushed by their owners
+    float u_pos[MAX_K + 1], u2_pos[MAX_K + 1];  // Philox uniforms of positions 0..K
     // decision (identical in every CTA of the cluster)
     int j, valid, sample, use_d, err;
     float u2;
     SoftPart st, sd;
-    double total, tc;
+    ff total, tc;
     int cstar;
-    int total_slots;
+    int total_chunks;
 };
+
+// Two CTAs per SM: 2 x (ring + this + 1 KB reserved) within 228 KB.
+static_assert(2 * (RING_BYTES + sizeof(SeqShared) + 1024) <= 228 * 1024,
+              "shared state too large for two CTAs per SM");
 
 // The NBUF ring stages a warp owns (w, w + NCW, ...). Chunk number `seq` of
 // this warp (counted over both passes) lives in stage seq % NBUF and is that
@@ -615,66 +625,90 @@ __device__ __forceinline__ void flush_row(SeqShared& sh, int warp, int lane, int
 
 constexpr int CHUNK_LANE_SLOTS = STAGE_SLOTS / 32;  // 8 slots per lane
 
+// A chunk of one row held by a lane: slot u of d is chunk slot u * 32 + lane,
+// valid below n; q0 is the row slot of chunk slot 0. Reduced in groups of
+// GROUP_SLOTS slots per lane.
+constexpr int GROUP_SLOTS = 4;
+
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ void reduce_piece(SoftAcc& sa, ArgPart& ag, const uint4 (&d)[CHUNK_LANE_SLOTS],
-                                             int off, int n, int q0, int head, float c, int lane,
-                                             bool whole) {
+__device__ __forceinline__ void reduce_chunk(SoftAcc& sa, ArgPart& ag, const uint4 (&d)[CHUNK_LANE_SLOTS],
+                                             int n, int q0, int head, float c, int lane) {
+    const bool whole = n == STAGE_SLOTS;
 #pragma unroll
-    for (int g = 0; g < CHUNK_LANE_SLOTS / LANE_SLOTS; ++g) {
-        uint4 x[LANE_SLOTS];
-        int qs[LANE_SLOTS];
+    for (int g = 0; g < CHUNK_LANE_SLOTS / GROUP_SLOTS; ++g) {
+        uint4 x[GROUP_SLOTS];
+        int qs[GROUP_SLOTS];
 #pragma unroll
-        for (int u = 0; u < LANE_SLOTS; ++u) {
-            const int i = (g * LANE_SLOTS + u) * 32 + lane;  // slot of the chunk
-            x[u] = (whole || (i >= off && i < off + n)) ? d[g * LANE_SLOTS + u] : neg_inf_slot<T>();
-            qs[u] = q0 + (i - off);
+        for (int u = 0; u < GROUP_SLOTS; ++u) {
+            const int i = (g * GROUP_SLOTS + u) * 32 + lane;
+            x[u] = (whole || i < n) ? d[g * GROUP_SLOTS + u] : neg_inf_slot<T>();
+            qs[u] = q0 + i;
         }
-        if (SAMPLE) soft_group<T, LANE_SLOTS>(sa, x, c);
-        else arg_group<T, LANE_SLOTS>(ag, x, qs, head);
+        if (SAMPLE) soft_group<T, GROUP_SLOTS>(sa, x, c);
+        else arg_group<T, GROUP_SLOTS>(ag, x, qs, head);
     }
 }
 
-// Issues the bulk copies of pass-1 chunk `chunk` into stage b (lane 0 issues,
-// every lane walks the pieces with the row cursor `r`).
+// The row of pass-1 chunk `chunk` for a warp that visits chunks in order.
+struct RowCursor {
+    int r, c0, c1;
+};
+
+__device__ __forceinline__ void seek_row(RowCursor& rc, const RowInfo* rows, int chunk) {
+    while (chunk >= rc.c1) {  // rows with no chunk of their own are skipped
+        ++rc.r;
+        rc.c0 = rc.c1;
+        rc.c1 = rows[rc.r].c1;
+    }
+}
+
+// Issues the bulk copy of pass-1 chunk `chunk` (one piece of one row) as fill
+// `fseq` of the warp; lane 0 issues.
 __device__ __forceinline__ void fill_pass1(SeqShared& sh, WarpRing& wr, char* ring, uint32_t fseq, int chunk,
-                                           int total_slots, int& r, int lane) {
-    const int cstart = chunk * STAGE_SLOTS;
-    const int cend = min(cstart + STAGE_SLOTS, total_slots);
-    wr.begin_fill(sh, fseq, (uint32_t)(cend - cstart) * 16u, lane);
-    char* stage = wr.stage(ring, fseq);
-    int g = cstart;
-    while (g < cend) {
-        while (sh.rows[r].pre + (sh.rows[r].ib - sh.rows[r].ia) <= g) ++r;
-        const RowInfo& ri = sh.rows[r];
-        const int n = min(cend, ri.pre + (ri.ib - ri.ia)) - g;
-        if (lane == 0)
-            bulk_g2s(stage + (g - cstart) * 16, ri.base + ri.ia + (g - ri.pre), (uint32_t)n * 16u,
-                     wr.bar(sh, fseq));
-        g += n;
-    }
+                                           RowCursor& rc, int lane) {
+    seek_row(rc, sh.rows, chunk);
+    const RowInfo& ri = sh.rows[rc.r];
+    const int q0 = ri.ia + (chunk - rc.c0) * STAGE_SLOTS;
+    const int n = min(STAGE_SLOTS, ri.ib - q0);
+    wr.begin_fill(sh, fseq, (uint32_t)n * 16u, lane);
+    if (lane == 0) bulk_g2s(wr.stage(ring, fseq), ri.base + q0, (uint32_t)n * 16u, wr.bar(sh, fseq));
 }
 
-// The logit at the draft token of row r, if this piece of the row holds it,
-// read from the stage before it is refilled: lane 0 writes it into every CTA
-// of the cluster (exactly one CTA's slice holds any given element, so each
-// value has one writer). Row r is target row r (r < K) or draft row r - K - 1;
-// row K has no draft token. x_reg: lane i holds draft token x_i.
+// Where the draft token of row r lies in this CTA's pass-1 chunks: the chunk
+// (or -1 when the token is not in the row's interior slots here), the byte
+// offset of its element in the stage, and the token's position i. Row r is
+// target row r (r < K) or draft row r - K - 1; row K has no draft token.
+// x_reg: lane i holds draft token x_i. Called by the whole warp.
+struct TokenSpot {
+    int chunk, byte, i;
+};
+
+template <typename T>
+__device__ __forceinline__ TokenSpot token_spot(const RowInfo& ri, int r, int K, int x_reg, int c0) {
+    constexpr int E = Elem<T>::E;
+    TokenSpot ts{-1, 0, -1};
+    if (r == K) return ts;
+    ts.i = r < K ? r : r - K - 1;
+    const int x = __shfl_sync(FULL, x_reg, ts.i);
+    if (x < 0) return ts;  // an invalid token (caught in the decision)
+    const int slot = (x + ri.head) / E;
+    if (slot < ri.ia || slot >= ri.ib) return ts;
+    ts.chunk = c0 + (slot - ri.ia) / STAGE_SLOTS;
+    ts.byte = ((slot - ri.ia) % STAGE_SLOTS) * 16 + ((x + ri.head) % E) * (int)sizeof(T);
+    return ts;
+}
+
+// Lane 0 writes the logit at ts into every CTA of the cluster (exactly one
+// CTA's slice holds any given element, so each value has one writer).
 template <typename T>
 __device__ __forceinline__ void capture_logit(SeqShared& sh, cg::cluster_group& cluster, int CS,
-                                              const char* stage, int r, int K, int x_reg, int q0,
-                                              int n, int off, int head, int lane) {
-    constexpr int E = Elem<T>::E;
-    if (r == K) return;
-    const int i = r < K ? r : r - K - 1;
-    const int x = __shfl_sync(FULL, x_reg, i);
-    const int slot = (x + head) / E;  // x + head >= 0 for a valid token
-    if (lane != 0 || x < 0 || slot < q0 || slot >= q0 + n) return;
-    const char* at = stage + (slot - q0 + off) * 16 + ((x + head) % E) * (int)sizeof(T);
+                                              const char* stage, const TokenSpot& ts, int K, int r) {
+    const char* at = stage + ts.byte;
     float v;
     if constexpr (sizeof(T) == 4) v = *reinterpret_cast<const float*>(at);
     else v = __uint_as_float((uint32_t)(*reinterpret_cast<const unsigned short*>(at)) << 16);
     float* dst = r < K ? sh.lt_x : sh.ld_x;
-    for (int cr = 0; cr < CS; ++cr) cluster.map_shared_rank(dst, cr)[i] = v;
+    for (int cr = 0; cr < CS; ++cr) cluster.map_shared_rank(dst, cr)[ts.i] = v;
 }
 
 // As capture_logit for the partial edge slots: each lane holds one slot q
@@ -695,65 +729,59 @@ __device__ __forceinline__ void capture_edge_logit(SeqShared& sh, cg::cluster_gr
 
 // Pass 1 of one warp: chunks warp, warp + NCW, ... of the schedule, buffered
 // in the warp's NBUF stages. Writes one partial per row it saw.
-template <typename TT, typename TD, bool SAMPLE>
-__device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* ring, int total_slots,
+template <typename TT, typename TD, bool SAMPLE, typename WhileWaiting>
+__device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* ring, int nchunks,
                                              float c, int warp, int lane, uint32_t& seq,
-                                             cg::cluster_group& cluster, int CS, int K, int x_reg) {
-    const int nchunks = (total_slots + STAGE_SLOTS - 1) / STAGE_SLOTS;
-    int r_fill = 0, r_proc = 0;
+                                             cg::cluster_group& cluster, int CS, int K, int x_reg,
+                                             WhileWaiting&& while_waiting) {
+    RowCursor fill_rc{-1, 0, 0}, rc{-1, 0, 0};
     for (int j = 0; j < NBUF; ++j) {
         const int chunk = warp + NCW * j;
-        if (chunk < nchunks) fill_pass1(sh, wr, ring, seq + j, chunk, total_slots, r_fill, lane);
+        if (chunk < nchunks) fill_pass1(sh, wr, ring, seq + j, chunk, fill_rc, lane);
     }
-    int cur_row = -1;
+    while_waiting();  // work that fits in the first copies' latency
+    int cur_row = -1, ia = 0, ib = 0, head = 0;
+    TokenSpot ts{-1, 0, -1};
     SoftAcc sa = soft_acc_empty();
     ArgPart ag{-INFINITY, INT_MAX};
     for (int chunk = warp; chunk < nchunks; chunk += NCW, ++seq) {
+        seek_row(rc, sh.rows, chunk);
+        if (rc.r != cur_row) {  // a new row: flush the last one, look the new one up once
+            if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
+            sa = soft_acc_empty();
+            ag = ArgPart{-INFINITY, INT_MAX};
+            cur_row = rc.r;
+            const RowInfo ri = sh.rows[cur_row];
+            ia = ri.ia;
+            ib = ri.ib;
+            head = ri.head;
+            if (SAMPLE)
+                ts = (std::is_same<TT, TD>::value || cur_row <= K) ? token_spot<TT>(ri, cur_row, K, x_reg, rc.c0)
+                                                                  : token_spot<TD>(ri, cur_row, K, x_reg, rc.c0);
+        }
         if (!wr.wait(sh, seq)) {
             atomicExch(&sh.err, 1);
             break;
         }
-        const int cstart = chunk * STAGE_SLOTS;
-        const int cend = min(cstart + STAGE_SLOTS, total_slots);
+        const int q0 = ia + (chunk - rc.c0) * STAGE_SLOTS;
+        const int n = min(STAGE_SLOTS, ib - q0);
         const char* stage = wr.stage(ring, seq);
         uint4 d[CHUNK_LANE_SLOTS];
 #pragma unroll
         for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) {
             const int i = u * 32 + lane;
-            d[u] = i < cend - cstart ? lds128(stage + i * 16) : neg_inf_slot<TT>();
+            d[u] = i < n ? lds128(stage + i * 16) : neg_inf_slot<TT>();
         }
-        if (SAMPLE) {
-            PieceIter ic{r_proc, cstart, cend};
-            int row, q0, n, off;
-            while (next_piece(ic, sh.rows, row, q0, n, off, cstart)) {
-                if (row <= K) capture_logit<TT>(sh, cluster, CS, stage, row, K, x_reg, q0, n, off, sh.rows[row].head, lane);
-                else capture_logit<TD>(sh, cluster, CS, stage, row, K, x_reg, q0, n, off, sh.rows[row].head, lane);
-            }
+        if (SAMPLE && chunk == ts.chunk && lane == 0) {
+            if (std::is_same<TT, TD>::value || cur_row <= K) capture_logit<TT>(sh, cluster, CS, stage, ts, K, cur_row);
+            else capture_logit<TD>(sh, cluster, CS, stage, ts, K, cur_row);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (chunk + NBUF * NCW < nchunks)
-            fill_pass1(sh, wr, ring, seq + NBUF, chunk + NBUF * NCW, total_slots, r_fill, lane);
-        PieceIter it{r_proc, cstart, cend};
-        int row, q0, n, off;
-        while (next_piece(it, sh.rows, row, q0, n, off, cstart)) {
-            if (row != cur_row) {
-                if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
-                sa = soft_acc_empty();
-                ag = ArgPart{-INFINITY, INT_MAX};
-                cur_row = row;
-            }
-            const bool whole = off == 0 && n == STAGE_SLOTS;
-            const int head = sh.rows[row].head;
-            if (std::is_same<TT, TD>::value || row <= K) {
-                if (whole) reduce_piece<TT, SAMPLE>(sa, ag, d, 0, n, q0, head, c, lane, true);
-                else reduce_piece<TT, SAMPLE>(sa, ag, d, off, n, q0, head, c, lane, false);
-            } else {
-                if (whole) reduce_piece<TD, SAMPLE>(sa, ag, d, 0, n, q0, head, c, lane, true);
-                else reduce_piece<TD, SAMPLE>(sa, ag, d, off, n, q0, head, c, lane, false);
-            }
-        }
-        r_proc = it.r;
+            fill_pass1(sh, wr, ring, seq + NBUF, chunk + NBUF * NCW, fill_rc, lane);
+        if (std::is_same<TT, TD>::value || cur_row <= K) reduce_chunk<TT, SAMPLE>(sa, ag, d, n, q0, head, c, lane);
+        else reduce_chunk<TD, SAMPLE>(sa, ag, d, n, q0, head, c, lane);
     }
     if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
 }
@@ -847,7 +875,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) mbar_init(&sh.full[s], 1);
         sh.err = 0;
-        sh.total_slots = 0;
+        sh.total_chunks = 0;
         fence_barrier_init();
     }
     if (mode_ok && tid < nrows)
@@ -859,24 +887,24 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     }
     __syncthreads();
     if (mode_ok && warp == 0) {
-        // prefix sums of the rows' interior slot counts (the pass-1 schedule)
+        // prefix sums of the rows' chunk counts (the pass-1 schedule)
         int cnt = 0;
         for (int r0 = 0; r0 < nrows; r0 += 32) {
             const int r = r0 + lane;
-            const int m = r < nrows ? sh.rows[r].ib - sh.rows[r].ia : 0;
+            const int m = r < nrows ? (sh.rows[r].ib - sh.rows[r].ia + STAGE_SLOTS - 1) / STAGE_SLOTS : 0;
             int incl = m;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(FULL, incl, o);
                 if (lane >= o) incl += y;
             }
-            if (r < nrows) sh.rows[r].pre = cnt + incl - m;
+            if (r < nrows) sh.rows[r].c1 = cnt + incl;
             cnt += __shfl_sync(FULL, incl, 31);
         }
-        if (lane == 0) sh.total_slots = cnt;
+        if (lane == 0) sh.total_chunks = cnt;
     }
     __syncthreads();
-    const int total_slots = mode_ok ? sh.total_slots : 0;
+    const int total_chunks = mode_ok ? sh.total_chunks : 0;
 
     WarpRing wr{warp, 0u, 0u};
     uint32_t seq = 0;  // chunks this warp has handled, over both passes
@@ -885,9 +913,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const int x_reg = lane < K ? __ldg(p.tokens + (size_t)b * K + lane) : -1;
 
     // ---------------- pass 1: row partials over this CTA's slice ----------------
+    // Warp 0 draws the Philox uniforms of positions 0..K while its first
+    // copies are in flight; the decision reads them from shared memory.
+    const uint64_t seqid = (sample && warp == 0 && p.seq_ids) ? __ldg(p.seq_ids + b) : (uint64_t)b;
+    auto draw_uniforms = [&] {
+        if (warp == 0 && lane <= K) position_uniforms(p.seed, seqid, (uint32_t)lane, sh.u_pos[lane], sh.u2_pos[lane]);
+    };
     if (mode_ok) {
-        if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
-        else stream_pass1<TT, TD, false>(sh, wr, ring, total_slots, c, warp, lane, seq, cluster, CS, K, x_reg);
+        if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, K, x_reg, draw_uniforms);
+        else stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, K, x_reg, [] {});
         if (warp == 0) {
             if (sample) edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
             else edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
@@ -907,18 +941,32 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     }
     cluster.sync();
 
+    // Every row's CS partials merge in a butterfly over lanes: lane (r, cr) of
+    // a row group holds CTA cr's partial of row r. The merge is symmetric, so
+    // every CTA (and every lane) obtains the same bits.
+    if (mode_ok) {
+        const int rows_per_pass = 32 / CS;
+        const int r_in = lane / CS, cr = lane % CS;
+        const float2 empty = sample ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+        for (int r0 = warp * rows_per_pass; r0 < nrows; r0 += NCW * rows_per_pass) {
+            const int r = r0 + r_in;
+            float2 acc = r < nrows ? sh.gathered[cr][r] : empty;
+            for (int o = CS >> 1; o > 0; o >>= 1) {
+                const float2 other = make_float2(__shfl_xor_sync(FULL, acc.x, o), __shfl_xor_sync(FULL, acc.y, o));
+                acc = sample ? pack(merge_soft(as_soft(acc), as_soft(other)))
+                             : pack(merge_arg(as_arg(acc), as_arg(other)));
+            }
+            if (cr == 0 && r < nrows) sh.merged[r] = acc;
+        }
+    }
+    __syncthreads();
+
     // ---------------- decide (redundantly in every CTA) ----------------
     if (warp == 0) {
         bool bad = !mode_ok;
         if (mode_ok) {
             for (int r = lane; r < nrows; r += 32) {
-                float2 acc = sh.gathered[0][r];
-                for (int cr = 1; cr < CS; ++cr) {
-                    const float2 o = sh.gathered[cr][r];
-                    acc = sample ? pack(merge_soft(as_soft(acc), as_soft(o)))
-                                 : pack(merge_arg(as_arg(acc), as_arg(o)));
-                }
-                sh.merged[r] = acc;
+                const float2 acc = sh.merged[r];
                 if (sample) {
                     const SoftPart sp = as_soft(acc);
                     bad |= !(isfinite(sp.R) && isfinite(sp.s) && sp.s > 0.0f);
@@ -928,13 +976,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 }
             }
         }
-        __syncwarp();
-        const uint64_t seqid = p.seq_ids ? __ldg(p.seq_ids + b) : (uint64_t)b;
         float u = 0.0f, u2 = 0.0f;
-        if (lane <= K) position_uniforms(p.seed, seqid, (uint32_t)lane, u, u2);
+        if (sample && lane <= K) {
+            u = sh.u_pos[lane];
+            u2 = sh.u2_pos[lane];
+        }
         int x = -1;
         bool bad_token = false, rej = false;
-        float pt = __int_as_float(0x7fc00000), pd = pt;
+        float et = 0.0f, ed = 0.0f, St = 1.0f, Sd = 1.0f;
         if (lane < K) {
             x = x_reg;
             bad_token = x < 0 || x >= V;
@@ -945,14 +994,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                     const SoftPart st = as_soft(sh.merged[lane]);
                     const SoftPart sd = as_soft(sh.merged[K + 1 + lane]);
                     // the logits at x, captured during pass 1 by the CTA holding them
-                    const float lt = sh.lt_x[lane];
-                    const float ld = sh.ld_x[lane];
-                    const float et = ex2(fmaf(lt, c, -st.R));
-                    const float ed = ex2(fmaf(ld, c, -sd.R));
-                    pt = et / st.s;
-                    pd = ed / sd.s;
-                    // u * P_d(x) < P_t(x)  <=>  u * e_d * S_t < e_t * S_d
-                    rej = !((double)u * (double)ed * (double)st.s < (double)et * (double)sd.s);
+                    et = ex2(fmaf(sh.lt_x[lane], c, -st.R));
+                    ed = ex2(fmaf(sh.ld_x[lane], c, -sd.R));
+                    St = st.s;
+                    Sd = sd.s;
+                    rej = !accept_draft(u, ed, St, et, Sd);
                 }
             }
         }
@@ -984,8 +1030,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             if (lane == 0) p.out_n_accepted[b] = invalid ? -1 : j;
             if (lane < K) {
                 const float qnan = __int_as_float(0x7fc00000);
-                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = (sample && !invalid) ? pt : qnan;
-                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = (sample && !invalid) ? pd : qnan;
+                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = (sample && !invalid) ? et / St : qnan;
+                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = (sample && !invalid) ? ed / Sd : qnan;
             }
             if (lane == 0 && (!sample || invalid) && p.out_residual_mass)
                 p.out_residual_mass[b] = __int_as_float(0x7fc00000);
@@ -1026,38 +1072,61 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const int n_chunks = (sl.ib - sl.ia + P2_SLOTS - 1) / P2_SLOTS;
     constexpr int STEPS = P2_SLOTS / 32;
 
+    // When pass 1's chunks all fit the ring (none was refilled), chunk c still
+    // sits in stage c, so row r's interior slot q is at ring + 16 (c0 *
+    // STAGE_SLOTS + q - ia): row j's slices are read back from shared memory
+    // instead of HBM.
+    const RowInfo rt = sh.rows[j];
+    const bool resident_t = total_chunks <= NSTAGE && rt.ia == sl.ia && rt.ib == sl.ib;
+    const int rd_row = sh.use_d ? K + 1 + j : j;
+    const RowInfo rd = sh.rows[rd_row];
+    const int rt_c0 = row_c0(sh.rows, j), rd_c0 = row_c0(sh.rows, rd_row);
+    const bool resident_d = resident_t && draft_in_ring && rd.ia == sl.ia && rd.ib == sl.ib;
     int attempt = 0;
     for (;; ++attempt) {
         w.use_d = sh.use_d && attempt == 0;
         const bool ring_d = w.use_d && draft_in_ring;
+        const bool resident = resident_t && (!ring_d || resident_d);
         if (!sh.err) {
-            for (int jj = 0; jj < NBUF; ++jj) {
+            for (int jj = 0; !resident && jj < NBUF; ++jj) {
                 const int ci = warp + NCW * jj;
                 if (ci < n_chunks) fill_pass2<TT, TD>(sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, lane);
             }
-            for (int ci = warp; ci < n_chunks; ci += NCW, ++seq) {
-                if (!wr.wait(sh, seq)) {
-                    atomicExch(&sh.err, 1);
-                    break;
-                }
+            for (int ci = warp; ci < n_chunks; ci += NCW) {
                 const int q = sl.ia + ci * P2_SLOTS;
                 const int n = min(P2_SLOTS, sl.ib - q);
-                const char* stage = wr.stage(ring, seq);
                 uint4 dt[STEPS], dd[STEPS];
+                if (resident) {
+                    const char* res_t = ring + (size_t)(rt_c0 * STAGE_SLOTS + ci * P2_SLOTS) * 16;
+                    const char* res_d = ring + (size_t)(rd_c0 * STAGE_SLOTS + ci * P2_SLOTS) * 16;
 #pragma unroll
-                for (int kk = 0; kk < STEPS; ++kk) {
-                    const int i = kk * 32 + lane;
-                    dt[kk] = neg_inf_slot<TT>();
-                    dd[kk] = neg_inf_slot<TT>();
-                    if (i < n) {
-                        dt[kk] = lds128(stage + i * 16);
-                        if (ring_d) dd[kk] = lds128(stage + P2_DRAFT_OFF + i * 16);
+                    for (int kk = 0; kk < STEPS; ++kk) {
+                        const int i = kk * 32 + lane;
+                        dt[kk] = i < n ? lds128(res_t + i * 16) : neg_inf_slot<TT>();
+                        dd[kk] = (ring_d && i < n) ? lds128(res_d + i * 16) : neg_inf_slot<TT>();
                     }
+                } else {
+                    if (!wr.wait(sh, seq)) {
+                        atomicExch(&sh.err, 1);
+                        break;
+                    }
+                    const char* stage = wr.stage(ring, seq);
+#pragma unroll
+                    for (int kk = 0; kk < STEPS; ++kk) {
+                        const int i = kk * 32 + lane;
+                        dt[kk] = neg_inf_slot<TT>();
+                        dd[kk] = neg_inf_slot<TT>();
+                        if (i < n) {
+                            dt[kk] = lds128(stage + i * 16);
+                            if (ring_d) dd[kk] = lds128(stage + P2_DRAFT_OFF + i * 16);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (ci + NBUF * NCW < n_chunks)
+                        fill_pass2<TT, TD>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, lane);
+                    ++seq;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (ci + NBUF * NCW < n_chunks)
-                    fill_pass2<TT, TD>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, lane);
                 // the chunk's draw mass: per lane over its slots, then one warp sum
                 f32x2 acc = 0ull;
 #pragma unroll
@@ -1094,111 +1163,119 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             }
         }
         __syncthreads();
-        // this CTA's draw mass, in the canonical order, pushed to every CTA
+        // this CTA's draw mass (float-float), pushed to every CTA
         if (warp == 0) {
-            double t = 0.0;
-            for (int i = lane; i < n_chunks; i += 32) t += (double)sh.p2_part[i];
-            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
-            t += (double)sh.p2_edge[0] + (double)sh.p2_edge[1];
-            if (sh.err) t = 0.0;
-            t = __shfl_sync(FULL, t, 0);  // one value for every destination CTA
-            if (lane < CS) cluster.map_shared_rank(&sh.gathered_tot[0][0], lane)[attempt * MAX_CS + rank] = t;
+            ff t = ff_from(0.0f);
+            for (int i = lane; i < n_chunks; i += 32) t = ff_add(t, sh.p2_part[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t = ff_add(t, ff_shfl_xor(t, o));
+            t = ff_add(ff_add(t, sh.p2_edge[0]), sh.p2_edge[1]);
+            if (sh.err) t = ff_from(0.0f);
+            t = ff_shfl(t, 0);  // one value for every destination CTA
+            if (lane < CS) cluster.map_shared_rank(&sh.gathered_tot[0][0], lane)[attempt * MAX_CS + rank] = make_float2(t.hi, t.lo);
         }
         cluster.sync();
-        if (tid == 0) {
-            double S = 0.0;
-            for (int cr = 0; cr < CS; ++cr) S += sh.gathered_tot[attempt][cr];
-            sh.total = S;
+        // the cluster's total and, for the draw, the CTA whose mass holds
+        // t = u2 * total: an inclusive float-float scan over lanes cr < CS
+        if (warp == 0) {
+            const float2 g = lane < CS ? sh.gathered_tot[attempt][lane] : make_float2(0.0f, 0.0f);
+            const ff v{g.x, g.y};
+            ff incl = v;
+#pragma unroll
+            for (int o = 1; o < MAX_CS; o <<= 1) {
+                const ff y = ff_shfl_up(incl, o);
+                if (lane >= o) incl = ff_add(y, incl);
+            }
+            const ff S = ff_shfl(incl, MAX_CS - 1);
+            const ff t = ff_mul(S, sh.u2);
+            const unsigned hit = __ballot_sync(FULL, lane < CS && ff_gt(incl, t));
+            const unsigned pos = __ballot_sync(FULL, lane < CS && v.hi > 0.0f);
+            const ff excl = ff_add(incl, ff_neg(v));
+            int cstar;
+            ff tc;
+            if (hit) {
+                cstar = __ffs(hit) - 1;
+                tc = ff_shfl(ff_add(t, ff_neg(excl)), cstar);
+            } else {  // t at or past the summed mass: take the last positive element
+                cstar = pos ? 31 - __clz(pos) : -1;
+                tc = ff{INFINITY, 0.0f};
+            }
+            if (lane == 0) {
+                sh.total = S;
+                sh.cstar = cstar;
+                sh.tc = tc;
+            }
         }
         __syncthreads();
-        if (sh.total > 0.0 || !w.use_d) break;
+        if (sh.total.hi > 0.0f || !w.use_d) break;
         // The residual summed to zero in float: fall back to P_t of row j.
         if (rank == 0 && tid == 0 && p.status_word)
             atomicOr(p.status_word, (unsigned)SV_FLAG_RESIDUAL_FALLBACK);
     }
 
     if (tid == 0) {
-        const double S = sh.total;
-        const double t = (double)sh.u2 * S;
-        double cum = 0.0;
-        int cstar = -1, last_pos = -1;
-        double tc = 0.0;
-        for (int cr = 0; cr < CS; ++cr) {
-            const double tot = sh.gathered_tot[attempt][cr];
-            if (tot > 0.0) last_pos = cr;
-            if (cstar < 0 && cum + tot > t) {
-                cstar = cr;
-                tc = t - cum;
-            }
-            cum += tot;
-        }
-        if (cstar < 0) {  // t at or past the summed mass: take the last positive element
-            cstar = last_pos;
-            tc = INFINITY;
-            if (rank == 0 && p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_DRAW_EDGE);
-        }
-        if (cstar < 0 && rank == 0) {
+        if (sh.cstar >= 0 && isinf(sh.tc.hi) && rank == 0 && p.status_word)
+            atomicOr(p.status_word, (unsigned)SV_FLAG_DRAW_EDGE);
+        if (sh.cstar < 0 && rank == 0) {
             // No mass at all (cannot happen for a valid row): report the
             // sequence as invalid rather than leave a slot unwritten.
             p.out_tokens[(size_t)b * (K + 1) + j] = -1;
             p.out_n_accepted[b] = -1;
             if (p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_BAD_ROW);
         }
-        sh.cstar = cstar;
-        sh.tc = tc;
-        if (rank == 0 && p.out_residual_mass) p.out_residual_mass[b] = (float)S;
+        if (rank == 0 && p.out_residual_mass) p.out_residual_mass[b] = sh.total.hi + sh.total.lo;
     }
-    __syncthreads();
 
     if (rank == sh.cstar && warp == 0) {
         // Walk down this CTA's parts in index order (low edge slot, the chunk
         // parts, high edge slot): each lane sums a contiguous run of parts, a
         // warp scan finds the run holding tc, its lane walks the run.
         const int P = n_chunks + 2;
-        auto part_val = [&](int i) -> double {
-            if (i == 0) return (double)sh.p2_edge[0];
-            if (i == P - 1) return (double)sh.p2_edge[1];
-            return (double)sh.p2_part[i - 1];
+        auto part_val = [&](int i) -> float {
+            if (i == 0) return sh.p2_edge[0];
+            if (i == P - 1) return sh.p2_edge[1];
+            return sh.p2_part[i - 1];
         };
         const int per = (P + 31) / 32;
         const int i0 = min(P, lane * per), i1 = min(P, i0 + per);
-        double mine = 0.0;
+        ff mine = ff_from(0.0f);
         int last_pos = -1;
         for (int i = i0; i < i1; ++i) {
-            const double v = part_val(i);
-            mine += v;
-            if (v > 0.0) last_pos = i;
+            const float v = part_val(i);
+            mine = ff_add(mine, v);
+            if (v > 0.0f) last_pos = i;
         }
-        double incl = mine;
+        ff incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(FULL, incl, o);
-            if (lane >= o) incl += y;
+            const ff y = ff_shfl_up(incl, o);
+            if (lane >= o) incl = ff_add(y, incl);
         }
-        const double tc = sh.tc;
-        const unsigned hit = __ballot_sync(FULL, incl > tc);
+        const ff tc = sh.tc;
+        const bool tc_inf = isinf(tc.hi);
+        const unsigned hit = __ballot_sync(FULL, !tc_inf && ff_gt(incl, tc));
         int found = -1;
-        double tw = INFINITY;
+        ff tw{INFINITY, 0.0f};
         if (hit) {
             const int l = __ffs(hit) - 1;
             if (lane == l) {
-                double t = tc - (incl - mine);
+                ff t = ff_add(tc, ff_neg(ff_add(incl, ff_neg(mine))));
                 for (int i = i0; i < i1; ++i) {
-                    const double v = part_val(i);
-                    if (v > t) { found = i; tw = t; break; }
-                    t -= v;
+                    const float v = part_val(i);
+                    if (ff_gt(ff_from(v), t)) { found = i; tw = t; break; }
+                    t = ff_add(t, -v);
                 }
                 if (found < 0) found = last_pos;  // rounding: this run's last positive part
             }
             found = __shfl_sync(FULL, found, l);
-            tw = __shfl_sync(FULL, tw, l);
+            tw = ff_shfl(tw, l);
         }
         if (found < 0) {  // rounding put tc past every part: the last positive part
             int lp = last_pos;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
             found = lp;
-            tw = INFINITY;
+            tw = ff{INFINITY, 0.0f};
         }
         if (found >= 0) {
             int q0, n;
@@ -1221,6 +1298,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 // Type pairs (target, draft): 0 = fp32/fp32, 1 = bf16/bf16, 2 = fp32/bf16.
 constexpr int N_COMBOS = 3;
 
+// Dynamic shared memory of a launch whose clusters fit on the GPU at one CTA
+// per SM: the kernel uses RING_BYTES of it; the rest keeps a second CTA off
+// the SM, so a small batch spreads over twice as many SMs.
+constexpr int SPREAD_SMEM = 128 * 1024;
+
 // Function attributes are per device; set them once per device and pair.
 static std::atomic<int> g_attr_done[64][N_COMBOS];
 
@@ -1237,7 +1319,7 @@ static cudaError_t prepare_kernel() {
     constexpr int ci = combo_of<TT, TD>();
     if (dev >= 0 && dev < 64 && g_attr_done[dev][ci].load(std::memory_order_acquire)) return cudaSuccess;
     e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             RING_BYTES);
+                             SPREAD_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1247,11 +1329,11 @@ static cudaError_t prepare_kernel() {
 }
 
 static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, unsigned grid, int cs,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int smem) {
     cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(NTHREADS, 1, 1);
-    cfg.dynamicSmemBytes = RING_BYTES;
+    cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
@@ -1262,30 +1344,60 @@ static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, unsi
 }
 
 template <typename TT, typename TD>
-static cudaError_t launch_typed(const VerifyParams& p, int cs, cudaStream_t stream) {
-    cudaError_t e = prepare_kernel<TT, TD>();
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
-    fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream);
-    return cudaLaunchKernelEx(&cfg, verify_logits_kernel<TT, TD>, p);
-}
-
-template <typename TT, typename TD>
-static int max_active_clusters(int cs) {
+static int max_active_clusters(int cs, int smem = RING_BYTES) {
     if (prepare_kernel<TT, TD>() != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    fill_config(cfg, attr, (unsigned)cs, cs, 0);
+    fill_config(cfg, attr, (unsigned)cs, cs, 0, smem);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, verify_logits_kernel<TT, TD>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
+}
+
+// Per device, pair and log2(cluster size): how many clusters are co-resident
+// at one CTA per SM, plus one (0 = not yet known); and the SM count.
+static std::atomic<int> g_spread_clusters[64][N_COMBOS][5];
+static std::atomic<int> g_num_sms[64];
+
+static int log2_cs(int cs) { return cs >= 16 ? 4 : cs >= 8 ? 3 : cs >= 4 ? 2 : cs >= 2 ? 1 : 0; }
+
+// One CTA per SM when every cluster of the launch is co-resident that way.
+template <typename TT, typename TD>
+static int launch_smem(int B, int cs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RING_BYTES;
+    int sms = g_num_sms[dev].load(std::memory_order_acquire);
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return RING_BYTES;
+        }
+        g_num_sms[dev].store(sms, std::memory_order_release);
+    }
+    if ((long long)B * cs > sms) return RING_BYTES;
+    std::atomic<int>& slot = g_spread_clusters[dev][combo_of<TT, TD>()][log2_cs(cs)];
+    int n = slot.load(std::memory_order_acquire);
+    if (n == 0) {
+        n = max_active_clusters<TT, TD>(cs, SPREAD_SMEM) + 1;
+        slot.store(n, std::memory_order_release);
+    }
+    return n - 1 >= B ? SPREAD_SMEM : RING_BYTES;
+}
+
+template <typename TT, typename TD>
+static cudaError_t launch_typed(const VerifyParams& p, int cs, cudaStream_t stream) {
+    cudaError_t e = prepare_kernel<TT, TD>();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream, launch_smem<TT, TD>(p.B, cs));
+    return cudaLaunchKernelEx(&cfg, verify_logits_kernel<TT, TD>, p);
 }
 
 static int combo_index(int dtype_target, int dtype_draft) {
@@ -1308,7 +1420,7 @@ int usable_cluster_size(int dtype_target, int dtype_draft, int cs) {
     const int ci = combo_index(dtype_target, dtype_draft);
     if (ci < 0) return 0;
     for (; cs >= 1; cs >>= 1) {
-        const int lg = cs >= 16 ? 4 : cs >= 8 ? 3 : cs >= 4 ? 2 : cs >= 2 ? 1 : 0;
+        const int lg = log2_cs(cs);
         int state = g_cluster_ok[dev][ci][lg].load(std::memory_order_acquire);
         if (state == 0) {
             const int n = ci == 0   ? max_active_clusters<float, float>(cs)
