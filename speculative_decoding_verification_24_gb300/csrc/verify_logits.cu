@@ -223,6 +223,18 @@ __device__ __forceinline__ float group_max(const uint4 (&d)[U]) {
     }
 }
 
+// NaN-propagating maximum of one slot's elements.
+template <typename T>
+__device__ __forceinline__ float slot_max(const uint4& d) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(d.x, d.y), max_nan_bf16x2(d.z, d.w));
+        return max_nan(bf16_lo(m), bf16_hi(m));
+    } else {
+        return max_nan(max_nan(__uint_as_float(d.x), __uint_as_float(d.y)),
+                       max_nan(__uint_as_float(d.z), __uint_as_float(d.w)));
+    }
+}
+
 __device__ __forceinline__ float warp_incl_scan(float x, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -318,6 +330,49 @@ __device__ __forceinline__ void arg_group(ArgPart& best, const uint4 (&d)[U], co
         }
         if (idx != INT_MAX) best = merge_arg(best, ArgPart{m, idx});
     }
+}
+
+// Greedy accumulation of one lane over its slots in increasing index order:
+// the largest slot maximum so far, that slot's index and its data. Strictly
+// larger maxima replace it, so the first occurrence wins; a NaN replaces any
+// number (the row is then invalid). The element index is found once, when
+// the lane's partial is flushed.
+struct ArgAcc {
+    float v;
+    int q;
+    uint4 d;
+};
+
+__device__ __forceinline__ ArgAcc arg_acc_empty() { return ArgAcc{-INFINITY, -1, make_uint4(0u, 0u, 0u, 0u)}; }
+
+template <typename T, int U>
+__device__ __forceinline__ void arg_slots(ArgAcc& a, const uint4 (&d)[U], const int (&q)[U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const float m = slot_max<T>(d[u]);
+        const bool take = m > a.v || (is_nan(m) && !is_nan(a.v));
+        if (take) {
+            a.v = m;
+            a.q = q[u];
+            a.d = d[u];
+        }
+    }
+}
+
+// The lane's (value, lowest element index) from its accumulation.
+template <typename T>
+__device__ __forceinline__ ArgPart arg_acc_part(const ArgAcc& a, int head) {
+    constexpr int E = Elem<T>::E;
+    int idx = INT_MAX;
+    if (a.q >= 0) {
+        const bool want_nan = is_nan(a.v);
+#pragma unroll
+        for (int e = E - 1; e >= 0; --e) {
+            const float x = elem<T>(a.d, e);
+            if (want_nan ? is_nan(x) : x == a.v) idx = a.q * E + e - head;
+        }
+    }
+    return ArgPart{a.v, idx};
 }
 
 // ---------------------------------------------------------------------------
@@ -462,64 +517,74 @@ __device__ __forceinline__ void load_draw_slot(const DrawSrc<TT, TD>& src, bool 
     else dd = load_elems_as<TT, TD>(src.drow, src.V, q * E - src.gt.head);
 }
 
-// Inverse CDF over the slots [q_begin, q_begin + n) of the target row, in
-// steps of 32 slots (one per lane) and batches of 4 steps loaded together from
-// global memory: the first element whose cumulative mass exceeds tw, or with
-// tw = +inf the last element with positive mass. Every lane returns the
-// element index. The summation order matches the pass-2 totals.
+// Inverse CDF over the slots [q_begin, q_begin + n) of the target row (one
+// pass-2 chunk: n <= P2_SLOTS), one slot per lane and step, all steps loaded
+// together from global memory: the first element whose cumulative mass
+// exceeds tw, or with tw = +inf (or when rounding leaves tw past the chunk's
+// mass) the last element with positive mass. Each element's mass is formed
+// once per slot sum, and again only for the slot that holds the answer.
+// Every lane returns the element index.
 template <typename TT, typename TD>
 __device__ int warp_draw_search(const DrawSrc<TT, TD>& src, const DrawRows& w, int q_begin, int n,
                                 ff tw, int lane) {
     using T = TT;
-    constexpr int E = Elem<T>::E, BATCH = 4;
+    constexpr int E = Elem<T>::E, STEPS = P2_SLOTS / 32;
     const bool tw_inf = isinf(tw.hi);
-    ff run = ff_from(0.0f);
-    int last_pos = -1;
-    for (int k0 = 0; k0 < n; k0 += 32 * BATCH) {
-        uint4 dt[BATCH], dd[BATCH];
-        int qs[BATCH];
+    uint4 dt[STEPS], dd[STEPS];
+    int qs[STEPS];
 #pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            const int i = k0 + k * 32 + lane;
-            qs[k] = i < n ? q_begin + i : -1;
-            load_draw_slot<TT, TD>(src, w.use_d, qs[k], dt[k], dd[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-            const float ls = slot_mass<T>(w, dt[k], dd[k]);
-            const float incl = warp_incl_scan(ls, lane);
-            const float prev = __shfl_up_sync(FULL, incl, 1);  // inclusive value of lane - 1
-            const int i0 = qs[k] * E - src.gt.head;
-            int lp = -1;
-#pragma unroll
-            for (int e = 0; e < E; ++e)
-                if (qs[k] >= 0 && draw_mass(w, elem<T>(dt[k], e), elem<T>(dd[k], e)) > 0.0f) lp = i0 + e;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
-            if (lp >= 0) last_pos = lp;
-            const unsigned hit = __ballot_sync(FULL, !tw_inf && ff_gt(ff_add(run, incl), tw));
-            if (hit) {
-                const int l = __ffs(hit) - 1;
-                int tok = -1;
-                if (lane == l) {
-                    ff cum = ff_add(run, l == 0 ? 0.0f : prev);
-                    int lastp = -1;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) {
-                        const float r = draw_mass(w, elem<T>(dt[k], e), elem<T>(dd[k], e));
-                        if (r > 0.0f) {
-                            lastp = i0 + e;
-                            cum = ff_add(cum, r);
-                            if (tok < 0 && ff_gt(cum, tw)) tok = i0 + e;
-                        }
-                    }
-                    if (tok < 0) tok = lastp;  // rounding put tw past this lane's last mass
-                }
-                return __shfl_sync(FULL, tok, l);
-            }
-            run = ff_add(run, __shfl_sync(FULL, incl, 31));
-        }
+    for (int k = 0; k < STEPS; ++k) {
+        const int i = k * 32 + lane;
+        qs[k] = i < n ? q_begin + i : -1;
+        load_draw_slot<TT, TD>(src, w.use_d, qs[k], dt[k], dd[k]);
     }
+    float incl[STEPS], tot[STEPS];
+    int last_pos = -1;  // this lane's last element with positive mass
+#pragma unroll
+    for (int k = 0; k < STEPS; ++k) {
+        float ls = 0.0f;
+#pragma unroll
+        for (int k2 = 0; k2 < E / 2; ++k2) {
+            float m0, m1;
+            unpack2(draw_mass2(w, slot_pair<T>(dt[k], k2), slot_pair<T>(dd[k], k2)), m0, m1);
+            ls += m0;
+            ls += m1;
+            const int i0 = qs[k] * E + 2 * k2 - src.gt.head;
+            if (qs[k] >= 0 && m0 > 0.0f) last_pos = i0;
+            if (qs[k] >= 0 && m1 > 0.0f) last_pos = i0 + 1;
+        }
+        incl[k] = warp_incl_scan(ls, lane);
+        tot[k] = __shfl_sync(FULL, incl[k], 31);
+    }
+    ff run = ff_from(0.0f);
+#pragma unroll
+    for (int k = 0; k < STEPS; ++k) {
+        const float prev = __shfl_up_sync(FULL, incl[k], 1);  // inclusive value of lane - 1
+        const unsigned hit = __ballot_sync(FULL, !tw_inf && ff_gt(ff_add(run, incl[k]), tw));
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            int tok = -1;
+            if (lane == l) {
+                ff cum = ff_add(run, l == 0 ? 0.0f : prev);
+                const int i0 = qs[k] * E - src.gt.head;
+                int lastp = -1;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const float r = draw_mass(w, elem<T>(dt[k], e), elem<T>(dd[k], e));
+                    if (r > 0.0f) {
+                        lastp = i0 + e;
+                        cum = ff_add(cum, r);
+                        if (tok < 0 && ff_gt(cum, tw)) tok = i0 + e;
+                    }
+                }
+                if (tok < 0) tok = lastp;  // rounding put tw past this lane's last mass
+            }
+            return __shfl_sync(FULL, tok, l);
+        }
+        run = ff_add(run, tot[k]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(FULL, last_pos, o));
     return last_pos;
 }
 
@@ -605,9 +670,9 @@ struct WarpRing {
     }
 };
 
-template <bool SAMPLE>
+template <typename T, bool SAMPLE>
 __device__ __forceinline__ void flush_row(SeqShared& sh, int warp, int lane, int row,
-                                          const SoftAcc& sa, ArgPart ag) {
+                                          const SoftAcc& sa, const ArgAcc& aa, int head) {
     if (SAMPLE) {
         SoftPart pp{sa.R, soft_acc_sum(sa)};
         if (sa.R == -INFINITY) pp.s = 0.0f;
@@ -616,6 +681,7 @@ __device__ __forceinline__ void flush_row(SeqShared& sh, int warp, int lane, int
             pp = merge_soft(pp, SoftPart{__shfl_xor_sync(FULL, pp.R, o), __shfl_xor_sync(FULL, pp.s, o)});
         if (lane == 0) sh.warp_part[warp][row] = pack(pp);
     } else {
+        ArgPart ag = arg_acc_part<T>(aa, head);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             ag = merge_arg(ag, ArgPart{__shfl_xor_sync(FULL, ag.v, o), __shfl_xor_sync(FULL, ag.i, o)});
@@ -631,8 +697,8 @@ constexpr int CHUNK_LANE_SLOTS = STAGE_SLOTS / 32;  // 8 slots per lane
 constexpr int GROUP_SLOTS = 4;
 
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ void reduce_chunk(SoftAcc& sa, ArgPart& ag, const uint4 (&d)[CHUNK_LANE_SLOTS],
-                                             int n, int q0, int head, float c, int lane) {
+__device__ __forceinline__ void reduce_chunk(SoftAcc& sa, ArgAcc& aa, const uint4 (&d)[CHUNK_LANE_SLOTS],
+                                             int n, int q0, float c, int lane) {
     const bool whole = n == STAGE_SLOTS;
 #pragma unroll
     for (int g = 0; g < CHUNK_LANE_SLOTS / GROUP_SLOTS; ++g) {
@@ -645,7 +711,7 @@ __device__ __forceinline__ void reduce_chunk(SoftAcc& sa, ArgPart& ag, const uin
             qs[u] = q0 + i;
         }
         if (SAMPLE) soft_group<T, GROUP_SLOTS>(sa, x, c);
-        else arg_group<T, GROUP_SLOTS>(ag, x, qs, head);
+        else arg_slots<T, GROUP_SLOTS>(aa, x, qs);
     }
 }
 
@@ -743,13 +809,16 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
     int cur_row = -1, ia = 0, ib = 0, head = 0;
     TokenSpot ts{-1, 0, -1};
     SoftAcc sa = soft_acc_empty();
-    ArgPart ag{-INFINITY, INT_MAX};
+    ArgAcc aa = arg_acc_empty();
     for (int chunk = warp; chunk < nchunks; chunk += NCW, ++seq) {
         seek_row(rc, sh.rows, chunk);
         if (rc.r != cur_row) {  // a new row: flush the last one, look the new one up once
-            if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
+            if (cur_row >= 0) {
+                if (std::is_same<TT, TD>::value || cur_row <= K) flush_row<TT, SAMPLE>(sh, warp, lane, cur_row, sa, aa, head);
+                else flush_row<TD, SAMPLE>(sh, warp, lane, cur_row, sa, aa, head);
+            }
             sa = soft_acc_empty();
-            ag = ArgPart{-INFINITY, INT_MAX};
+            aa = arg_acc_empty();
             cur_row = rc.r;
             const RowInfo ri = sh.rows[cur_row];
             ia = ri.ia;
@@ -780,10 +849,13 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
         __syncwarp();
         if (chunk + NBUF * NCW < nchunks)
             fill_pass1(sh, wr, ring, seq + NBUF, chunk + NBUF * NCW, fill_rc, lane);
-        if (std::is_same<TT, TD>::value || cur_row <= K) reduce_chunk<TT, SAMPLE>(sa, ag, d, n, q0, head, c, lane);
-        else reduce_chunk<TD, SAMPLE>(sa, ag, d, n, q0, head, c, lane);
+        if (std::is_same<TT, TD>::value || cur_row <= K) reduce_chunk<TT, SAMPLE>(sa, aa, d, n, q0, c, lane);
+        else reduce_chunk<TD, SAMPLE>(sa, aa, d, n, q0, c, lane);
     }
-    if (cur_row >= 0) flush_row<SAMPLE>(sh, warp, lane, cur_row, sa, ag);
+    if (cur_row >= 0) {
+        if (std::is_same<TT, TD>::value || cur_row <= K) flush_row<TT, SAMPLE>(sh, warp, lane, cur_row, sa, aa, head);
+        else flush_row<TD, SAMPLE>(sh, warp, lane, cur_row, sa, aa, head);
+    }
 }
 
 // Issues pass-2 chunk ci (target slots, and the draft slots when they share
