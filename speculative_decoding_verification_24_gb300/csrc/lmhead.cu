@@ -12,18 +12,22 @@
 // V-contiguous W as an MN-major operand) and the M rows of hidden as the MMA's
 // N dimension (B = hidden, K-major), N = M rounded up to 16 (at most 256).
 //
-// One CTA per 128-column slice of V:
+// Persistent CTAs, one per SM, each taking the 128-column tiles t = block,
+// block + grid, ...:
 //   warp 0  TMA producer: per 64-wide step of d, two 64x64 boxes of W and one
-//           64 x N box of hidden (128-byte swizzle) into a 4-stage ring whose
-//           stages complete on mbarriers;
-//   warp 1  allocates the TMEM accumulator (128 lanes x 256 columns) and one
+//           64 x N box of hidden (128-byte swizzle) into an S-stage ring that
+//           runs on across tiles; stages complete on mbarriers;
+//   warp 1  allocates TMEM (two 128-lane x 256-column accumulators) and one
 //           thread issues tcgen05.mma (kind::f16, 4 per stage, K = 16 each),
-//           committing each stage back to the producer and the last one to
-//           the epilogue;
-//   warps 4-7  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
-//           32(w-4)...), one coalesced 128-byte store per column and warp.
+//           committing each stage back to the producer and each finished tile
+//           to the epilogue; a tile's MMAs wait until the epilogue has drained
+//           the accumulator they reuse;
+//   warps 4-7  epilogue: tcgen05.ld of the finished accumulator (warp w reads
+//           TMEM lanes 32(w-4)...), one coalesced 128-byte store per column and
+//           warp, then the accumulator is handed back; it overlaps the next
+//           tile's loads and MMAs.
 // Every mbarrier wait is bounded; a wait that gives up sets SV_FLAG_TIMEOUT,
-// the CTA skips the remaining work, waits for what it issued and frees TMEM.
+// the CTA stops issuing work, waits for what it issued and frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,19 +39,21 @@
 
 namespace sv {
 
-constexpr int LM_BLOCK_V = 128;                       // slice of V per CTA (MMA M)
-constexpr int LM_BLOCK_K = 64;                        // d per stage (one 128-byte row of bf16)
-constexpr int LM_STAGES = 4;
+constexpr int LM_BLOCK_V = 128;                          // columns of V per tile (MMA M)
+constexpr int LM_BLOCK_K = 64;                           // d per stage (one 128-byte row of bf16)
 constexpr int LM_A_BYTES = LM_BLOCK_V * LM_BLOCK_K * 2;  // 16 KB: two 64 x 64 boxes of W
 constexpr int LM_BOX_BYTES = 64 * LM_BLOCK_K * 2;        // 8 KB: one box of W
-constexpr int LM_MAX_N = 256;
-constexpr int LM_B_STAGE_MAX = LM_MAX_N * LM_BLOCK_K * 2;  // 32 KB
+constexpr int LM_MAX_STAGES = 8;
+constexpr int LM_SMEM_BUDGET = 220 * 1024;               // dynamic shared memory for the ring
 constexpr int LM_THREADS = 256;
-constexpr int LM_TMEM_COLS = 256;
+constexpr int LM_ACC_COLS = 256;                         // TMEM columns per accumulator
+constexpr int LM_TMEM_COLS = 2 * LM_ACC_COLS;
 constexpr uint32_t LM_WAIT_LIMIT = 1u << 24;
 
 struct LmParams {
     int M, d, V, N;     // N: M rounded up to 16
+    int stages;         // ring stages (<= LM_MAX_STAGES)
+    int tiles;          // ceil(V / LM_BLOCK_V)
     float* out;         // [M, V]
     uint32_t* status;   // optional
 };
@@ -117,29 +123,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ bool lm_error(const int* err) { return *(volatile const int*)err != 0; }
+
 __global__ void __launch_bounds__(LM_THREADS, 1)
     lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
                        LmParams p) {
     extern __shared__ __align__(1024) char smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    char* a_stage = smem;                                   // LM_STAGES x 16 KB
-    char* b_stage = smem + LM_STAGES * LM_A_BYTES;          // LM_STAGES x N*128 B
+    const int S = p.stages;
     const int b_bytes = p.N * LM_BLOCK_K * 2;
-    __shared__ __align__(8) uint64_t full[LM_STAGES], empty[LM_STAGES], accum_full;
+    char* a_ring = smem;                      // S x 16 KB
+    char* b_ring = smem + S * LM_A_BYTES;     // S x b_bytes (b_bytes is a multiple of 2 KB)
+    __shared__ __align__(8) uint64_t full[LM_MAX_STAGES], empty[LM_MAX_STAGES];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
     __shared__ uint32_t tmem_base;
     __shared__ int err;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int v0 = blockIdx.x * LM_BLOCK_V;
     const int ksteps = p.d / LM_BLOCK_K;
+    const int my_tiles = p.tiles > (int)blockIdx.x ? (p.tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < LM_STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(&accum_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&acc_full[a], 1);
+            mbar_init(&acc_empty[a], 128);  // every epilogue thread
+        }
+        mbar_init(&mma_done, 1);
         err = 0;
         fence_barrier_init();
     }
@@ -155,75 +169,98 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     const uint32_t tmem = tmem_base;
 
     if (warp == 0 && lane == 0) {
-        // ---- TMA producer
+        // ---- TMA producer: one continuous ring over all of this CTA's tiles
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_h)) : "memory");
-        // A slice whose second 64 columns lie wholly past V loads only the
-        // first box; the MMA rows of the other half are never stored.
-        const bool second_box = v0 + 64 < p.V;
-        const uint32_t stage_tx = (uint32_t)((second_box ? LM_A_BYTES : LM_BOX_BYTES) + b_bytes);
-        int issued = 0;
-        for (int ks = 0; ks < ksteps; ++ks) {
-            const int s = ks % LM_STAGES, k = ks / LM_STAGES;
-            if (k > 0 && !mbar_wait(&empty[s], (k - 1) & 1, LM_WAIT_LIMIT)) {
-                atomicExch(&err, 1);
-                break;
+        int it = 0;
+        for (int li = 0; li < my_tiles && !lm_error(&err); ++li) {
+            const int v0 = ((int)blockIdx.x + li * (int)gridDim.x) * LM_BLOCK_V;
+            // a tile whose second 64 columns lie wholly past V loads only the
+            // first box; the MMA rows of the other half are never stored
+            const bool second_box = v0 + 64 < p.V;
+            const uint32_t stage_tx = (uint32_t)((second_box ? LM_A_BYTES : LM_BOX_BYTES) + b_bytes);
+            for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                const int s = it % S, n = it / S;
+                if (n > 0 && !mbar_wait(&empty[s], (n - 1) & 1, LM_WAIT_LIMIT)) {
+                    atomicExch(&err, 1);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[s], stage_tx);
+                char* a = a_ring + s * LM_A_BYTES;
+                tma_load_2d(a, &tm_w, v0, ks * LM_BLOCK_K, &full[s]);
+                if (second_box) tma_load_2d(a + LM_BOX_BYTES, &tm_w, v0 + 64, ks * LM_BLOCK_K, &full[s]);
+                tma_load_2d(b_ring + s * b_bytes, &tm_h, ks * LM_BLOCK_K, 0, &full[s]);
             }
-            mbar_arrive_expect_tx(&full[s], stage_tx);
-            char* a = a_stage + s * LM_A_BYTES;
-            tma_load_2d(a, &tm_w, v0, ks * LM_BLOCK_K, &full[s]);
-            if (second_box) tma_load_2d(a + LM_BOX_BYTES, &tm_w, v0 + 64, ks * LM_BLOCK_K, &full[s]);
-            tma_load_2d(b_stage + s * LM_B_STAGE_MAX, &tm_h, ks * LM_BLOCK_K, 0, &full[s]);
-            ++issued;
         }
-        // every load issued has landed before this thread leaves the loop
-        for (int q = issued - LM_STAGES > 0 ? issued - LM_STAGES : 0; q < issued; ++q)
-            (void)mbar_wait(&full[q % LM_STAGES], (q / LM_STAGES) & 1, LM_WAIT_LIMIT);
+        // every load issued has landed before this thread leaves: the last
+        // min(S, it) loads are the latest phase of their stages
+        for (int q = it - S > 0 ? it - S : 0; q < it; ++q)
+            (void)mbar_wait(&full[q % S], (q / S) & 1, LM_WAIT_LIMIT);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         const uint32_t idesc = umma_idesc_bf16(p.N, LM_BLOCK_V);
-        for (int ks = 0; ks < ksteps; ++ks) {
-            const int s = ks % LM_STAGES, k = ks / LM_STAGES;
-            if (!mbar_wait(&full[s], k & 1, LM_WAIT_LIMIT)) {
-                atomicExch(&err, 1);
+        int it = 0;
+        bool ok = true;
+        for (int li = 0; li < my_tiles && ok; ++li) {
+            const int a = li & 1;
+            if (li >= 2 && !mbar_wait(&acc_empty[a], ((li >> 1) - 1) & 1, LM_WAIT_LIMIT)) {
+                ok = false;
                 break;
             }
             tmem_fence_after();
-            const uint32_t a0 = smem_u32(a_stage + s * LM_A_BYTES);
-            const uint32_t b0 = smem_u32(b_stage + s * LM_B_STAGE_MAX);
+            const uint32_t acc = tmem + (uint32_t)(a * LM_ACC_COLS);
+            for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                const int s = it % S, n = it / S;
+                if (!mbar_wait(&full[s], n & 1, LM_WAIT_LIMIT)) {
+                    ok = false;
+                    break;
+                }
+                tmem_fence_after();
+                const uint32_t a0 = smem_u32(a_ring + s * LM_A_BYTES);
+                const uint32_t b0 = smem_u32(b_ring + s * b_bytes);
 #pragma unroll
-            for (int kk = 0; kk < LM_BLOCK_K / 16; ++kk) {
-                // A (MN-major): 16 rows of d = two 8-row swizzle atoms (2 KB);
-                //   LBO = the second 64-wide block of V (the second box), SBO = 8 rows.
-                // B (K-major): 16 elements of d = 32 bytes inside the 128-byte row.
-                const uint64_t ad = umma_desc_sw128(a0 + kk * 2048, LM_BOX_BYTES, 1024);
-                const uint64_t bd = umma_desc_sw128(b0 + kk * 32, 16, 1024);
-                umma_bf16(tmem, ad, bd, idesc, (ks | kk) != 0);
+                for (int kk = 0; kk < LM_BLOCK_K / 16; ++kk) {
+                    // A (MN-major): 16 rows of d = two 8-row swizzle atoms (2 KB);
+                    //   LBO = the second 64-wide block of V (the second box), SBO = 8 rows.
+                    // B (K-major): 16 elements of d = 32 bytes inside the 128-byte row.
+                    const uint64_t ad = umma_desc_sw128(a0 + kk * 2048, LM_BOX_BYTES, 1024);
+                    const uint64_t bd = umma_desc_sw128(b0 + kk * 32, 16, 1024);
+                    umma_bf16(acc, ad, bd, idesc, (ks | kk) != 0);
+                }
+                umma_commit(&empty[s]);  // the stage is free once these MMAs completed
             }
-            umma_commit(&empty[s]);  // the stage is free once these MMAs completed
+            if (!ok) break;
+            umma_commit(&acc_full[a]);  // the tile's accumulator is complete
         }
-        umma_commit(&accum_full);
+        if (!ok) atomicExch(&err, 1);
+        // every MMA issued has completed before TMEM is released
+        umma_commit(&mma_done);
+        (void)mbar_wait(&mma_done, 0, LM_WAIT_LIMIT);
     } else if (warp >= 4) {
         // ---- epilogue: TMEM -> registers -> global (coalesced per column)
         const int q = warp - 4;
-        bool ok = mbar_wait(&accum_full, 0, LM_WAIT_LIMIT);
-        tmem_fence_after();
-        if (!ok) atomicExch(&err, 1);
-        // tcgen05.ld is warp-collective: the whole warp reads or none of it
-        ok = __all_sync(0xffffffffu, ok && *(volatile int*)&err == 0);
-        const int v = v0 + 32 * q + lane;
-        if (ok) {
+        for (int li = 0; li < my_tiles; ++li) {
+            const int a = li & 1;
+            bool ok = mbar_wait(&acc_full[a], (li >> 1) & 1, LM_WAIT_LIMIT);
+            tmem_fence_after();
+            if (!ok) atomicExch(&err, 1);
+            // tcgen05.ld is warp-collective: the whole warp reads or none of it
+            ok = __all_sync(0xffffffffu, ok && !lm_error(&err));
+            if (!ok) break;
+            const int v = ((int)blockIdx.x + li * (int)gridDim.x) * LM_BLOCK_V + 32 * q + lane;
+            const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * LM_ACC_COLS);
             for (int c0 = 0; c0 < p.N; c0 += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, r);
+                tmem_ld32(acc + (uint32_t)c0, r);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const int m = c0 + c;
                     if (m < p.M && v < p.V) p.out[(size_t)m * p.V + v] = __uint_as_float(r[c]);
                 }
             }
+            tmem_fence_before();
+            mbar_arrive(&acc_empty[a]);
         }
-        tmem_fence_before();
     }
     __syncthreads();
     if (warp == 1) {
@@ -267,32 +304,47 @@ static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, ui
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int lmhead_smem_bytes(int N) {
-    (void)N;
-    return 1024 + LM_STAGES * (LM_A_BYTES + LM_B_STAGE_MAX);
+static int lmhead_stages(int N) {
+    const int stage = LM_A_BYTES + N * LM_BLOCK_K * 2;
+    const int st = (LM_SMEM_BUDGET - 1024) / stage;
+    return st < LM_MAX_STAGES ? st : LM_MAX_STAGES;
 }
+
+static std::atomic<int> g_lm_sms[64];
 
 cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
                                uint32_t* status, cudaStream_t stream) {
-    static std::atomic<int> attr_done{0};
-    const int smem = lmhead_smem_bytes(0);
-    if (!attr_done.load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::atomic<int> attr_done[64];
+    if (!attr_done[dev].load(std::memory_order_acquire)) {
+        e = cudaFuncSetAttribute(lmhead_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LM_SMEM_BUDGET);
         if (e != cudaSuccess) return e;
-        attr_done.store(1, std::memory_order_release);
+        attr_done[dev].store(1, std::memory_order_release);
+    }
+    int sms = g_lm_sms[dev].load(std::memory_order_acquire);
+    if (sms == 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_lm_sms[dev].store(sms, std::memory_order_release);
     }
     LmParams p;
     p.M = M;
     p.d = d;
     p.V = V;
     p.N = (M + 15) / 16 * 16;
+    p.stages = lmhead_stages(p.N);
+    p.tiles = (V + LM_BLOCK_V - 1) / LM_BLOCK_V;
     p.out = out;
     p.status = status;
     CUtensorMap tm_w, tm_h;
     if (!encode_bf16_2d(&tm_w, W, (uint64_t)d, (uint64_t)V, 64) ||
         !encode_bf16_2d(&tm_h, hidden, (uint64_t)M, (uint64_t)d, (uint32_t)p.N))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((V + LM_BLOCK_V - 1) / LM_BLOCK_V));
+    const int smem = 1024 + p.stages * (LM_A_BYTES + p.N * LM_BLOCK_K * 2);
+    const dim3 grid((unsigned)(p.tiles < sms ? p.tiles : sms));
     lmhead_gemm_kernel<<<grid, LM_THREADS, smem, stream>>>(tm_w, tm_h, p);
     return cudaGetLastError();
 }
