@@ -230,7 +230,8 @@ def time_device(sets, steps, warmup, stream, seed0=0):
     def step(i):
         c = sets[i % len(sets)]
         spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=modes[i % len(sets)],
-                       seed=seed0 + i, out_tokens=out_tok[i], out_n_accepted=out_n[i], stream=stream)
+                       seed=seed0 + i, out_tokens=out_tok[i], out_n_accepted=out_n[i], stream=stream,
+                       overlap_previous=True)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -364,7 +365,9 @@ def run_ours(args, rank, world, device):
         "gpu_launches": args.steps,
         "clocks": clocks,
         "timing": "one CUDA graph of the K steps, replayed between CUDA events on the "
-                  "launching stream",
+                  "launching stream; each step is launched with SV_ARG_OVERLAP_PREVIOUS "
+                  "(programmatic dependent launch: a step may stream its inputs while the "
+                  "previous step finishes; it writes its outputs after that step completes)",
         "eager_rows_per_s": world * rows_per_step * args.steps / (eager_ms / 1e3),
     }
     result["e2e"] = run_e2e(args, sets, device, stream, world)

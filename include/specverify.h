@@ -141,7 +141,15 @@ typedef struct {
     int cluster_size;            /* CTAs that share one sequence: 0 = automatic,
                                     else 1, 2, 4, 8 or 16                         */
     sv_stream_t stream;
+    uint32_t flags;              /* SV_ARG_* bits, 0 for none                     */
 } sv_verify_args;
+
+/* sv_verify_args.flags: the inputs of this call are not written by the work
+ * enqueued just before it on `stream`, so the call may start reading them
+ * while that work (typically the previous verify call) is still running. Its
+ * outputs are still written only after that work has completed. Without the
+ * flag a call starts after everything before it on the stream. */
+#define SV_ARG_OVERLAP_PREVIOUS 1u
 
 /* spec_verify with per-sequence modes, explicit sequence ids and optional
  * probability outputs. Same conventions and errors as spec_verify. */

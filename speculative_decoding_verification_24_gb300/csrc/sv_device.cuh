@@ -69,6 +69,12 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 __device__ __forceinline__ bool is_nan(float x) { return x != x; }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory is visible (returns at once when the
+// launch had no such dependency); let the next grid on the stream launch.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // --------------------------------------------------------------------------
 // Streaming loads: read-only path, no L1 allocation (each byte is used once).
 // --------------------------------------------------------------------------

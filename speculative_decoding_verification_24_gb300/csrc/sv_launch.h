@@ -25,6 +25,7 @@ struct VerifyParams {
     float* out_p_draft;        // [B, K] or nullptr
     float* out_residual_mass;  // [B] or nullptr
     uint32_t* status_word;     // or nullptr
+    int overlap_previous;      // inputs not written by the previous work on the stream
 };
 
 // CTAs per cluster chosen from the shape when the caller asks for automatic.

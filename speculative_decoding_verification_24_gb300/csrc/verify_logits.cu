@@ -938,6 +938,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const TT* tgt = static_cast<const TT*>(p.target);
     const TD* drf = static_cast<const TD*>(p.draft);
 
+    // Programmatic dependent launch: without overlap, nothing is read before
+    // the work ahead on the stream has completed; with it, only inputs are
+    // read until then (outputs are written after the wait below pass 1).
+    if (!p.overlap_previous) grid_dependency_wait();
     const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
     const bool mode_ok = (mode == 0 || mode == 1) && !(mode == 1 && drf == nullptr);
     const bool sample = mode == 1 && mode_ok;
@@ -1000,6 +1004,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         }
     }
     __syncthreads();
+    launch_dependents();  // the next call on the stream may start streaming its inputs
+    if (p.overlap_previous) grid_dependency_wait();
     // This CTA's partial of every row, pushed into every CTA of the cluster.
     for (int t = tid; mode_ok && t < CS * nrows; t += NTHREADS) {
         const int dst = t / nrows, r = t % nrows;
@@ -1467,8 +1473,13 @@ static cudaError_t launch_typed(const VerifyParams& p, int cs, cudaStream_t stre
     cudaError_t e = prepare_kernel<TT, TD>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream, launch_smem<TT, TD>(p.B, cs));
+    if (p.overlap_previous) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, verify_logits_kernel<TT, TD>, p);
 }
 

@@ -273,3 +273,29 @@ def test_large_vocab_long_draft():
     g, ref = run_pair(case, seed=0)
     check(g, ref, "V=262144 K=31")
     assert g["n_accepted"].max() > 3
+
+
+def test_overlapping_calls_match_serial_calls():
+    """Calls launched with overlap_previous on one stream (each may start while
+    the previous one runs) give the results of plain calls, including when
+    they write the same output buffers."""
+    cases = [synth.make_workload("c2", seed=40 + i, device="cuda", tau=1.0) for i in range(4)]
+    want = []
+    for i, c in enumerate(cases):
+        out = spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes="sample", seed=i)
+        want.append((out["tokens"].clone(), out["n_accepted"].clone()))
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        for i, c in enumerate(cases):
+            outs.append((i, spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes="sample",
+                                           seed=i, overlap_previous=True)))
+    shared_t = torch.empty_like(want[0][0])
+    shared_n = torch.empty_like(want[0][1])
+    for i, c in enumerate(cases):  # the same output buffers, back to back
+        spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes="sample", seed=i,
+                       out_tokens=shared_t, out_n_accepted=shared_n, overlap_previous=True)
+    torch.cuda.synchronize()
+    for i, out in outs:
+        assert torch.equal(out["tokens"], want[i][0]) and torch.equal(out["n_accepted"], want[i][1])
+    assert torch.equal(shared_t, want[-1][0]) and torch.equal(shared_n, want[-1][1])
