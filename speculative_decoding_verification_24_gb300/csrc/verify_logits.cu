@@ -389,6 +389,7 @@ constexpr int P2_SLOTS = STAGE_SLOTS / 2;       // target slots per pass-2 chunk
 constexpr int P2_DRAFT_OFF = P2_SLOTS * 16;     // draft half of a pass-2 stage
 constexpr int MAX_P2_CHUNKS = 256;              // per CTA slice of one row
 constexpr int MAX_CS = 16;
+constexpr int MAX_ORDERED_B = 256;              // batches up to this size are taken sample-first
 constexpr uint32_t WAIT_LIMIT = 1u << 22;       // polls before a wait gives up
 
 // One row of the sequence as this CTA sees it: the 16-byte slots of its slice,
@@ -622,8 +623,7 @@ struct SeqShared {
     float2 merged[MAX_ROWS];
     float p2_part[MAX_P2_CHUNKS];
     float p2_edge[2];
-    int x_tok[MAX_K];                   // draft tokens, and the logits at them
-    float lt_x[MAX_K], ld_x[MAX_K];     // (prefetched at the start)
+    float lt_x[MAX_K], ld_x[MAX_K];     // the logits at the draft tokens (captured in pass 1)
     float2 gathered_tot[2][MAX_CS];     // every CTA's draw mass (float-float), pushed by their owners
     float u_pos[MAX_K + 1], u2_pos[MAX_K + 1];  // Philox uniforms of positions 0..K
     // decision (identical in every CTA of the cluster)
@@ -633,6 +633,7 @@ struct SeqShared {
     ff total, tc;
     int cstar;
     int total_chunks;
+    int seq_b;                          // the sequence this cluster verifies
 };
 
 // Two CTAs per SM: 2 x (ring + this + 1 KB reserved) within 228 KB.
@@ -932,8 +933,43 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     cg::cluster_group cluster = cg::this_cluster();
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
-    const int b = (int)(blockIdx.x / CS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // Cluster c verifies sequence c, or, with per-sequence modes, the c-th of
+    // the order (sample sequences, then the others, each in index order): the
+    // sequences with the most rows to read start first. Every CTA derives the
+    // same order from the modes array; results do not depend on it.
+    if (warp == 0) {
+        const int c = (int)(blockIdx.x / CS);
+        int seq = c;
+        if (p.modes && p.B <= MAX_ORDERED_B) {
+            constexpr int PER = MAX_ORDERED_B / 32;
+            unsigned smask[PER];
+            int ns = 0;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int i = k * 32 + lane;
+                const bool s = i < p.B && __ldg(p.modes + i) == 1;
+                smask[k] = __ballot_sync(FULL, s);
+                ns += __popc(smask[k]);
+            }
+            const bool want_sample = c < ns;
+            int left = want_sample ? c : c - ns;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) {
+                const int n_here = min(32, p.B - k * 32);
+                unsigned m = want_sample ? smask[k] : (~smask[k] & (n_here >= 32 ? FULL : ((1u << max(n_here, 0)) - 1u)));
+                const int cnt = __popc(m);
+                if (left >= 0 && left < cnt) {
+                    for (int t = 0; t < left; ++t) m &= m - 1u;
+                    seq = k * 32 + __ffs(m) - 1;
+                }
+                left -= cnt;
+            }
+        }
+        if (lane == 0) sh.seq_b = seq;
+    }
+    __syncthreads();
+    const int b = sh.seq_b;
     const int K = p.K, V = p.V;
     const TT* tgt = static_cast<const TT*>(p.target);
     const TD* drf = static_cast<const TD*>(p.draft);
