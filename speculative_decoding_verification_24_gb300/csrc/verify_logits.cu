@@ -518,76 +518,62 @@ __device__ __forceinline__ void load_draw_slot(const DrawSrc<TT, TD>& src, bool 
     else dd = load_elems_as<TT, TD>(src.drow, src.V, q * E - src.gt.head);
 }
 
-// Inverse CDF over the slots [q_begin, q_begin + n) of the target row (one
-// pass-2 chunk: n <= P2_SLOTS), one slot per lane and step, all steps loaded
-// together from global memory: the first element whose cumulative mass
-// exceeds tw, or with tw = +inf (or when rounding leaves tw past the chunk's
-// mass) the last element with positive mass. Each element's mass is formed
-// once per slot sum, and again only for the slot that holds the answer.
-// Every lane returns the element index.
+// One 32-slot step of the final search, for the warp that owns it: lane l
+// holds slot q_begin + step * 32 + l of the part (valid below n). Each
+// element's draw mass is formed once; the lane keeps them, with the warp's
+// inclusive scan of the slot sums in the pass-2 order.
 template <typename TT, typename TD>
-__device__ int warp_draw_search(const DrawSrc<TT, TD>& src, const DrawRows& w, int q_begin, int n,
-                                ff tw, int lane) {
-    using T = TT;
-    constexpr int E = Elem<T>::E, STEPS = P2_SLOTS / 32;
-    const bool tw_inf = isinf(tw.hi);
-    uint4 dt[STEPS], dd[STEPS];
-    int qs[STEPS];
-#pragma unroll
-    for (int k = 0; k < STEPS; ++k) {
-        const int i = k * 32 + lane;
-        qs[k] = i < n ? q_begin + i : -1;
-        load_draw_slot<TT, TD>(src, w.use_d, qs[k], dt[k], dd[k]);
-    }
-    float incl[STEPS], tot[STEPS];
-    int last_pos = -1;  // this lane's last element with positive mass
-#pragma unroll
-    for (int k = 0; k < STEPS; ++k) {
+struct DrawStep {
+    static constexpr int E = Elem<TT>::E;
+    float m[E];        // this lane's element masses
+    float incl, prev;  // inclusive scan of the slot sums: this lane and lane - 1
+    float tot;         // the step's total
+    int last_pos;      // the warp's last element with positive mass (-1: none)
+    int i0;            // row element index of this lane's first element
+
+    __device__ __forceinline__ void load(const DrawSrc<TT, TD>& src, const DrawRows& w, int q_begin,
+                                         int n, int step, int lane) {
+        const int i = step * 32 + lane;
+        const int q = i < n ? q_begin + i : -1;
+        uint4 dt, dd;
+        load_draw_slot<TT, TD>(src, w.use_d, q, dt, dd);
+        i0 = q * E - src.gt.head;
         float ls = 0.0f;
+        int lp = -1;
 #pragma unroll
         for (int k2 = 0; k2 < E / 2; ++k2) {
-            float m0, m1;
-            unpack2(draw_mass2(w, slot_pair<T>(dt[k], k2), slot_pair<T>(dd[k], k2)), m0, m1);
-            ls += m0;
-            ls += m1;
-            const int i0 = qs[k] * E + 2 * k2 - src.gt.head;
-            if (qs[k] >= 0 && m0 > 0.0f) last_pos = i0;
-            if (qs[k] >= 0 && m1 > 0.0f) last_pos = i0 + 1;
+            unpack2(draw_mass2(w, slot_pair<TT>(dt, k2), slot_pair<TT>(dd, k2)), m[2 * k2], m[2 * k2 + 1]);
+            ls += m[2 * k2];
+            ls += m[2 * k2 + 1];
         }
-        incl[k] = warp_incl_scan(ls, lane);
-        tot[k] = __shfl_sync(FULL, incl[k], 31);
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (q >= 0 && m[e] > 0.0f) lp = i0 + e;
+        incl = warp_incl_scan(ls, lane);
+        prev = __shfl_up_sync(FULL, incl, 1);
+        tot = __shfl_sync(FULL, incl, 31);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
+        last_pos = lp;
     }
-    ff run = ff_from(0.0f);
+
+    // The element of lane l's slot where the cumulative mass from `run`
+    // (the masses before this lane) first exceeds tw; its last positive
+    // element if rounding leaves tw past it.
+    __device__ __forceinline__ int walk(ff run, ff tw, int l) const {
+        ff cum = ff_add(run, l == 0 ? 0.0f : prev);
+        int tok = -1, lastp = -1;
 #pragma unroll
-    for (int k = 0; k < STEPS; ++k) {
-        const float prev = __shfl_up_sync(FULL, incl[k], 1);  // inclusive value of lane - 1
-        const unsigned hit = __ballot_sync(FULL, !tw_inf && ff_gt(ff_add(run, incl[k]), tw));
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            int tok = -1;
-            if (lane == l) {
-                ff cum = ff_add(run, l == 0 ? 0.0f : prev);
-                const int i0 = qs[k] * E - src.gt.head;
-                int lastp = -1;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const float r = draw_mass(w, elem<T>(dt[k], e), elem<T>(dd[k], e));
-                    if (r > 0.0f) {
-                        lastp = i0 + e;
-                        cum = ff_add(cum, r);
-                        if (tok < 0 && ff_gt(cum, tw)) tok = i0 + e;
-                    }
-                }
-                if (tok < 0) tok = lastp;  // rounding put tw past this lane's last mass
+        for (int e = 0; e < E; ++e) {
+            if (m[e] > 0.0f) {
+                lastp = i0 + e;
+                cum = ff_add(cum, m[e]);
+                if (tok < 0 && ff_gt(cum, tw)) tok = i0 + e;
             }
-            return __shfl_sync(FULL, tok, l);
         }
-        run = ff_add(run, tot[k]);
+        return tok < 0 ? lastp : tok;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) last_pos = max(last_pos, __shfl_xor_sync(FULL, last_pos, o));
-    return last_pos;
-}
+};
 
 // The accept test u * P_d(x) < P_t(x) with P = e / S, i.e. u * e_d * S_t <
 // e_t * S_d, decided as if in exact arithmetic on these float inputs. The
@@ -634,6 +620,10 @@ struct SeqShared {
     int cstar;
     int total_chunks;
     int seq_b;                          // the sequence this cluster verifies
+    // the final search in the CTA holding the draw
+    int found, step_lp[P2_SLOTS / 32], step_hit[P2_SLOTS / 32];
+    float step_tot[P2_SLOTS / 32];
+    ff tw;
 };
 
 // Two CTAs per SM: 2 x (ring + this + 1 KB reserved) within 228 KB.
@@ -1340,58 +1330,71 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         if (rank == 0 && p.out_residual_mass) p.out_residual_mass[b] = sh.total.hi + sh.total.lo;
     }
 
-    if (rank == sh.cstar && warp == 0) {
-        // Walk down this CTA's parts in index order (low edge slot, the chunk
-        // parts, high edge slot): each lane sums a contiguous run of parts, a
-        // warp scan finds the run holding tc, its lane walks the run.
-        const int P = n_chunks + 2;
-        auto part_val = [&](int i) -> float {
-            if (i == 0) return sh.p2_edge[0];
-            if (i == P - 1) return sh.p2_edge[1];
-            return sh.p2_part[i - 1];
-        };
-        const int per = (P + 31) / 32;
-        const int i0 = min(P, lane * per), i1 = min(P, i0 + per);
-        ff mine = ff_from(0.0f);
-        int last_pos = -1;
-        for (int i = i0; i < i1; ++i) {
-            const float v = part_val(i);
-            mine = ff_add(mine, v);
-            if (v > 0.0f) last_pos = i;
-        }
-        ff incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const ff y = ff_shfl_up(incl, o);
-            if (lane >= o) incl = ff_add(y, incl);
-        }
-        const ff tc = sh.tc;
-        const bool tc_inf = isinf(tc.hi);
-        const unsigned hit = __ballot_sync(FULL, !tc_inf && ff_gt(incl, tc));
-        int found = -1;
-        ff tw{INFINITY, 0.0f};
-        if (hit) {
-            const int l = __ffs(hit) - 1;
-            if (lane == l) {
-                ff t = ff_add(tc, ff_neg(ff_add(incl, ff_neg(mine))));
-                for (int i = i0; i < i1; ++i) {
-                    const float v = part_val(i);
-                    if (ff_gt(ff_from(v), t)) { found = i; tw = t; break; }
-                    t = ff_add(t, -v);
-                }
-                if (found < 0) found = last_pos;  // rounding: this run's last positive part
+    if (rank == sh.cstar) {  // the CTA holding the draw (uniform over the CTA)
+        if (warp == 0) {
+            // Walk down this CTA's parts in index order (low edge slot, the
+            // chunk parts, high edge slot): each lane sums a contiguous run of
+            // parts, a warp scan finds the run holding tc, its lane walks it.
+            const int P = n_chunks + 2;
+            auto part_val = [&](int i) -> float {
+                if (i == 0) return sh.p2_edge[0];
+                if (i == P - 1) return sh.p2_edge[1];
+                return sh.p2_part[i - 1];
+            };
+            const int per = (P + 31) / 32;
+            const int i0 = min(P, lane * per), i1 = min(P, i0 + per);
+            ff mine = ff_from(0.0f);
+            int last_pos = -1;
+            for (int i = i0; i < i1; ++i) {
+                const float v = part_val(i);
+                mine = ff_add(mine, v);
+                if (v > 0.0f) last_pos = i;
             }
-            found = __shfl_sync(FULL, found, l);
-            tw = ff_shfl(tw, l);
-        }
-        if (found < 0) {  // rounding put tc past every part: the last positive part
-            int lp = last_pos;
+            ff incl = mine;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
-            found = lp;
-            tw = ff{INFINITY, 0.0f};
+            for (int o = 1; o < 32; o <<= 1) {
+                const ff y = ff_shfl_up(incl, o);
+                if (lane >= o) incl = ff_add(y, incl);
+            }
+            const ff tc = sh.tc;
+            const bool tc_inf = isinf(tc.hi);
+            const unsigned hit = __ballot_sync(FULL, !tc_inf && ff_gt(incl, tc));
+            int found = -1;
+            ff tw{INFINITY, 0.0f};
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                if (lane == l) {
+                    ff t = ff_add(tc, ff_neg(ff_add(incl, ff_neg(mine))));
+                    for (int i = i0; i < i1; ++i) {
+                        const float v = part_val(i);
+                        if (ff_gt(ff_from(v), t)) { found = i; tw = t; break; }
+                        t = ff_add(t, -v);
+                    }
+                    if (found < 0) found = last_pos;  // rounding: this run's last positive part
+                }
+                found = __shfl_sync(FULL, found, l);
+                tw = ff_shfl(tw, l);
+            }
+            if (found < 0) {  // rounding put tc past every part: the last positive part
+                int lp = last_pos;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(FULL, lp, o));
+                found = lp;
+                tw = ff{INFINITY, 0.0f};
+            }
+            if (lane == 0) {
+                sh.found = found;
+                sh.tw = tw;
+            }
         }
+        __syncthreads();
+        // Inverse CDF inside the part: warp k takes its k-th step of 32 slots
+        // (all loaded at once); the first step whose running mass passes tw
+        // holds the token.
+        const int found = sh.found;
+        constexpr int STEPS = P2_SLOTS / 32;
         if (found >= 0) {
+            const int P = n_chunks + 2;
             int q0, n;
             if (found == 0) { q0 = sl.edge_lo; n = 1; }
             else if (found == P - 1) { q0 = sl.edge_hi; n = 1; }
@@ -1399,8 +1402,36 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 q0 = sl.ia + (found - 1) * P2_SLOTS;
                 n = min(P2_SLOTS, sl.ib - q0);
             }
-            const int token = warp_draw_search<TT, TD>(src, w, q0, n, tw, lane);
-            if (lane == 0) p.out_tokens[(size_t)b * (K + 1) + j] = token;
+            const ff tw = sh.tw;
+            const bool tw_inf = isinf(tw.hi);
+            DrawStep<TT, TD> st;
+            if (warp < STEPS) {
+                st.load(src, w, q0, n, warp, lane);
+                if (lane == 0) {
+                    sh.step_tot[warp] = st.tot;
+                    sh.step_lp[warp] = st.last_pos;
+                }
+            }
+            __syncthreads();
+            ff run = ff_from(0.0f);
+            if (warp < STEPS) {
+                for (int k = 0; k < warp; ++k) run = ff_add(run, sh.step_tot[k]);
+                const unsigned hit = __ballot_sync(FULL, !tw_inf && ff_gt(ff_add(run, st.incl), tw));
+                if (lane == 0) sh.step_hit[warp] = hit ? __ffs(hit) - 1 : -1;
+            }
+            __syncthreads();
+            int kstar = -1;
+            for (int k = STEPS - 1; k >= 0; --k)
+                if (sh.step_hit[k] >= 0) kstar = k;
+            if (kstar >= 0 && warp == kstar) {
+                const int l = sh.step_hit[kstar];
+                const int token = st.walk(run, tw, l);
+                if (lane == l) p.out_tokens[(size_t)b * (K + 1) + j] = token;
+            } else if (kstar < 0 && tid == 0) {
+                int lp = -1;  // tw past the part's mass: its last positive element
+                for (int k = 0; k < STEPS; ++k) lp = max(lp, sh.step_lp[k]);
+                p.out_tokens[(size_t)b * (K + 1) + j] = lp;
+            }
         }
     }
     wr.drain(sh);
