@@ -1007,6 +1007,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     }
     __syncthreads();
     const int total_chunks = mode_ok ? sh.total_chunks : 0;
+    // The next call on the stream may launch once every CTA of this one has
+    // started: its first pass then overlaps this call wherever SMs have room.
+    launch_dependents();
 
     WarpRing wr{warp, 0u, 0u};
     uint32_t seq = 0;  // chunks this warp has handled, over both passes
@@ -1030,7 +1033,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         }
     }
     __syncthreads();
-    launch_dependents();  // the next call on the stream may start streaming its inputs
     if (p.overlap_previous) grid_dependency_wait();
     // This CTA's partial of every row, pushed into every CTA of the cluster.
     for (int t = tid; mode_ok && t < CS * nrows; t += NTHREADS) {
