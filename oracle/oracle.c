@@ -312,7 +312,8 @@ int oracle_verify(const void* target, const void* draft,
                   int32_t* out_tokens, int32_t* out_n_accepted,
                   double* out_p_target, double* out_p_draft,
                   double* out_residual_mass, double* out_accept_margin,
-                  double* out_draw_margin, int32_t* out_fallback) {
+                  double* out_draw_margin, int32_t* out_fallback,
+                  const int32_t* draft_lens) {
     double* Pt = (double*)malloc(sizeof(double) * (size_t)V);
     double* Pd = (double*)malloc(sizeof(double) * (size_t)V);
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
@@ -334,12 +335,30 @@ int oracle_verify(const void* target, const void* draft,
         }
         seq_extra ex;
         int mode = modes ? modes[b] : ORC_SAMPLE;
-        int j = verify_sequence(
-            target, (size_t)b * (K + 1) * V, draft, (size_t)b * K * V, dtype_t,
-            dtype_d, draft_tokens + (size_t)b * K, K, V, mode, temperature, u, u2,
-            out_tokens + (size_t)b * (K + 1),
-            out_p_target ? out_p_target + (size_t)b * K : NULL,
-            out_p_draft ? out_p_draft + (size_t)b * K : NULL, &ex, Pt, Pd, r);
+        /* A sequence may verify fewer drafts than the layout holds: its own
+         * draft length Kb reads target rows 0..Kb and draft rows 0..Kb-1 of
+         * its block (continuous batching); positions past Kb emit -1. */
+        const int Kb = draft_lens ? draft_lens[b] : K;
+        int32_t* tok_b = out_tokens + (size_t)b * (K + 1);
+        for (int i = 0; i <= K; ++i) tok_b[i] = -1;
+        for (int i = 0; i < K; ++i) {
+            if (out_p_target) out_p_target[(size_t)b * K + i] = NAN;
+            if (out_p_draft) out_p_draft[(size_t)b * K + i] = NAN;
+        }
+        int j;
+        if (Kb < 0 || Kb > K) {
+            j = -1;
+            ex.accept_margin = INFINITY;
+            ex.draw_margin = INFINITY;
+            ex.residual_mass = NAN;
+            ex.fallback = 0;
+        } else {
+            j = verify_sequence(
+                target, (size_t)b * (K + 1) * V, draft, (size_t)b * K * V, dtype_t,
+                dtype_d, draft_tokens + (size_t)b * K, Kb, V, mode, temperature, u, u2,
+                tok_b, out_p_target ? out_p_target + (size_t)b * K : NULL,
+                out_p_draft ? out_p_draft + (size_t)b * K : NULL, &ex, Pt, Pd, r);
+        }
         out_n_accepted[b] = j;
         if (out_residual_mass) out_residual_mass[b] = ex.residual_mass;
         if (out_accept_margin) out_accept_margin[b] = ex.accept_margin;

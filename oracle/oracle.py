@@ -48,7 +48,7 @@ def _bind(path: str):
     lib.oracle_verify.argtypes = [
         P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_double, P, ctypes.c_uint64, P, P, ctypes.c_int, ctypes.c_int,
-        P, P, P, P, P, P, P, P]
+        P, P, P, P, P, P, P, P, P]
     lib.oracle_philox4x32_10.restype = None
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox_uniforms.restype = None
@@ -102,7 +102,7 @@ def philox_uniforms(seed: int, seq_ids, n_pos: int):
 
 
 def verify(target, draft, draft_tokens, temperature=1.0, modes=SAMPLE, seed=0, seq_ids=None,
-           uniforms=None, threads=1, seq_range=None):
+           uniforms=None, threads=1, seq_range=None, draft_lens=None):
     """Run the oracle verify step.
 
     target [B, K+1, V] and draft [B, K, V]: float32, float64 or uint16 (bf16
@@ -110,6 +110,8 @@ def verify(target, draft, draft_tokens, temperature=1.0, modes=SAMPLE, seed=0, s
     [B, K] int. modes: 0/1 or an array [B]. uniforms: optional (u, u2), each
     [B, K+1], replacing the Philox draws. seq_range=(b0, b1) restricts the
     work to those sequences (the other outputs stay at their fill values).
+    draft_lens: optional [B] ints, sequence b verifying only its first
+    draft_lens[b] drafts (0..K; other values make it invalid).
     Returns a dict of numpy arrays.
     """
     lib = _load()
@@ -126,6 +128,7 @@ def verify(target, draft, draft_tokens, temperature=1.0, modes=SAMPLE, seed=0, s
         assert not modes_arr.any(), "sample mode needs draft logits"
         dtype_d = F32
     ids = None if seq_ids is None else np.ascontiguousarray(seq_ids, dtype=np.uint64)
+    lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, dtype=np.int32).reshape(B)
     uni = None
     if uniforms is not None:
         uni = np.ascontiguousarray(np.stack([np.asarray(uniforms[0], dtype=np.float64).reshape(B, K1),
@@ -148,7 +151,7 @@ def verify(target, draft, draft_tokens, temperature=1.0, modes=SAMPLE, seed=0, s
             float(temperature), _ptr(modes_arr), ctypes.c_uint64(seed), _ptr(ids), _ptr(uni),
             lo, hi, _ptr(out["tokens"]), _ptr(out["n_accepted"]), _ptr(out["p_target"]),
             _ptr(out["p_draft"]), _ptr(out["residual_mass"]), _ptr(out["accept_margin"]),
-            _ptr(out["draw_margin"]), _ptr(out["fallback"]))
+            _ptr(out["draw_margin"]), _ptr(out["fallback"]), _ptr(lens))
         if rc != 0:
             raise MemoryError("oracle_verify could not allocate its work buffers")
 

@@ -488,3 +488,42 @@ def test_lmhead_logits_c_loop_matches_float64_matmul():
     c = h.double().numpy() @ w.double().numpy()
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(a, c, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_ragged_draft_lengths_equal_separate_fixed_k_calls(mode):
+    """Continuous batching: a sequence that verifies only its first Kb of the
+    layout's K drafts gives exactly the result of a call laid out with K = Kb
+    (same Philox stream: the same sequence id); positions past Kb emit -1."""
+    rng = np.random.default_rng(7)
+    B, K, V = 7, 5, 40
+    tgt = rng.normal(0, 2, (B, K + 1, V))
+    drf = tgt[:, :K] + rng.normal(0, 1, (B, K, V))
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    lens = np.array([0, 1, 2, 3, 4, 5, 2], dtype=np.int32)
+    got = orc.verify(tgt, drf, tok, 1.0, mode, seed=11, draft_lens=lens)
+    for b in range(B):
+        k = int(lens[b])
+        one = orc.verify(np.ascontiguousarray(tgt[b:b + 1, :k + 1]),
+                         np.ascontiguousarray(drf[b:b + 1, :k]) if mode else None,
+                         np.ascontiguousarray(tok[b:b + 1, :k]), 1.0, mode, seed=11, seq_ids=[b])
+        assert got["n_accepted"][b] == one["n_accepted"][0]
+        assert (got["tokens"][b, :k + 1] == one["tokens"][0]).all()
+        assert (got["tokens"][b, k + 1:] == -1).all()
+        if mode:
+            assert np.isnan(got["p_target"][b, k:]).all()
+
+
+def test_ragged_full_lengths_equal_the_fixed_layout_and_bad_lengths_are_invalid():
+    rng = np.random.default_rng(8)
+    B, K, V = 5, 4, 30
+    tgt = rng.normal(0, 2, (B, K + 1, V))
+    drf = tgt[:, :K] + rng.normal(0, 1, (B, K, V))
+    tok = rng.integers(0, V, (B, K)).astype(np.int32)
+    a = orc.verify(tgt, drf, tok, 1.0, 1, seed=3)
+    b = orc.verify(tgt, drf, tok, 1.0, 1, seed=3, draft_lens=np.full(B, K))
+    assert (a["tokens"] == b["tokens"]).all() and (a["n_accepted"] == b["n_accepted"]).all()
+    c = orc.verify(tgt, drf, tok, 1.0, 1, seed=3, draft_lens=[K, -1, K + 1, 0, K])
+    assert list(c["n_accepted"][[1, 2]]) == [-1, -1]
+    assert (c["tokens"][[1, 2]] == -1).all()
+    assert c["n_accepted"][3] == 0 and c["tokens"][3, 0] >= 0 and (c["tokens"][3, 1:] == -1).all()
