@@ -87,8 +87,9 @@ typedef enum {
     SV_FLAG_DRAW_EDGE = 8u,        /* a draw landed past the summed mass (rounding)*/
     SV_FLAG_BAD_MODE = 16u,        /* a per-sequence mode that is neither greedy nor
                                       sample, or sample mode without draft logits  */
-    SV_FLAG_TIMEOUT = 32u          /* a bounded wait inside the kernel gave up; the
+    SV_FLAG_TIMEOUT = 32u,         /* a bounded wait inside the kernel gave up; the
                                       sequence is reported invalid                 */
+    SV_FLAG_BAD_LENGTH = 64u       /* a per-sequence draft length outside [0, K]   */
 } sv_device_flag;
 
 /* Batched verify over logits already in device memory.
@@ -142,6 +143,12 @@ typedef struct {
                                     else 1, 2, 4, 8 or 16                         */
     sv_stream_t stream;
     uint32_t flags;              /* SV_ARG_* bits, 0 for none                     */
+    const int32_t* draft_lens;   /* [B] int32 (device) or NULL: sequence b verifies
+                                    only its first draft_lens[b] drafts (0..K;
+                                    continuous batching). It reads target rows
+                                    0..Kb and draft rows 0..Kb-1 of its block and
+                                    writes -1 / NaN past Kb; a value outside
+                                    [0, K] makes the sequence invalid            */
 } sv_verify_args;
 
 /* sv_verify_args.flags: the inputs of this call are not written by the work

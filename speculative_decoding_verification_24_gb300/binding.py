@@ -26,6 +26,7 @@ SV_FLAG_RESIDUAL_FALLBACK = 4
 SV_FLAG_DRAW_EDGE = 8
 SV_FLAG_BAD_MODE = 16
 SV_FLAG_TIMEOUT = 32
+SV_FLAG_BAD_LENGTH = 64
 SV_ARG_OVERLAP_PREVIOUS = 1
 SV_ERR_SCRATCH_LIMIT = 12
 SV_LMHEAD_SCRATCH_BYTES = 32 << 20  # include/specverify.h
@@ -70,6 +71,7 @@ class sv_verify_args(ctypes.Structure):
         ("cluster_size", ctypes.c_int),
         ("stream", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
+        ("draft_lens", ctypes.c_void_p),
     ]
 
 
@@ -189,12 +191,13 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=1.0, mode
 def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, modes="sample",
                    seed=0, seq_ids=None, out_tokens=None, out_n_accepted=None, out_p_target=None,
                    out_p_draft=None, out_residual_mass=None, status_word=None, cluster_size=0,
-                   stream=None, debug=False, overlap_previous=False):
+                   stream=None, debug=False, overlap_previous=False, draft_lens=None):
     """Verify with per-sequence modes ([B] int32 tensor, or 'greedy'/'sample'
     for all), explicit Philox sequence ids and optional debug outputs.
     debug=True allocates out_p_target, out_p_draft, out_residual_mass and
     status_word. overlap_previous=True sets SV_ARG_OVERLAP_PREVIOUS (the
     inputs are not written by the work just before this call on the stream).
+    draft_lens: optional [B] int32 device tensor of per-sequence draft counts.
     Returns a dict of the output tensors."""
     B, K1, V = target_logits.shape
     K = K1 - 1
@@ -235,6 +238,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     a.status_word = _ptr(status_word)
     a.cluster_size = int(cluster_size)
     a.flags = SV_ARG_OVERLAP_PREVIOUS if overlap_previous else 0
+    a.draft_lens = _ptr(draft_lens)
     with torch.cuda.device(dev):
         a.stream = _stream(stream, dev)
         st = _load().spec_verify_ex(ctypes.byref(a))

@@ -81,6 +81,7 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     if (!aligned(a->target_logits, es_t) || (a->draft_logits && !aligned(a->draft_logits, es_d)) ||
         !aligned(a->draft_tokens, 4) || !aligned(a->out_tokens, 4) || !aligned(a->out_n_accepted, 4) ||
         (a->modes && !aligned(a->modes, 4)) || (a->seq_ids && !aligned(a->seq_ids, 8)) ||
+        (a->draft_lens && !aligned(a->draft_lens, 4)) ||
         (a->out_p_target && !aligned(a->out_p_target, 4)) ||
         (a->out_p_draft && !aligned(a->out_p_draft, 4)) ||
         (a->out_residual_mass && !aligned(a->out_residual_mass, 4)) ||
@@ -123,6 +124,7 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     p.out_residual_mass = a->out_residual_mass;
     p.status_word = a->status_word;
     p.overlap_previous = (a->flags & SV_ARG_OVERLAP_PREVIOUS) != 0;
+    p.draft_lens = a->draft_lens;
     cudaError_t e = sv::launch_verify_logits(p, (int)dtype_t, (int)dtype_d, cs, (cudaStream_t)a->stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return SV_OK;

@@ -26,6 +26,7 @@ struct VerifyParams {
     float* out_residual_mass;  // [B] or nullptr
     uint32_t* status_word;     // or nullptr
     int overlap_previous;      // inputs not written by the previous work on the stream
+    const int32_t* draft_lens; // [B] per-sequence draft counts (0..K) or nullptr (all K)
 };
 
 // CTAs per cluster chosen from the shape when the caller asks for automatic.

@@ -407,14 +407,16 @@ struct RowInfo {
 
 __device__ __forceinline__ int row_c0(const RowInfo* rows, int r) { return r == 0 ? 0 : rows[r - 1].c1; }
 
-// Row r of sequence b: target row r (r <= K) or draft row r - K - 1.
+// Target row i and draft row i of sequence b in the [B, K+1, V] and [B, K, V]
+// layouts. A sequence verifying Kb <= K drafts reads its rows 0..Kb and
+// 0..Kb-1; its row table numbers them 0..Kb (target) then Kb+1..2Kb (draft).
 template <typename TT>
-__device__ __forceinline__ const TT* target_row(const TT* tgt, int b, int K, int V, int r) {
-    return tgt + ((size_t)b * (K + 1) + r) * V;
+__device__ __forceinline__ const TT* target_row(const TT* tgt, int b, int K, int V, int i) {
+    return tgt + ((size_t)b * (K + 1) + i) * V;
 }
 template <typename TD>
-__device__ __forceinline__ const TD* draft_row(const TD* drf, int b, int K, int V, int r) {
-    return drf + ((size_t)b * K + (r - K - 1)) * V;
+__device__ __forceinline__ const TD* draft_row(const TD* drf, int b, int K, int V, int i) {
+    return drf + ((size_t)b * K + i) * V;
 }
 
 // E_TT consecutive elements of a TD row starting at element i0, in the slot
@@ -900,17 +902,18 @@ __device__ __forceinline__ float2 edge_row(SeqShared& sh, const T* row, const Ro
 // Partial slots at the two ends of this CTA's slices (warp 0).
 template <typename TT, typename TD, bool SAMPLE>
 __device__ __forceinline__ void edge_pass1(SeqShared& sh, const TT* tgt, const TD* drf, int b, int K,
-                                           int V, int nrows, float c, int lane,
+                                           int Kb, int V, int nrows, float c, int lane,
                                            cg::cluster_group& cluster, int CS, int x_reg) {
     for (int r = 0; r < nrows; ++r) {
         const RowInfo ri = sh.rows[r];
         float2 part;
         if (ri.edge_lo < 0 && ri.edge_hi < 0) {
             part = SAMPLE ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
-        } else if (r <= K) {
-            part = edge_row<TT, SAMPLE>(sh, target_row(tgt, b, K, V, r), ri, r, K, V, c, lane, cluster, CS, x_reg);
+        } else if (r <= Kb) {
+            part = edge_row<TT, SAMPLE>(sh, target_row(tgt, b, K, V, r), ri, r, Kb, V, c, lane, cluster, CS, x_reg);
         } else {
-            part = edge_row<TD, SAMPLE>(sh, draft_row(drf, b, K, V, r), ri, r, K, V, c, lane, cluster, CS, x_reg);
+            part = edge_row<TD, SAMPLE>(sh, draft_row(drf, b, K, V, r - Kb - 1), ri, r, Kb, V, c, lane, cluster,
+                                        CS, x_reg);
         }
         if (lane == 0) sh.edge_part[r] = part;
     }
@@ -969,9 +972,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // read until then (outputs are written after the wait below pass 1).
     if (!p.overlap_previous) grid_dependency_wait();
     const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
-    const bool mode_ok = (mode == 0 || mode == 1) && !(mode == 1 && drf == nullptr);
+    // Kb: the drafts this sequence verifies (continuous batching), 0..K
+    const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
+    const bool len_ok = Kb >= 0 && Kb <= K;
+    const bool mode_ok = (mode == 0 || mode == 1) && !(mode == 1 && drf == nullptr) && len_ok;
     const bool sample = mode == 1 && mode_ok;
-    const int nrows = sample ? 2 * K + 1 : K + 1;
+    const int nrows = mode_ok ? (sample ? 2 * Kb + 1 : Kb + 1) : 0;
     const float c = p.c;
 
     if (tid == 0) {
@@ -981,8 +987,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         fence_barrier_init();
     }
     if (mode_ok && tid < nrows)
-        sh.rows[tid] = tid <= K ? make_row_info<TT>(target_row(tgt, b, K, V, tid), V, rank, CS)
-                                : make_row_info<TD>(draft_row(drf, b, K, V, tid), V, rank, CS);
+        sh.rows[tid] = tid <= Kb ? make_row_info<TT>(target_row(tgt, b, K, V, tid), V, rank, CS)
+                                 : make_row_info<TD>(draft_row(drf, b, K, V, tid - Kb - 1), V, rank, CS);
     for (int t = tid; t < NCW * MAX_ROWS; t += NTHREADS) {
         const int w = t / MAX_ROWS, r = t % MAX_ROWS;
         sh.warp_part[w][r] = sample ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
@@ -1015,21 +1021,21 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     uint32_t seq = 0;  // chunks this warp has handled, over both passes
     // Lane i of every warp holds draft token x_i (first used after the
     // warp's first chunk has arrived, so the load overlaps the copies).
-    const int x_reg = lane < K ? __ldg(p.tokens + (size_t)b * K + lane) : -1;
+    const int x_reg = (mode_ok && lane < Kb) ? __ldg(p.tokens + (size_t)b * K + lane) : -1;
 
     // ---------------- pass 1: row partials over this CTA's slice ----------------
     // Warp 0 draws the Philox uniforms of positions 0..K while its first
     // copies are in flight; the decision reads them from shared memory.
     const uint64_t seqid = (sample && warp == 0 && p.seq_ids) ? __ldg(p.seq_ids + b) : (uint64_t)b;
     auto draw_uniforms = [&] {
-        if (warp == 0 && lane <= K) position_uniforms(p.seed, seqid, (uint32_t)lane, sh.u_pos[lane], sh.u2_pos[lane]);
+        if (warp == 0 && lane <= Kb) position_uniforms(p.seed, seqid, (uint32_t)lane, sh.u_pos[lane], sh.u2_pos[lane]);
     };
     if (mode_ok) {
-        if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, K, x_reg, draw_uniforms);
-        else stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, K, x_reg, [] {});
+        if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
+        else stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
         if (warp == 0) {
-            if (sample) edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
-            else edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, V, nrows, c, lane, cluster, CS, x_reg);
+            if (sample) edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+            else edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
         }
     }
     __syncthreads();
@@ -1083,14 +1089,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             }
         }
         float u = 0.0f, u2 = 0.0f;
-        if (sample && lane <= K) {
+        if (sample && lane <= Kb) {
             u = sh.u_pos[lane];
             u2 = sh.u2_pos[lane];
         }
         int x = -1;
         bool bad_token = false, rej = false;
         float et = 0.0f, ed = 0.0f, St = 1.0f, Sd = 1.0f;
-        if (lane < K) {
+        if (mode_ok && lane < Kb) {
             x = x_reg;
             bad_token = x < 0 || x >= V;
             if (!bad_token && mode_ok) {
@@ -1098,7 +1104,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                     rej = x != as_arg(sh.merged[lane]).i;
                 } else {
                     const SoftPart st = as_soft(sh.merged[lane]);
-                    const SoftPart sd = as_soft(sh.merged[K + 1 + lane]);
+                    const SoftPart sd = as_soft(sh.merged[Kb + 1 + lane]);
                     // the logits at x, captured during pass 1 by the CTA holding them
                     et = ex2(fmaf(sh.lt_x[lane], c, -st.R));
                     ed = ex2(fmaf(sh.ld_x[lane], c, -sd.R));
@@ -1111,7 +1117,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         const bool any_bad_token = __any_sync(FULL, bad_token);
         const bool invalid = __any_sync(FULL, bad) || any_bad_token;
         const unsigned rejm = __ballot_sync(FULL, rej);
-        const int j = rejm ? __ffs(rejm) - 1 : K;
+        const int j = rejm ? __ffs(rejm) - 1 : Kb;
         const float u2j = __shfl_sync(FULL, u2, j);
         if (lane == 0) {
             sh.j = j;
@@ -1120,8 +1126,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             sh.u2 = u2j;
             if (sample && !invalid) {
                 sh.st = as_soft(sh.merged[j]);
-                sh.use_d = j < K;
-                sh.sd = j < K ? as_soft(sh.merged[K + 1 + j]) : SoftPart{-INFINITY, 0.0f};
+                sh.use_d = j < Kb;
+                sh.sd = j < Kb ? as_soft(sh.merged[Kb + 1 + j]) : SoftPart{-INFINITY, 0.0f};
             }
         }
         if (rank == 0) {
@@ -1136,13 +1142,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             if (lane == 0) p.out_n_accepted[b] = invalid ? -1 : j;
             if (lane < K) {
                 const float qnan = __int_as_float(0x7fc00000);
-                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = (sample && !invalid) ? et / St : qnan;
-                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = (sample && !invalid) ? ed / Sd : qnan;
+                const bool tested = sample && !invalid && lane < Kb;
+                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = tested ? et / St : qnan;
+                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = tested ? ed / Sd : qnan;
             }
             if (lane == 0 && (!sample || invalid) && p.out_residual_mass)
                 p.out_residual_mass[b] = __int_as_float(0x7fc00000);
             if (lane == 0 && p.status_word && invalid)
-                atomicOr(p.status_word, !mode_ok       ? (unsigned)SV_FLAG_BAD_MODE
+                atomicOr(p.status_word, !len_ok        ? (unsigned)SV_FLAG_BAD_LENGTH
+                                        : !mode_ok     ? (unsigned)SV_FLAG_BAD_MODE
                                         : any_bad_token ? (unsigned)SV_FLAG_BAD_TOKEN
                                                         : (unsigned)SV_FLAG_BAD_ROW);
             if (lane == 0 && p.status_word && sh.err) atomicOr(p.status_word, (unsigned)SV_FLAG_TIMEOUT);
@@ -1184,7 +1192,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // instead of HBM.
     const RowInfo rt = sh.rows[j];
     const bool resident_t = total_chunks <= NSTAGE && rt.ia == sl.ia && rt.ib == sl.ib;
-    const int rd_row = sh.use_d ? K + 1 + j : j;
+    const int rd_row = sh.use_d ? Kb + 1 + j : j;
     const RowInfo rd = sh.rows[rd_row];
     const int rt_c0 = row_c0(sh.rows, j), rd_c0 = row_c0(sh.rows, rd_row);
     const bool resident_d = resident_t && draft_in_ring && rd.ia == sl.ia && rd.ib == sl.ib;

@@ -14,7 +14,7 @@ import torch
 import synth
 from oracle import oracle as orc
 from oracle.parity import compare, compare_probabilities, near_ties
-from speculative_decoding_verification_24_gb300 import spec_verify, spec_verify_ex
+from speculative_decoding_verification_24_gb300 import binding, spec_verify, spec_verify_ex
 from speculative_decoding_verification_24_gb300.build import build
 from synth.workloads import to_numpy_logits
 
@@ -299,3 +299,44 @@ def test_overlapping_calls_match_serial_calls():
     for i, out in outs:
         assert torch.equal(out["tokens"], want[i][0]) and torch.equal(out["n_accepted"], want[i][1])
     assert torch.equal(shared_t, want[-1][0]) and torch.equal(shared_n, want[-1][1])
+
+
+@pytest.mark.parametrize("name,dtype_case", [("c2", "f32"), ("c3", "bf16")])
+def test_ragged_draft_lengths(name, dtype_case):
+    """Per-sequence draft counts in one launch (0..K, including 0 and K);
+    rows past a sequence's count hold NaN and must not be read."""
+    case = synth.make_workload(name, seed=61, device="cuda", **({"tau": 1.0} if name == "c2" else {}))
+    B, K1, V = case.target.shape
+    K = K1 - 1
+    g = torch.Generator().manual_seed(5)
+    lens = torch.randint(0, K + 1, (B,), generator=g, dtype=torch.int32)
+    lens[0], lens[-1] = 0, K
+    target, draft = case.target.clone(), case.draft.clone()
+    for b in range(B):
+        target[b, int(lens[b]) + 1:] = float("nan")
+        draft[b, int(lens[b]):] = float("nan")
+    lens_d = lens.cuda()
+    out = spec_verify_ex(target, draft, case.tokens, case.temperature, modes=case.modes, seed=9,
+                         debug=True, draft_lens=lens_d)
+    torch.cuda.synchronize()
+    ref = orc.verify(to_numpy_logits(target), to_numpy_logits(draft), case.tokens.cpu().numpy(),
+                     case.temperature, case.modes.cpu().numpy(), seed=9, threads=THREADS,
+                     draft_lens=lens.numpy())
+    g_out = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in out.items()}
+    assert (ref["n_accepted"] >= 0).all() and (ref["n_accepted"] <= lens.numpy()).all()
+    check(g_out, ref, label=f"ragged {name}")
+    assert int(g_out["status_word"][0]) == 0
+
+
+def test_ragged_length_out_of_range_is_flagged():
+    case = synth.make_workload("c2", seed=62, device="cuda", tau=1.0)
+    B, K1, _ = case.target.shape
+    lens = torch.full((B,), K1 - 1, dtype=torch.int32)
+    lens[1], lens[2] = -1, K1
+    out = spec_verify_ex(case.target, case.draft, case.tokens, case.temperature, modes="sample",
+                         seed=1, debug=True, draft_lens=lens.cuda())
+    torch.cuda.synchronize()
+    n = out["n_accepted"].cpu()
+    assert n[1] == -1 and n[2] == -1 and (n[[0, 3]] >= 0).all()
+    assert (out["tokens"].cpu()[[1, 2]] == -1).all()
+    assert int(out["status_word"].cpu()[0]) & binding.SV_FLAG_BAD_LENGTH
