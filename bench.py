@@ -203,6 +203,24 @@ def min_bytes(case) -> int:
     return B * K1 * V * s + n_sample * (K1 - 1) * V * s
 
 
+# ----------------------------------------------------------------- ranks
+
+
+def shard_seq_ids(rank: int, B: int, device) -> torch.Tensor:
+    """Global Philox sequence ids of rank `rank`'s shard of B sequences: the
+    ranks verify disjoint slices of one global batch, so N ranks draw exactly
+    what one GPU would for the whole batch (no collective on the data path)."""
+    return torch.arange(rank * B, (rank + 1) * B, dtype=torch.int64, device=device)
+
+
+def max_over_ranks(x: float, device, world: int) -> float:
+    """The largest value over the ranks (the slowest rank's time)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------- our arm
 
 
@@ -217,11 +235,12 @@ def uniform_mode(modes: torch.Tensor):
     return modes
 
 
-def time_device(sets, steps, warmup, stream, seed0=0):
+def time_device(sets, steps, warmup, stream, seed0=0, rank=0):
     from speculative_decoding_verification_24_gb300 import spec_verify_ex
 
     B, K1, _ = sets[0].target.shape
     dev = sets[0].target.device
+    seq_ids = shard_seq_ids(rank, B, dev)
     out_tok = torch.empty(steps + warmup, B, K1, dtype=torch.int32, device=dev)
     out_n = torch.empty(steps + warmup, B, dtype=torch.int32, device=dev)
 
@@ -230,8 +249,8 @@ def time_device(sets, steps, warmup, stream, seed0=0):
     def step(i):
         c = sets[i % len(sets)]
         spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=modes[i % len(sets)],
-                       seed=seed0 + i, out_tokens=out_tok[i], out_n_accepted=out_n[i], stream=stream,
-                       overlap_previous=True)
+                       seed=seed0 + i, seq_ids=seq_ids, out_tokens=out_tok[i], out_n_accepted=out_n[i],
+                       stream=stream, overlap_previous=True)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -273,7 +292,7 @@ def run_ours(args, rank, world, device):
     B, K1, V = case0.target.shape
     rows_per_step = B * K1
     stream = torch.cuda.Stream(device)
-    step, out_n = time_device(sets, args.steps, args.warmup, stream, seed0=1000 * rank)
+    step, out_n = time_device(sets, args.steps, args.warmup, stream, rank=rank)
 
     # The timed steps replay from one CUDA graph (launch overhead of the
     # Python binding off the device timeline); the eager number is reported too.
@@ -316,10 +335,7 @@ def run_ours(args, rank, world, device):
                     for i in range(args.warmup, args.warmup + args.steps))
     bytes_min = sum(min_bytes(sets[i % len(sets)])
                     for i in range(args.warmup, args.warmup + args.steps))
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, device, world)
     value = world * rows_per_step * args.steps / (ms_max / 1e3)
     gbs = bytes_alg / (ms / 1e3) / 1e9
     peak, peak_src = measured_peaks()
@@ -343,7 +359,8 @@ def run_ours(args, rank, world, device):
             "B": B, "K": K1 - 1, "V": V, "rows_per_step": rows_per_step,
             "l2": f"inputs rotate over {len(sets)} seeded sets "
                   f"({len(sets) * set_bytes / 2**20:.0f} MiB > 2 x L2 of {l2 / 2**20:.0f} MiB)",
-            "parallelism": f"replicas x{world} (sequences shard with no collective)",
+            "parallelism": f"dp x{world}: each rank verifies its own shard of sequences "
+                           "(global Philox ids), no collective on the data path",
         },
         "hbm_gbs": gbs,
         "hbm_bytes_per_step": bytes_alg / args.steps,
@@ -428,10 +445,7 @@ def run_e2e(args, sets, device, stream, world):
     stop.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(stop)
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    value = world * B * K1 * args.steps / (float(t.item()) / 1e3)
+    value = world * B * K1 * args.steps / (max_over_ranks(ms, device, world) / 1e3)
     return {"value": value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "how": "pinned host inputs copied to the device, spec_verify_ex, results copied "
