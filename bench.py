@@ -235,7 +235,7 @@ def uniform_mode(modes: torch.Tensor):
     return modes
 
 
-def time_device(sets, steps, warmup, stream, seed0=0, rank=0):
+def time_device(sets, steps, warmup, stream, seed0=0, rank=0, overlap=True):
     from speculative_decoding_verification_24_gb300 import spec_verify_ex
 
     B, K1, _ = sets[0].target.shape
@@ -250,7 +250,7 @@ def time_device(sets, steps, warmup, stream, seed0=0, rank=0):
         c = sets[i % len(sets)]
         spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=modes[i % len(sets)],
                        seed=seed0 + i, seq_ids=seq_ids, out_tokens=out_tok[i], out_n_accepted=out_n[i],
-                       stream=stream, overlap_previous=True)
+                       stream=stream, overlap_previous=overlap)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -329,6 +329,13 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     eager_ms = e_start.elapsed_time(e_stop)
 
+    # the same steps with no overlap between calls (each waits for the last)
+    serial_step, _ = time_device(sets, args.steps, args.warmup, stream, rank=rank, overlap=False)
+    serial_graph = capture(serial_step, args.warmup, args.steps, stream)
+    replay_ms(serial_graph, stream)
+    serial_ms = max_over_ranks(replay_ms(serial_graph, stream), device, world)
+    del serial_graph
+
     # exact algorithmic bytes of every timed step, from its own outputs
     n_all = out_n.cpu().numpy()
     bytes_alg = sum(alg_bytes(sets[i % len(sets)], n_all[i])
@@ -386,6 +393,11 @@ def run_ours(args, rank, world, device):
                   "(programmatic dependent launch: a step may stream its inputs while the "
                   "previous step finishes; it writes its outputs after that step completes)",
         "eager_rows_per_s": world * rows_per_step * args.steps / (eager_ms / 1e3),
+        "serial": {"ms_per_step": serial_ms / args.steps,
+                   "rows_per_s": world * rows_per_step * args.steps / (serial_ms / 1e3),
+                   "hbm_gbs": bytes_alg / (serial_ms / 1e3) / 1e9,
+                   "how": "the same graph of K steps launched without SV_ARG_OVERLAP_PREVIOUS: "
+                          "each call starts after the previous one has completed"},
     }
     result["e2e"] = run_e2e(args, sets, device, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -498,6 +510,12 @@ def other_workloads(args, device, l2, stream):
             graph = capture(step, args.warmup, steps, stream)
             replay_ms(graph, stream)
             ms = replay_ms(graph, stream)
+            del graph
+            serial_step, _ = time_device(sets, steps, args.warmup, stream, overlap=False)
+            graph = capture(serial_step, args.warmup, steps, stream)
+            replay_ms(graph, stream)
+            serial_ms = replay_ms(graph, stream)
+            del graph
             n_all = out_n.cpu().numpy()
             ba = sum(alg_bytes(sets[i % len(sets)], n_all[i])
                      for i in range(args.warmup, args.warmup + steps))
@@ -511,6 +529,8 @@ def other_workloads(args, device, l2, stream):
                          "rows_per_s": B * K1 * steps / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
                          "hbm_gbs": gbs, "frac_of_measured_peak": gbs / peak,
                          "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+                         "serial_us_per_step": serial_ms * 1e3 / steps,
+                         "serial_frac_of_measured_peak": ba / (serial_ms / 1e3) / 1e9 / peak,
                          "input_sets": len(sets)}
             del sets
             torch.cuda.empty_cache()

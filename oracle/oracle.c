@@ -369,6 +369,71 @@ int oracle_verify(const void* target, const void* draft,
     return 0;
 }
 
+/* Greedy tree verification ("Inference-4", section "Medusa": the candidate
+ * continuations form a tree, all of them are verified in one forward pass,
+ * and the longest accepted path is kept). Node 0 is the root (the last
+ * committed token); node i > 0 carries token tokens[i] and has parent
+ * parents[i] < i; target row i is the target's distribution after the prefix
+ * that ends at node i. With the greedy rule a node is accepted when its
+ * parent is and its token is the argmax of its parent's row. The kept path
+ * ends at the deepest accepted node (lowest index among equally deep ones);
+ * the output is the path's tokens followed by the argmax of that node's row.
+ * Layout: target [B, N, V], tokens and parents [B, N]; outputs tokens [B, N]
+ * (-1 padded), n_accepted [B] (the path length, -1 for an invalid sequence:
+ * a parent outside [0, i), a token outside [0, V) on a tested node, or a row
+ * without a finite maximum) and last_node [B]. */
+int oracle_verify_tree(const void* target, int dtype, const int32_t* tokens,
+                       const int32_t* parents, int B, int N, int V,
+                       int b_begin, int b_end, int32_t* out_tokens,
+                       int32_t* out_n_accepted, int32_t* out_last_node) {
+    int* am = (int*)malloc(sizeof(int) * (size_t)N);
+    int* acc = (int*)malloc(sizeof(int) * (size_t)N);
+    int* depth = (int*)malloc(sizeof(int) * (size_t)N);
+    if (!am || !acc || !depth) {
+        free(am); free(acc); free(depth);
+        return -1;
+    }
+    for (int b = b_begin; b < b_end; ++b) {
+        const int32_t* tok = tokens + (size_t)b * N;
+        const int32_t* par = parents + (size_t)b * N;
+        int32_t* out = out_tokens + (size_t)b * N;
+        for (int i = 0; i < N; ++i) out[i] = -1;
+        out_n_accepted[b] = -1;
+        out_last_node[b] = -1;
+        int ok = 1;
+        for (int i = 1; i < N; ++i)
+            if (par[i] < 0 || par[i] >= i) ok = 0;
+        for (int i = 0; i < N && ok; ++i) {
+            size_t off = ((size_t)b * N + i) * V;
+            if (!row_valid(target, dtype, off, V)) ok = 0;
+            else row_max(target, dtype, off, V, &am[i]);
+        }
+        if (!ok) continue;
+        acc[0] = 1;
+        depth[0] = 0;
+        for (int i = 1; i < N; ++i) {
+            depth[i] = depth[par[i]] + 1;
+            acc[i] = 0;
+            if (acc[par[i]]) {
+                /* a tested node: its token is compared with its parent's argmax */
+                if (tok[i] < 0 || tok[i] >= V) ok = 0;
+                acc[i] = tok[i] == am[par[i]];
+            }
+        }
+        if (!ok) continue;
+        int best = 0;
+        for (int i = 1; i < N; ++i)
+            if (acc[i] && depth[i] > depth[best]) best = i;
+        const int n = depth[best];
+        for (int i = best, k = n - 1; i != 0; i = par[i], --k) out[k] = tok[i];
+        out[n] = am[best];
+        out_n_accepted[b] = n;
+        out_last_node[b] = best;
+    }
+    free(am); free(acc); free(depth);
+    return 0;
+}
+
 /* Logits of the fused LM-head variant: logits[m, v] = sum_k hidden[m, k] *
  * W[k, v] over bf16 inputs widened exactly, accumulated in double in k order.
  * hidden [M, d] and W [d, V] are raw bf16 bits; rows [m_begin, m_end) only. */

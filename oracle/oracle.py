@@ -49,6 +49,9 @@ def _bind(path: str):
         P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_double, P, ctypes.c_uint64, P, P, ctypes.c_int, ctypes.c_int,
         P, P, P, P, P, P, P, P, P]
+    lib.oracle_verify_tree.restype = ctypes.c_int
+    lib.oracle_verify_tree.argtypes = [P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, P, P, P]
     lib.oracle_philox4x32_10.restype = None
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox_uniforms.restype = None
@@ -162,6 +165,24 @@ def verify(target, draft, draft_tokens, temperature=1.0, modes=SAMPLE, seed=0, s
         bounds = np.linspace(b0, b1, threads + 1).astype(int)
         with ThreadPoolExecutor(threads) as pool:
             list(pool.map(lambda i: run(bounds[i], bounds[i + 1]), range(threads)))
+    return out
+
+
+def verify_tree(target, tokens, parents):
+    """Greedy tree verification. target [B, N, V] (float32, float64 or bf16
+    bits), tokens and parents [B, N] (parents[b, 0] is ignored: node 0 is the
+    root). Returns dict(tokens [B, N], n_accepted [B], last_node [B])."""
+    lib = _load()
+    target = np.ascontiguousarray(target)
+    B, N, V = target.shape
+    tok = np.ascontiguousarray(np.broadcast_to(np.asarray(tokens, dtype=np.int32), (B, N)))
+    par = np.ascontiguousarray(np.broadcast_to(np.asarray(parents, dtype=np.int32), (B, N)))
+    out = {"tokens": np.full((B, N), -1, dtype=np.int32), "n_accepted": np.full(B, -2, dtype=np.int32),
+           "last_node": np.full(B, -2, dtype=np.int32)}
+    rc = lib.oracle_verify_tree(_ptr(target), _dtype_code(target), _ptr(tok), _ptr(par), B, N, V, 0, B,
+                                _ptr(out["tokens"]), _ptr(out["n_accepted"]), _ptr(out["last_node"]))
+    if rc != 0:
+        raise MemoryError("oracle_verify_tree could not allocate its work buffers")
     return out
 
 

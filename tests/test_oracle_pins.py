@@ -527,3 +527,98 @@ def test_ragged_full_lengths_equal_the_fixed_layout_and_bad_lengths_are_invalid(
     assert list(c["n_accepted"][[1, 2]]) == [-1, -1]
     assert (c["tokens"][[1, 2]] == -1).all()
     assert c["n_accepted"][3] == 0 and c["tokens"][3, 0] >= 0 and (c["tokens"][3, 1:] == -1).all()
+
+
+# ----------------------------------------------------------------- tree verify
+
+
+def random_tree(rng, N, greedy_prefix, V, p_follow=0.5):
+    """A candidate tree of N nodes (node 0 the root): each new node hangs
+    under a random earlier node and carries, with probability p_follow, the
+    token plain greedy decoding emits there (if its parent is on the greedy
+    path), else a random token."""
+    parents = [-1]
+    tokens = [0]
+    on_path = [0]  # depth along the greedy path, or -1 off it
+    for i in range(1, N):
+        p = int(rng.integers(0, i))
+        parents.append(p)
+        d = on_path[p]
+        if d >= 0 and d < len(greedy_prefix) and rng.random() < p_follow:
+            tokens.append(greedy_prefix[d])
+            on_path.append(d + 1)
+        else:
+            t = int(rng.integers(0, V))
+            tokens.append(t)
+            on_path.append(d + 1 if d >= 0 and d < len(greedy_prefix) and t == greedy_prefix[d] else -1)
+    return np.array(tokens, np.int32), np.array(parents, np.int32)
+
+
+def node_context(prompt, tokens, parents, i):
+    path = []
+    while i != 0:
+        path.append(int(tokens[i]))
+        i = int(parents[i])
+    return list(prompt) + path[::-1]
+
+
+@pytest.mark.parametrize("N,V", [(8, 6), (24, 30), (32, 500)])
+def test_tree_verify_equals_plain_greedy_decoding(N, V):
+    """'Inference-4', section 'Medusa': every candidate in the tree is
+    verified in one pass and the longest accepted path is kept. With the
+    greedy rule the kept tokens plus the next one must be exactly what plain
+    greedy decoding of the target emits, and the path must be the longest one
+    whose tokens all follow plain greedy decoding (by brute force)."""
+    rng = np.random.default_rng(N * 1000 + V)
+    for trial in range(20):
+        prompt = [int(t) for t in rng.integers(0, V, 4)]
+        greedy = plain_greedy(prompt, N, V)[len(prompt):]
+        tokens, parents = random_tree(rng, N, greedy, V)
+        target = np.stack([toy_target_logits(node_context(prompt, tokens, parents, i), V) for i in range(N)])
+        out = orc.verify_tree(target[None], tokens[None], parents[None])
+        n = int(out["n_accepted"][0])
+        assert out["tokens"][0, :n + 1].tolist() == greedy[:n + 1]
+        assert (out["tokens"][0, n + 1:] == -1).all()
+        # brute force: the deepest node whose whole path follows greedy decoding
+        best_depth = 0
+        for i in range(1, N):
+            path = node_context([], tokens, parents, i)
+            if path == greedy[:len(path)]:
+                best_depth = max(best_depth, len(path))
+        assert n == best_depth
+        last = int(out["last_node"][0])
+        assert len(node_context([], tokens, parents, last)) == n
+
+
+def test_chain_tree_equals_linear_greedy_verify():
+    rng = np.random.default_rng(12)
+    B, K, V = 6, 7, 20
+    target = rng.normal(0, 2, (B, K + 1, V))
+    am = target.argmax(axis=2)
+    drafts = np.where(rng.random((B, K)) < 0.7, am[:, :K], rng.integers(0, V, (B, K))).astype(np.int32)
+    lin = orc.verify(target, None, drafts, 1.0, 0)
+    tokens = np.concatenate([np.zeros((B, 1), np.int32), drafts], axis=1)
+    parents = np.broadcast_to(np.arange(-1, K, dtype=np.int32), (B, K + 1))
+    tree = orc.verify_tree(target, tokens, parents)
+    assert (tree["n_accepted"] == lin["n_accepted"]).all()
+    assert (tree["tokens"] == lin["tokens"]).all()
+    assert (tree["last_node"] == lin["n_accepted"]).all()
+
+
+def test_tree_ties_take_the_lowest_node_and_invalid_trees_are_flagged():
+    V = 5
+    target = np.zeros((1, 5, V))
+    target[0, :, 2] = 1.0  # argmax 2 everywhere
+    # nodes 1 and 2 both hold the argmax under the root; node 3 under 2, node 4 under 1
+    tokens = np.array([[0, 2, 2, 2, 2]], np.int32)
+    out = orc.verify_tree(target, tokens, [[-1, 0, 0, 2, 1]])
+    assert out["n_accepted"][0] == 2 and out["last_node"][0] == 3  # nodes 3 and 4 equally deep: lower wins
+    out = orc.verify_tree(target, tokens, [[-1, 0, 0, 1, 2]])
+    assert out["n_accepted"][0] == 2 and out["last_node"][0] == 3
+    bad = orc.verify_tree(target, tokens, [[-1, 0, 3, 1, 2]])  # parent not earlier
+    assert bad["n_accepted"][0] == -1 and (bad["tokens"][0] == -1).all()
+    # an out-of-range token on an untested node (its parent was rejected) is ignored
+    ok = orc.verify_tree(target, np.array([[0, 1, 2, 9, 2]], np.int32), [[-1, 0, 0, 1, 2]])
+    assert ok["n_accepted"][0] == 2 and ok["last_node"][0] == 4
+    bad_tok = orc.verify_tree(target, np.array([[0, 1, 2, 2, 9]], np.int32), [[-1, 0, 0, 1, 2]])
+    assert bad_tok["n_accepted"][0] == -1
