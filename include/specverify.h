@@ -89,7 +89,9 @@ typedef enum {
                                       sample, or sample mode without draft logits  */
     SV_FLAG_TIMEOUT = 32u,         /* a bounded wait inside the kernel gave up; the
                                       sequence is reported invalid                 */
-    SV_FLAG_BAD_LENGTH = 64u       /* a per-sequence draft length outside [0, K]   */
+    SV_FLAG_BAD_LENGTH = 64u,      /* a per-sequence draft length outside [0, K]   */
+    SV_FLAG_BAD_TREE = 128u        /* a tree node whose parent is not an earlier
+                                      node                                         */
 } sv_device_flag;
 
 /* Batched verify over logits already in device memory.
@@ -186,6 +188,32 @@ sv_status spec_verify_lmhead(const void* hidden, const void* W,
                              sv_mode mode, uint64_t seed, void* workspace,
                              size_t workspace_bytes, int32_t* out_tokens,
                              int32_t* out_n_accepted, sv_stream_t stream);
+
+/* Greedy tree verification ("Inference-4", section "Medusa": the candidate
+ * continuations of a drafter form a tree, all of them are verified in one
+ * forward pass, and the longest accepted path is kept). Node 0 of each
+ * sequence's tree is its root (the last committed token); node i > 0 carries
+ * a candidate token and a parent node earlier than i. A node is accepted when
+ * its parent is and its token is the argmax of its parent's target row; the
+ * kept path ends at the deepest accepted node (lowest index among equally
+ * deep ones) and is followed by the argmax of that node's row.
+ *   target_logits [B, N, V] dtype (device): row i is the target's
+ *     distribution after the prefix ending at node i.
+ *   tree_tokens [B, N] int32 (device): node tokens (node 0's is ignored).
+ *   tree_parents [B, N] int32 (device): parent of node i (node 0's ignored);
+ *     a parent outside [0, i) makes the sequence invalid (SV_FLAG_BAD_TREE).
+ *   1 <= N <= 32, V >= 2.
+ *   out_tokens [B, N] int32 (device): the path's tokens, the next token, -1.
+ *   out_n_accepted [B] int32 (device): the path length (tree nodes kept),
+ *     -1 for an invalid sequence.
+ *   out_last_node [B] int32 (device) or NULL: the kept path's last node (the
+ *     caller keeps that node's cache entries), -1 when invalid.
+ * Same stream, ownership and error conventions as spec_verify. */
+sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype,
+                           const int32_t* tree_tokens,
+                           const int32_t* tree_parents, int B, int N, int V,
+                           int32_t* out_tokens, int32_t* out_n_accepted,
+                           int32_t* out_last_node, sv_stream_t stream);
 
 /* Capacity of the library's own device scratch used by
  * spec_verify_lmhead_noalloc: 32 MiB, i.e. B*(K+1)*V*4 <= 33554432 bytes of

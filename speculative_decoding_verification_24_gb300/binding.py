@@ -27,6 +27,7 @@ SV_FLAG_DRAW_EDGE = 8
 SV_FLAG_BAD_MODE = 16
 SV_FLAG_TIMEOUT = 32
 SV_FLAG_BAD_LENGTH = 64
+SV_FLAG_BAD_TREE = 128
 SV_ARG_OVERLAP_PREVIOUS = 1
 SV_ERR_SCRATCH_LIMIT = 12
 SV_LMHEAD_SCRATCH_BYTES = 32 << 20  # include/specverify.h
@@ -88,6 +89,7 @@ SIGNATURES = [
     ("spec_verify_lmhead", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I, ctypes.c_uint64, P,
                                ctypes.c_size_t, P, P, P]),
     ("spec_lmhead_logits", I, [P, P, I, I, I, P, P]),
+    ("spec_verify_tree", I, [P, I, P, P, I, I, I, P, P, P, P]),
     ("spec_verify_lmhead_noalloc", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I,
                                        ctypes.c_uint64, P, P, P]),
     ("sv_status_string", ctypes.c_char_p, [I]),
@@ -246,6 +248,27 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     return {"tokens": out_tokens, "n_accepted": out_n_accepted, "p_target": out_p_target,
             "p_draft": out_p_draft, "residual_mass": out_residual_mass,
             "status_word": status_word}
+
+
+def spec_verify_tree(target_logits, tree_tokens, tree_parents, out_tokens=None, out_n_accepted=None,
+                     out_last_node=None, stream=None):
+    """Greedy tree verification: target_logits [B, N, V], tree_tokens and
+    tree_parents [B, N] int32 (node 0 is the root). Returns (tokens [B, N],
+    n_accepted [B], last_node [B])."""
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, N, dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_last_node is None:
+        out_last_node = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().spec_verify_tree(_ptr(target_logits), _dtype_code(target_logits), _ptr(tree_tokens),
+                                      _ptr(tree_parents), B, N, V, _ptr(out_tokens), _ptr(out_n_accepted),
+                                      _ptr(out_last_node), _stream(stream, dev))
+    _check(st, "spec_verify_tree")
+    return out_tokens, out_n_accepted, out_last_node
 
 
 def spec_lmhead_logits(hidden, W, out=None, stream=None):

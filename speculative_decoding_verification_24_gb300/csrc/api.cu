@@ -105,7 +105,7 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     if (a->cluster_size && usable != cs) return SV_ERR_CONFIG;
     cs = usable;
 
-    sv::VerifyParams p;
+    sv::VerifyParams p = {};
     p.target = a->target_logits;
     p.draft = a->draft_logits;
     p.tokens = a->draft_tokens;
@@ -181,6 +181,43 @@ extern "C" int sv_last_cuda_error(void) { return g_last_cuda_error; }
 extern "C" int sv_version(void) { return 100; }
 
 extern "C" size_t sv_verify_args_size(void) { return sizeof(sv_verify_args); }
+
+extern "C" sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype,
+                                      const int32_t* tree_tokens, const int32_t* tree_parents, int B,
+                                      int N, int V, int32_t* out_tokens, int32_t* out_n_accepted,
+                                      int32_t* out_last_node, sv_stream_t stream) {
+    if (!target_logits || !tree_tokens || !tree_parents || !out_tokens || !out_n_accepted) return SV_ERR_NULL;
+    if (B < 1 || N < 1 || N > 32 || V < 2) return SV_ERR_SHAPE;
+    if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+    if ((long long)B * 16 > 0x7FFFFFFFLL) return SV_ERR_SHAPE;
+    const size_t es = (size_t)esize_of(dtype);
+    if (!aligned(target_logits, es) || !aligned(tree_tokens, 4) || !aligned(tree_parents, 4) ||
+        !aligned(out_tokens, 4) || !aligned(out_n_accepted, 4) || (out_last_node && !aligned(out_last_node, 4)))
+        return SV_ERR_ALIGN;
+    int sms = 0;
+    sv_status st = check_device(&sms);
+    if (st != SV_OK) return st;
+    const int cs_min = sv::min_cluster_size(V, (int)es);
+    if (cs_min == 0) return SV_ERR_SHAPE;
+    const int cs = sv::usable_cluster_size((int)dtype, (int)dtype, sv::auto_cluster_size(B, V, (int)es, sms));
+    if (cs == 0) return fail_cuda(cudaGetLastError());
+    sv::VerifyParams p = {};
+    p.target = target_logits;
+    p.draft = nullptr;
+    p.tokens = tree_tokens;
+    p.B = B;
+    p.K = N - 1;
+    p.V = V;
+    p.mode = SV_GREEDY;
+    p.c = 1.0f;
+    p.out_tokens = out_tokens;
+    p.out_n_accepted = out_n_accepted;
+    p.tree_parents = tree_parents;
+    p.out_last_node = out_last_node;
+    cudaError_t e = sv::launch_verify_logits(p, (int)dtype, (int)dtype, cs, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return SV_OK;
+}
 
 static size_t lmhead_logits_bytes(long long M, long long V) {
     return (size_t)(((M * V * 4) + 255) / 256 * 256);

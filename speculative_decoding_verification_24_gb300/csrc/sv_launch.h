@@ -27,6 +27,10 @@ struct VerifyParams {
     uint32_t* status_word;     // or nullptr
     int overlap_previous;      // inputs not written by the previous work on the stream
     const int32_t* draft_lens; // [B] per-sequence draft counts (0..K) or nullptr (all K)
+    // Greedy tree verification when tree_parents != nullptr: K + 1 = N nodes,
+    // tokens [B, N] (node tokens; node 0 the root), tree_parents [B, N].
+    const int32_t* tree_parents;
+    int32_t* out_last_node;    // [B] or nullptr (tree mode)
 };
 
 // CTAs per cluster chosen from the shape when the caller asks for automatic.

@@ -632,6 +632,77 @@ struct SeqShared {
 static_assert(2 * (RING_BYTES + sizeof(SeqShared) + 1024) <= 228 * 1024,
               "shared state too large for two CTAs per SM");
 
+// Greedy tree verification ("Inference-4", section "Medusa": every candidate
+// of the tree is verified in one pass and the longest accepted path is kept).
+// Lane i holds node i (N <= 32): its token x_reg and parent; a node is
+// accepted when its parent is and its token is the argmax of its parent's
+// row. Acceptance and depth follow parent links, one level per step. The
+// kept path ends at the deepest accepted node (lowest index among equally
+// deep ones); the output is its tokens and the argmax of its own row.
+__device__ __forceinline__ void tree_decide(const VerifyParams& p, SeqShared& sh, int b, int N, int V,
+                                            int lane, int rank, bool mode_ok, int x_reg) {
+    const bool node = lane < N && N <= 32;
+    const int par = (lane > 0 && node) ? __ldg(p.tree_parents + (size_t)b * N + lane) : -1;
+    bool bad_row = false;
+    if (node) {
+        const ArgPart ap = as_arg(sh.merged[lane]);
+        bad_row = !isfinite(ap.v) || ap.i < 0 || ap.i >= V;
+    }
+    const bool bad_link = lane > 0 && node && (par < 0 || par >= lane);
+    const bool any_bad_row = __any_sync(FULL, bad_row), any_bad_link = __any_sync(FULL, bad_link);
+    const int src = (par < 0 || bad_link) ? 0 : par;
+    const int am_par = (lane > 0 && node && !bad_link) ? as_arg(sh.merged[src]).i : -1;
+    const bool match = node && (lane == 0 || x_reg == am_par);
+    bool acc = match;
+    int depth = 0;
+    for (int it = 1; it < N; ++it) {  // no path is longer than N - 1 links
+        const bool acc_par = __shfl_sync(FULL, acc, src);
+        const int d_par = __shfl_sync(FULL, depth, src);
+        if (lane > 0 && node) {
+            acc = match && acc_par;
+            depth = d_par + 1;
+        }
+    }
+    const bool acc_src = __shfl_sync(FULL, acc, src);  // every lane takes part in the shuffle
+    const bool tested = lane > 0 && node && acc_src;
+    const bool any_bad_token = __any_sync(FULL, tested && (x_reg < 0 || x_reg >= V));
+    const bool invalid = !mode_ok || any_bad_row || any_bad_link || any_bad_token;
+    int key = (acc && node) ? (depth << 6) | (63 - lane) : -1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) key = max(key, __shfl_xor_sync(FULL, key, o));
+    const int last = invalid ? -1 : 63 - (key & 63);
+    const int n = invalid ? -1 : key >> 6;
+    // last < N and n < N by construction (key comes from a node lane); the
+    // guards below keep every store inside the sequence's N outputs regardless
+    if (lane == 0) {
+        sh.sample = 0;
+        sh.valid = !invalid;
+    }
+    if (rank != 0) return;
+    int32_t* out = p.out_tokens + (size_t)b * N;
+    if (!invalid) {
+        int cur = last;
+        for (int k = min(n, N) - 1; k >= 0; --k) {  // the path, from its last node up to the root
+            const int tok = __shfl_sync(FULL, x_reg, cur & 31);
+            const int up = __shfl_sync(FULL, par, cur & 31);
+            if (lane == 0) out[k] = tok;
+            cur = up < 0 ? 0 : up;
+        }
+    }
+    if (node && (invalid || lane >= n))
+        out[lane] = (!invalid && lane == n && last >= 0 && last < N) ? as_arg(sh.merged[last]).i : -1;
+    if (lane == 0) {
+        p.out_n_accepted[b] = n;
+        if (p.out_last_node) p.out_last_node[b] = last;
+        if (p.status_word && invalid)
+            atomicOr(p.status_word, any_bad_link    ? (unsigned)SV_FLAG_BAD_TREE
+                                    : any_bad_token ? (unsigned)SV_FLAG_BAD_TOKEN
+                                                    : (unsigned)SV_FLAG_BAD_ROW);
+        if (p.status_word && sh.err) atomicOr(p.status_word, (unsigned)SV_FLAG_TIMEOUT);
+    }
+}
+
+
 // The NBUF ring stages a warp owns (w, w + NCW, ...). Chunk number `seq` of
 // this warp (counted over both passes) lives in stage seq % NBUF and is that
 // stage's (seq / NBUF)-th fill, so its mbarrier phase parity is
@@ -1021,7 +1092,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     uint32_t seq = 0;  // chunks this warp has handled, over both passes
     // Lane i of every warp holds draft token x_i (first used after the
     // warp's first chunk has arrived, so the load overlaps the copies).
-    const int x_reg = (mode_ok && lane < Kb) ? __ldg(p.tokens + (size_t)b * K + lane) : -1;
+    const int x_reg = p.tree_parents ? (lane <= K ? __ldg(p.tokens + (size_t)b * (K + 1) + lane) : -1)
+                                     : (mode_ok && lane < Kb) ? __ldg(p.tokens + (size_t)b * K + lane) : -1;
 
     // ---------------- pass 1: row partials over this CTA's slice ----------------
     // Warp 0 draws the Philox uniforms of positions 0..K while its first
@@ -1074,7 +1146,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     __syncthreads();
 
     // ---------------- decide (redundantly in every CTA) ----------------
-    if (warp == 0) {
+    if (warp == 0 && p.tree_parents) {
+        tree_decide(p, sh, b, K + 1, V, lane, rank, mode_ok, x_reg);
+    } else if (warp == 0) {
         bool bad = !mode_ok;
         if (mode_ok) {
             for (int r = lane; r < nrows; r += 32) {

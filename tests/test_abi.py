@@ -148,3 +148,16 @@ def test_lmhead_host_validation(lib, kwargs, code):
 ])
 def test_lmhead_logits_host_validation(lib, args, code):
     assert lib.spec_lmhead_logits(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(target=None), 1), (dict(tokens=None), 1), (dict(parents=None), 1), (dict(out_n=None), 1),
+    (dict(B=0), 2), (dict(N=0), 2), (dict(N=33), 2), (dict(V=1), 2), (dict(dtype=5), 3),
+    (dict(target=FAKE + 2), 9), (dict(parents=FAKE + 1), 9), (dict(last=FAKE + 2), 9),
+])
+def test_tree_host_validation(lib, args, code):
+    a = dict(target=FAKE, dtype=0, tokens=FAKE, parents=FAKE, B=2, N=8, V=100, out_t=FAKE,
+             out_n=FAKE, last=None)
+    a.update(args)
+    assert lib.spec_verify_tree(a["target"], a["dtype"], a["tokens"], a["parents"], a["B"], a["N"],
+                                a["V"], a["out_t"], a["out_n"], a["last"], None) == code
