@@ -434,6 +434,47 @@ int oracle_verify_tree(const void* target, int dtype, const int32_t* tokens,
     return 0;
 }
 
+/* Prompt lookup drafting ("Inference-4", section "Prompt lookup decoding"):
+ * the drafts are the tokens that followed the most recent earlier occurrence
+ * of the sequence's last n-gram, trying n = max_ngram first and shorter
+ * n-grams after; no drafts when none of them occurred before. For each n with
+ * n < L: the candidate windows are the n-grams starting at s = 0 .. L-1-n (they
+ * end before the last token); the most recent match has the largest s; the
+ * drafts are tokens s+n .. s+n+n_drafts-1, cut at the end of the sequence.
+ * Layout: tokens [B, L_max] with lengths [B]; out_drafts [B, n_drafts]
+ * (-1 padded), out_n_drafts [B] (-1 for a length outside [0, L_max]). */
+void oracle_prompt_lookup(const int32_t* tokens, const int32_t* lengths, int B,
+                          int L_max, int max_ngram, int n_drafts, int b_begin,
+                          int b_end, int32_t* out_drafts, int32_t* out_n_drafts) {
+    for (int b = b_begin; b < b_end; ++b) {
+        const int32_t* seq = tokens + (size_t)b * L_max;
+        int32_t* out = out_drafts + (size_t)b * n_drafts;
+        const int L = lengths[b];
+        for (int i = 0; i < n_drafts; ++i) out[i] = -1;
+        if (L < 0 || L > L_max) {
+            out_n_drafts[b] = -1;
+            continue;
+        }
+        out_n_drafts[b] = 0;
+        for (int n = max_ngram; n >= 1; --n) {
+            if (L <= n) continue;
+            int found = -1;
+            for (int st = L - 1 - n; st >= 0 && found < 0; --st) {
+                int same = 1;
+                for (int t = 0; t < n && same; ++t)
+                    if (seq[st + t] != seq[L - n + t]) same = 0;
+                if (same) found = st;
+            }
+            if (found >= 0) {
+                int c = 0;
+                for (int i = found + n; i < L && c < n_drafts; ++i) out[c++] = seq[i];
+                out_n_drafts[b] = c;
+                break;
+            }
+        }
+    }
+}
+
 /* Logits of the fused LM-head variant: logits[m, v] = sum_k hidden[m, k] *
  * W[k, v] over bf16 inputs widened exactly, accumulated in double in k order.
  * hidden [M, d] and W [d, V] are raw bf16 bits; rows [m_begin, m_end) only. */

@@ -52,6 +52,9 @@ def _bind(path: str):
     lib.oracle_verify_tree.restype = ctypes.c_int
     lib.oracle_verify_tree.argtypes = [P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, P, P, P]
+    lib.oracle_prompt_lookup.restype = None
+    lib.oracle_prompt_lookup.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, P, P]
     lib.oracle_philox4x32_10.restype = None
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox_uniforms.restype = None
@@ -183,6 +186,19 @@ def verify_tree(target, tokens, parents):
                                 _ptr(out["tokens"]), _ptr(out["n_accepted"]), _ptr(out["last_node"]))
     if rc != 0:
         raise MemoryError("oracle_verify_tree could not allocate its work buffers")
+    return out
+
+
+def prompt_lookup(tokens, lengths, max_ngram=3, n_drafts=5):
+    """Prompt lookup drafting. tokens [B, L_max] int, lengths [B] int.
+    Returns dict(drafts [B, n_drafts] (-1 padded), n_drafts [B])."""
+    lib = _load()
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, L_max = tok.shape
+    lens = np.ascontiguousarray(np.broadcast_to(np.asarray(lengths, dtype=np.int32), (B,)))
+    out = {"drafts": np.full((B, n_drafts), -1, dtype=np.int32), "n_drafts": np.full(B, -2, dtype=np.int32)}
+    lib.oracle_prompt_lookup(_ptr(tok), _ptr(lens), B, L_max, int(max_ngram), int(n_drafts), 0, B,
+                             _ptr(out["drafts"]), _ptr(out["n_drafts"]))
     return out
 
 

@@ -622,3 +622,47 @@ def test_tree_ties_take_the_lowest_node_and_invalid_trees_are_flagged():
     assert ok["n_accepted"][0] == 2 and ok["last_node"][0] == 4
     bad_tok = orc.verify_tree(target, np.array([[0, 1, 2, 2, 9]], np.int32), [[-1, 0, 0, 1, 2]])
     assert bad_tok["n_accepted"][0] == -1
+
+
+# ----------------------------------------------------------------- prompt lookup
+
+
+def test_prompt_lookup_golden_cases():
+    cases = json.load(open(os.path.join(GOLDEN, "prompt_lookup_cases.json")))["cases"]
+    for c in cases:
+        L = len(c["tokens"])
+        row = np.array([c["tokens"] + [0] * (12 - L)], np.int32)
+        out = orc.prompt_lookup(row, [L], c["max_ngram"], c["n_drafts"])
+        n = int(out["n_drafts"][0])
+        assert out["drafts"][0, :n].tolist() == c["drafts"], c["why"]
+        assert (out["drafts"][0, n:] == -1).all()
+
+
+def test_prompt_lookup_properties_by_brute_force():
+    """On random short sequences over a small alphabet: the drafts follow an
+    occurrence of the last n-gram; no later occurrence of that n-gram and no
+    occurrence of any longer one exists; with no drafts, no n-gram recurs."""
+    rng = np.random.default_rng(2)
+    for trial in range(400):
+        L = int(rng.integers(0, 30))
+        seq = rng.integers(0, 4, L).tolist()
+        m, k = int(rng.integers(1, 5)), int(rng.integers(1, 8))
+        row = np.array([seq + [9] * (32 - L)], np.int32)
+        out = orc.prompt_lookup(row, [L], m, k)
+        got = out["drafts"][0, :int(out["n_drafts"][0])].tolist()
+
+        def occurrences(n):
+            return [s for s in range(0, L - n) if seq[s:s + n] == seq[L - n:]] if 0 < n < L else []
+
+        found = [(n, occurrences(n)) for n in range(m, 0, -1) if occurrences(n)]
+        if not found:
+            assert got == []
+            continue
+        n, occ = found[0]
+        assert got == seq[occ[-1] + n: occ[-1] + n + k]
+        assert all(not occurrences(n2) for n2 in range(n + 1, m + 1))
+
+
+def test_prompt_lookup_invalid_length():
+    out = orc.prompt_lookup(np.zeros((2, 8), np.int32), [9, -1], 3, 2)
+    assert (out["n_drafts"] == -1).all() and (out["drafts"] == -1).all()
