@@ -215,6 +215,23 @@ sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype,
                            int32_t* out_tokens, int32_t* out_n_accepted,
                            int32_t* out_last_node, sv_stream_t stream);
 
+/* Prompt lookup drafting ("Inference-4", section "Prompt lookup decoding"):
+ * for each sequence, the drafts are the tokens that followed the most recent
+ * earlier occurrence of its last n-gram, trying n = max_ngram first and then
+ * shorter n-grams; no drafts when none of them occurred before.
+ *   tokens [B, L_max] int32 (device): each sequence's prompt and generated
+ *     text so far, in its first lengths[b] entries.
+ *   lengths [B] int32 (device): a length outside [0, L_max] gives -1 drafts.
+ *   1 <= max_ngram <= 16, 1 <= n_drafts <= 64.
+ *   out_drafts [B, n_drafts] int32 (device): the drafts, -1 padded.
+ *   out_n_drafts [B] int32 (device): how many drafts (0..n_drafts; fewer when
+ *     the occurrence lies near the end of the sequence).
+ * Same stream, ownership and error conventions as spec_verify. */
+sv_status spec_prompt_lookup(const int32_t* tokens, const int32_t* lengths,
+                             int B, int L_max, int max_ngram, int n_drafts,
+                             int32_t* out_drafts, int32_t* out_n_drafts,
+                             sv_stream_t stream);
+
 /* Capacity of the library's own device scratch used by
  * spec_verify_lmhead_noalloc: 32 MiB, i.e. B*(K+1)*V*4 <= 33554432 bytes of
  * fp32 target logits (V = 128256 allows B*(K+1) <= 65). */

@@ -90,6 +90,7 @@ SIGNATURES = [
                                ctypes.c_size_t, P, P, P]),
     ("spec_lmhead_logits", I, [P, P, I, I, I, P, P]),
     ("spec_verify_tree", I, [P, I, P, P, I, I, I, P, P, P, P]),
+    ("spec_prompt_lookup", I, [P, P, I, I, I, I, P, P, P]),
     ("spec_verify_lmhead_noalloc", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I,
                                        ctypes.c_uint64, P, P, P]),
     ("sv_status_string", ctypes.c_char_p, [I]),
@@ -269,6 +270,24 @@ def spec_verify_tree(target_logits, tree_tokens, tree_parents, out_tokens=None, 
                                       _ptr(out_last_node), _stream(stream, dev))
     _check(st, "spec_verify_tree")
     return out_tokens, out_n_accepted, out_last_node
+
+
+def spec_prompt_lookup(tokens, lengths, max_ngram=3, n_drafts=5, out_drafts=None, out_n_drafts=None,
+                       stream=None):
+    """Prompt lookup drafting: tokens [B, L_max] int32, lengths [B] int32
+    (device). Returns (drafts [B, n_drafts] -1 padded, n_drafts [B])."""
+    B, L_max = tokens.shape
+    dev = tokens.device
+    if out_drafts is None:
+        out_drafts = torch.empty(B, n_drafts, dtype=torch.int32, device=dev)
+    if out_n_drafts is None:
+        out_n_drafts = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().spec_prompt_lookup(_ptr(tokens), _ptr(lengths), B, L_max, int(max_ngram),
+                                        int(n_drafts), _ptr(out_drafts), _ptr(out_n_drafts),
+                                        _stream(stream, dev))
+    _check(st, "spec_prompt_lookup")
+    return out_drafts, out_n_drafts
 
 
 def spec_lmhead_logits(hidden, W, out=None, stream=None):

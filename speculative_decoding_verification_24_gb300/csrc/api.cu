@@ -219,6 +219,24 @@ extern "C" sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype,
     return SV_OK;
 }
 
+extern "C" sv_status spec_prompt_lookup(const int32_t* tokens, const int32_t* lengths, int B, int L_max,
+                                        int max_ngram, int n_drafts, int32_t* out_drafts,
+                                        int32_t* out_n_drafts, sv_stream_t stream) {
+    if (!tokens || !lengths || !out_drafts || !out_n_drafts) return SV_ERR_NULL;
+    if (B < 1 || L_max < 1 || max_ngram < 1 || max_ngram > sv::PL_MAX_NGRAM || n_drafts < 1 ||
+        n_drafts > sv::PL_MAX_DRAFTS || B > 0x7FFFFFFF / 2)
+        return SV_ERR_SHAPE;
+    if (!aligned(tokens, 4) || !aligned(lengths, 4) || !aligned(out_drafts, 4) || !aligned(out_n_drafts, 4))
+        return SV_ERR_ALIGN;
+    int sms = 0;
+    sv_status st = check_device(&sms);
+    if (st != SV_OK) return st;
+    cudaError_t e = sv::launch_prompt_lookup(tokens, lengths, B, L_max, max_ngram, n_drafts, out_drafts,
+                                             out_n_drafts, (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return SV_OK;
+}
+
 static size_t lmhead_logits_bytes(long long M, long long V) {
     return (size_t)(((M * V * 4) + 255) / 256 * 256);
 }

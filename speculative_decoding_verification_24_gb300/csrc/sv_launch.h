@@ -53,6 +53,12 @@ cudaError_t launch_verify_logits(const VerifyParams& p, int dtype_target, int dt
 // LM head: logits[M, V] (fp32) = hidden[M, d] . W[d, V] (bf16) on the tensor
 // cores; 1 <= M <= 256, d a multiple of 64, V a multiple of 8, 16-byte
 // aligned bases.
+constexpr int PL_MAX_NGRAM = 16;
+constexpr int PL_MAX_DRAFTS = 64;
+cudaError_t launch_prompt_lookup(const int32_t* tokens, const int32_t* lengths, int B, int L_max,
+                                 int max_ngram, int n_drafts, int32_t* out_drafts, int32_t* out_n,
+                                 cudaStream_t stream);
+
 cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
                                uint32_t* status, cudaStream_t stream);
 

@@ -161,3 +161,15 @@ def test_tree_host_validation(lib, args, code):
     a.update(args)
     assert lib.spec_verify_tree(a["target"], a["dtype"], a["tokens"], a["parents"], a["B"], a["N"],
                                 a["V"], a["out_t"], a["out_n"], a["last"], None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(tokens=None), 1), (dict(lengths=None), 1), (dict(out_d=None), 1), (dict(out_n=None), 1),
+    (dict(B=0), 2), (dict(L=0), 2), (dict(m=0), 2), (dict(m=17), 2), (dict(k=0), 2), (dict(k=65), 2),
+    (dict(tokens=FAKE + 2), 9), (dict(out_n=FAKE + 1), 9),
+])
+def test_prompt_lookup_host_validation(lib, args, code):
+    a = dict(tokens=FAKE, lengths=FAKE, B=2, L=64, m=3, k=5, out_d=FAKE, out_n=FAKE)
+    a.update(args)
+    assert lib.spec_prompt_lookup(a["tokens"], a["lengths"], a["B"], a["L"], a["m"], a["k"], a["out_d"],
+                                  a["out_n"], None) == code
