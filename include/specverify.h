@@ -232,6 +232,20 @@ sv_status spec_prompt_lookup(const int32_t* tokens, const int32_t* lengths,
                              int32_t* out_drafts, int32_t* out_n_drafts,
                              sv_stream_t stream);
 
+/* Commit step of a decode loop (the pages' loop keeps the accepted drafts and
+ * the token after them): sequence b appends out_tokens[b, 0..n] (n =
+ * n_accepted[b]) to its context tokens[b, lengths[b]..] and advances
+ * lengths[b], stopping at L_max. An invalid verify result (n < 0 or n > K) or
+ * a length outside [0, L_max] commits nothing (out_n_committed -1). The pages
+ * have no such helper as a separate step; it keeps a drafting + verify loop
+ * on the device (prompt lookup reads the contexts it writes).
+ *   tokens [B, L_max], lengths [B] int32 (device, updated in place);
+ *   out_tokens [B, K+1], n_accepted [B] int32 (device, a verify call's output);
+ *   0 <= K <= 31; out_n_committed [B] int32 (device) or NULL. */
+sv_status spec_commit(int32_t* tokens, int32_t* lengths, int B, int L_max,
+                      const int32_t* out_tokens, const int32_t* n_accepted, int K,
+                      int32_t* out_n_committed, sv_stream_t stream);
+
 /* Capacity of the library's own device scratch used by
  * spec_verify_lmhead_noalloc: 32 MiB, i.e. B*(K+1)*V*4 <= 33554432 bytes of
  * fp32 target logits (V = 128256 allows B*(K+1) <= 65). */

@@ -91,6 +91,7 @@ SIGNATURES = [
     ("spec_lmhead_logits", I, [P, P, I, I, I, P, P]),
     ("spec_verify_tree", I, [P, I, P, P, I, I, I, P, P, P, P]),
     ("spec_prompt_lookup", I, [P, P, I, I, I, I, P, P, P]),
+    ("spec_commit", I, [P, P, I, I, P, P, I, P, P]),
     ("spec_verify_lmhead_noalloc", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I,
                                        ctypes.c_uint64, P, P, P]),
     ("sv_status_string", ctypes.c_char_p, [I]),
@@ -288,6 +289,22 @@ def spec_prompt_lookup(tokens, lengths, max_ngram=3, n_drafts=5, out_drafts=None
                                         _stream(stream, dev))
     _check(st, "spec_prompt_lookup")
     return out_drafts, out_n_drafts
+
+
+def spec_commit(tokens, lengths, out_tokens, n_accepted, out_n_committed=None, stream=None):
+    """Append each sequence's accepted drafts and next token to its context
+    (tokens [B, L_max], lengths [B], updated in place). Returns the number of
+    tokens committed per sequence."""
+    B, L_max = tokens.shape
+    K = out_tokens.shape[1] - 1
+    dev = tokens.device
+    if out_n_committed is None:
+        out_n_committed = torch.empty(B, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = _load().spec_commit(_ptr(tokens), _ptr(lengths), B, L_max, _ptr(out_tokens), _ptr(n_accepted), K,
+                                 _ptr(out_n_committed), _stream(stream, dev))
+    _check(st, "spec_commit")
+    return out_n_committed
 
 
 def spec_lmhead_logits(hidden, W, out=None, stream=None):

@@ -237,6 +237,23 @@ extern "C" sv_status spec_prompt_lookup(const int32_t* tokens, const int32_t* le
     return SV_OK;
 }
 
+extern "C" sv_status spec_commit(int32_t* tokens, int32_t* lengths, int B, int L_max,
+                                 const int32_t* out_tokens, const int32_t* n_accepted, int K,
+                                 int32_t* out_n_committed, sv_stream_t stream) {
+    if (!tokens || !lengths || !out_tokens || !n_accepted) return SV_ERR_NULL;
+    if (B < 1 || L_max < 1 || K < 0 || K > 31) return SV_ERR_SHAPE;
+    if (!aligned(tokens, 4) || !aligned(lengths, 4) || !aligned(out_tokens, 4) || !aligned(n_accepted, 4) ||
+        (out_n_committed && !aligned(out_n_committed, 4)))
+        return SV_ERR_ALIGN;
+    int sms = 0;
+    sv_status st = check_device(&sms);
+    if (st != SV_OK) return st;
+    cudaError_t e = sv::launch_commit(tokens, lengths, B, L_max, out_tokens, n_accepted, K, out_n_committed,
+                                      (cudaStream_t)stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return SV_OK;
+}
+
 static size_t lmhead_logits_bytes(long long M, long long V) {
     return (size_t)(((M * V * 4) + 255) / 256 * 256);
 }

@@ -76,3 +76,35 @@ cudaError_t launch_prompt_lookup(const int32_t* tokens, const int32_t* lengths, 
 }
 
 }  // namespace sv
+
+namespace sv {
+
+// Commit step of a decode loop: sequence b appends its n_accepted[b] accepted
+// drafts and the token after them (out_tokens[b, 0..n]) to its context and
+// advances its length, up to L_max. One warp per sequence (K + 1 <= 32).
+__global__ void commit_kernel(int32_t* tokens, int32_t* lengths, int B, int L_max, const int32_t* out_tokens,
+                              const int32_t* n_accepted, int K, int32_t* out_n_committed) {
+    const int b = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (b >= B) return;
+    const int n = __ldg(n_accepted + b);
+    const int L = lengths[b];
+    const bool ok = n >= 0 && n <= K && L >= 0 && L <= L_max;
+    const int c = ok ? min(n + 1, L_max - L) : 0;
+    if (lane < c) tokens[(size_t)b * L_max + L + lane] = __ldg(out_tokens + (size_t)b * (K + 1) + lane);
+    __syncwarp();
+    if (lane == 0) {
+        if (ok) lengths[b] = L + c;
+        if (out_n_committed) out_n_committed[b] = ok ? c : -1;
+    }
+}
+
+cudaError_t launch_commit(int32_t* tokens, int32_t* lengths, int B, int L_max, const int32_t* out_tokens,
+                          const int32_t* n_accepted, int K, int32_t* out_n_committed, cudaStream_t stream) {
+    constexpr int WARPS = 8;
+    commit_kernel<<<(B + WARPS - 1) / WARPS, WARPS * 32, 0, stream>>>(tokens, lengths, B, L_max, out_tokens,
+                                                                     n_accepted, K, out_n_committed);
+    return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -59,6 +59,9 @@ cudaError_t launch_prompt_lookup(const int32_t* tokens, const int32_t* lengths, 
                                  int max_ngram, int n_drafts, int32_t* out_drafts, int32_t* out_n,
                                  cudaStream_t stream);
 
+cudaError_t launch_commit(int32_t* tokens, int32_t* lengths, int B, int L_max, const int32_t* out_tokens,
+                          const int32_t* n_accepted, int K, int32_t* out_n_committed, cudaStream_t stream);
+
 cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
                                uint32_t* status, cudaStream_t stream);
 

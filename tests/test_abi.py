@@ -173,3 +173,15 @@ def test_prompt_lookup_host_validation(lib, args, code):
     a.update(args)
     assert lib.spec_prompt_lookup(a["tokens"], a["lengths"], a["B"], a["L"], a["m"], a["k"], a["out_d"],
                                   a["out_n"], None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(tokens=None), 1), (dict(lengths=None), 1), (dict(out_t=None), 1), (dict(n=None), 1),
+    (dict(B=0), 2), (dict(L=0), 2), (dict(K=-1), 2), (dict(K=32), 2),
+    (dict(tokens=FAKE + 2), 9), (dict(committed=FAKE + 1), 9),
+])
+def test_commit_host_validation(lib, args, code):
+    a = dict(tokens=FAKE, lengths=FAKE, B=2, L=64, out_t=FAKE, n=FAKE, K=4, committed=None)
+    a.update(args)
+    assert lib.spec_commit(a["tokens"], a["lengths"], a["B"], a["L"], a["out_t"], a["n"], a["K"],
+                           a["committed"], None) == code
