@@ -990,8 +990,15 @@ __device__ __forceinline__ void edge_pass1(SeqShared& sh, const TT* tgt, const T
     }
 }
 
-template <typename TT, typename TD>
+// The rules a launch can meet: sample only, greedy only (also trees), or both
+// (per-sequence modes). Each set is its own instantiation, so a uniform batch
+// runs a kernel without the other rule's code (fewer instructions to fetch in
+// the phases that run once per call).
+constexpr int MS_SAMPLE = 1, MS_GREEDY = 2, MS_MIXED = 3;
+
+template <typename TT, typename TD, int MS>
 __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams p) {
+    constexpr bool CAN_SAMPLE = (MS & MS_SAMPLE) != 0, CAN_GREEDY = (MS & MS_GREEDY) != 0;
     extern __shared__ __align__(128) char ring[];
     __shared__ SeqShared sh;
     cg::cluster_group cluster = cg::this_cluster();
@@ -1047,7 +1054,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
     const bool len_ok = Kb >= 0 && Kb <= K;
     const bool mode_ok = (mode == 0 || mode == 1) && !(mode == 1 && drf == nullptr) && len_ok;
-    const bool sample = mode == 1 && mode_ok;
+    const bool sample = CAN_SAMPLE && (!CAN_GREEDY || mode == 1) && mode_ok;
+    // which partials this launch merges (a constant unless the set is mixed)
+    const bool use_soft = !CAN_GREEDY || (CAN_SAMPLE && sample);
     const int nrows = mode_ok ? (sample ? 2 * Kb + 1 : Kb + 1) : 0;
     const float c = p.c;
 
@@ -1062,7 +1071,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                                  : make_row_info<TD>(draft_row(drf, b, K, V, tid - Kb - 1), V, rank, CS);
     for (int t = tid; t < NCW * MAX_ROWS; t += NTHREADS) {
         const int w = t / MAX_ROWS, r = t % MAX_ROWS;
-        sh.warp_part[w][r] = sample ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+        sh.warp_part[w][r] = use_soft ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
     }
     __syncthreads();
     if (mode_ok && warp == 0) {
@@ -1103,11 +1112,23 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         if (warp == 0 && lane <= Kb) position_uniforms(p.seed, seqid, (uint32_t)lane, sh.u_pos[lane], sh.u2_pos[lane]);
     };
     if (mode_ok) {
-        if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
-        else stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
+        if constexpr (!CAN_GREEDY) {
+            stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
+        } else if constexpr (!CAN_SAMPLE) {
+            stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
+        } else {
+            if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
+            else stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
+        }
         if (warp == 0) {
-            if (sample) edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
-            else edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+            if constexpr (!CAN_GREEDY) {
+                edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+            } else if constexpr (!CAN_SAMPLE) {
+                edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+            } else {
+                if (sample) edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+                else edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+            }
         }
     }
     __syncthreads();
@@ -1117,8 +1138,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         const int dst = t / nrows, r = t % nrows;
         float2 acc = sh.edge_part[r];
         for (int w = 0; w < NCW; ++w) {
-            acc = sample ? pack(merge_soft(as_soft(acc), as_soft(sh.warp_part[w][r])))
-                         : pack(merge_arg(as_arg(acc), as_arg(sh.warp_part[w][r])));
+            acc = use_soft ? pack(merge_soft(as_soft(acc), as_soft(sh.warp_part[w][r])))
+                           : pack(merge_arg(as_arg(acc), as_arg(sh.warp_part[w][r])));
         }
         if (sh.err) acc = make_float2(__int_as_float(0x7fc00000), 0.0f);  // poison: invalid
         cluster.map_shared_rank(&sh.gathered[0][0], dst)[rank * MAX_ROWS + r] = acc;
@@ -1131,14 +1152,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     if (mode_ok) {
         const int rows_per_pass = 32 / CS;
         const int r_in = lane / CS, cr = lane % CS;
-        const float2 empty = sample ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+        const float2 empty = use_soft ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
         for (int r0 = warp * rows_per_pass; r0 < nrows; r0 += NCW * rows_per_pass) {
             const int r = r0 + r_in;
             float2 acc = r < nrows ? sh.gathered[cr][r] : empty;
             for (int o = CS >> 1; o > 0; o >>= 1) {
                 const float2 other = make_float2(__shfl_xor_sync(FULL, acc.x, o), __shfl_xor_sync(FULL, acc.y, o));
-                acc = sample ? pack(merge_soft(as_soft(acc), as_soft(other)))
-                             : pack(merge_arg(as_arg(acc), as_arg(other)));
+                acc = use_soft ? pack(merge_soft(as_soft(acc), as_soft(other)))
+                               : pack(merge_arg(as_arg(acc), as_arg(other)));
             }
             if (cr == 0 && r < nrows) sh.merged[r] = acc;
         }
@@ -1146,14 +1167,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     __syncthreads();
 
     // ---------------- decide (redundantly in every CTA) ----------------
-    if (warp == 0 && p.tree_parents) {
+    if (MS == MS_GREEDY && warp == 0 && p.tree_parents) {
         tree_decide(p, sh, b, K + 1, V, lane, rank, mode_ok, x_reg);
     } else if (warp == 0) {
         bool bad = !mode_ok;
         if (mode_ok) {
             for (int r = lane; r < nrows; r += 32) {
                 const float2 acc = sh.merged[r];
-                if (sample) {
+                if (use_soft) {
                     const SoftPart sp = as_soft(acc);
                     bad |= !(isfinite(sp.R) && isfinite(sp.s) && sp.s > 0.0f);
                 } else {
@@ -1174,7 +1195,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             x = x_reg;
             bad_token = x < 0 || x >= V;
             if (!bad_token && mode_ok) {
-                if (!sample) {
+                if (!use_soft) {
                     rej = x != as_arg(sh.merged[lane]).i;
                 } else {
                     const SoftPart st = as_soft(sh.merged[lane]);
@@ -1232,7 +1253,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     }
     __syncthreads();
 
-    if (!(sh.sample && sh.valid)) {
+    if (!CAN_SAMPLE || !(sh.sample && sh.valid)) {
         wr.drain(sh);
         return;  // every remote access of this CTA's shared memory happened before the barrier
     }
@@ -1532,28 +1553,28 @@ constexpr int N_COMBOS = 3;
 // the SM, so a small batch spreads over twice as many SMs.
 constexpr int SPREAD_SMEM = 128 * 1024;
 
-// Function attributes are per device; set them once per device and pair.
-static std::atomic<int> g_attr_done[64][N_COMBOS];
+// Function attributes are per device; set them once per device, pair and
+// mode set (index MS - 1).
+static std::atomic<int> g_attr_done[64][N_COMBOS][3];
 
 template <typename TT, typename TD>
 static constexpr int combo_of() {
     return std::is_same<TT, TD>::value ? (sizeof(TT) == 4 ? 0 : 1) : 2;
 }
 
-template <typename TT, typename TD>
+template <typename TT, typename TD, int MS>
 static cudaError_t prepare_kernel() {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     constexpr int ci = combo_of<TT, TD>();
-    if (dev >= 0 && dev < 64 && g_attr_done[dev][ci].load(std::memory_order_acquire)) return cudaSuccess;
-    e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (dev >= 0 && dev < 64 && g_attr_done[dev][ci][MS - 1].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD, MS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SPREAD_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(verify_logits_kernel<TT, TD, MS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) g_attr_done[dev][ci].store(1, std::memory_order_release);
+    if (dev >= 0 && dev < 64) g_attr_done[dev][ci][MS - 1].store(1, std::memory_order_release);
     return cudaSuccess;
 }
 
@@ -1572,9 +1593,9 @@ static void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, unsi
     cfg.numAttrs = 1;
 }
 
-template <typename TT, typename TD>
+template <typename TT, typename TD, int MS>
 static int max_active_clusters(int cs, int smem = RING_BYTES) {
-    if (prepare_kernel<TT, TD>() != cudaSuccess) {
+    if (prepare_kernel<TT, TD, MS>() != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -1582,22 +1603,22 @@ static int max_active_clusters(int cs, int smem = RING_BYTES) {
     cudaLaunchAttribute attr[1];
     fill_config(cfg, attr, (unsigned)cs, cs, 0, smem);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, verify_logits_kernel<TT, TD>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, verify_logits_kernel<TT, TD, MS>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
-// Per device, pair and log2(cluster size): how many clusters are co-resident
-// at one CTA per SM, plus one (0 = not yet known); and the SM count.
-static std::atomic<int> g_spread_clusters[64][N_COMBOS][5];
+// Per device, pair, mode set and log2(cluster size): how many clusters are
+// co-resident at one CTA per SM, plus one (0 = not yet known); the SM count.
+static std::atomic<int> g_spread_clusters[64][N_COMBOS][3][5];
 static std::atomic<int> g_num_sms[64];
 
 static int log2_cs(int cs) { return cs >= 16 ? 4 : cs >= 8 ? 3 : cs >= 4 ? 2 : cs >= 2 ? 1 : 0; }
 
 // One CTA per SM when every cluster of the launch is co-resident that way.
-template <typename TT, typename TD>
+template <typename TT, typename TD, int MS>
 static int launch_smem(int B, int cs) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RING_BYTES;
@@ -1610,28 +1631,37 @@ static int launch_smem(int B, int cs) {
         g_num_sms[dev].store(sms, std::memory_order_release);
     }
     if ((long long)B * cs > sms) return RING_BYTES;
-    std::atomic<int>& slot = g_spread_clusters[dev][combo_of<TT, TD>()][log2_cs(cs)];
+    std::atomic<int>& slot = g_spread_clusters[dev][combo_of<TT, TD>()][MS - 1][log2_cs(cs)];
     int n = slot.load(std::memory_order_acquire);
     if (n == 0) {
-        n = max_active_clusters<TT, TD>(cs, SPREAD_SMEM) + 1;
+        n = max_active_clusters<TT, TD, MS>(cs, SPREAD_SMEM) + 1;
         slot.store(n, std::memory_order_release);
     }
     return n - 1 >= B ? SPREAD_SMEM : RING_BYTES;
 }
 
-template <typename TT, typename TD>
-static cudaError_t launch_typed(const VerifyParams& p, int cs, cudaStream_t stream) {
-    cudaError_t e = prepare_kernel<TT, TD>();
+template <typename TT, typename TD, int MS>
+static cudaError_t launch_ms(const VerifyParams& p, int cs, cudaStream_t stream) {
+    cudaError_t e = prepare_kernel<TT, TD, MS>();
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream, launch_smem<TT, TD>(p.B, cs));
+    fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream, launch_smem<TT, TD, MS>(p.B, cs));
     if (p.overlap_previous) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, verify_logits_kernel<TT, TD>, p);
+    return cudaLaunchKernelEx(&cfg, verify_logits_kernel<TT, TD, MS>, p);
+}
+
+// The mode set a launch needs: trees and all-greedy batches run the greedy
+// kernel, all-sample batches the sample kernel, per-sequence modes both.
+template <typename TT, typename TD>
+static cudaError_t launch_typed(const VerifyParams& p, int cs, cudaStream_t stream) {
+    if (p.tree_parents || (!p.modes && p.mode == SV_GREEDY)) return launch_ms<TT, TD, MS_GREEDY>(p, cs, stream);
+    if (!p.modes && p.mode == SV_SAMPLE) return launch_ms<TT, TD, MS_SAMPLE>(p, cs, stream);
+    return launch_ms<TT, TD, MS_MIXED>(p, cs, stream);
 }
 
 static int combo_index(int dtype_target, int dtype_draft) {
@@ -1657,9 +1687,9 @@ int usable_cluster_size(int dtype_target, int dtype_draft, int cs) {
         const int lg = log2_cs(cs);
         int state = g_cluster_ok[dev][ci][lg].load(std::memory_order_acquire);
         if (state == 0) {
-            const int n = ci == 0   ? max_active_clusters<float, float>(cs)
-                          : ci == 1 ? max_active_clusters<__nv_bfloat16, __nv_bfloat16>(cs)
-                                    : max_active_clusters<float, __nv_bfloat16>(cs);
+            const int n = ci == 0   ? max_active_clusters<float, float, MS_MIXED>(cs)
+                          : ci == 1 ? max_active_clusters<__nv_bfloat16, __nv_bfloat16, MS_MIXED>(cs)
+                                    : max_active_clusters<float, __nv_bfloat16, MS_MIXED>(cs);
             state = n > 0 ? 1 : 2;
             g_cluster_ok[dev][ci][lg].store(state, std::memory_order_release);
         }
