@@ -160,6 +160,12 @@ typedef struct {
  * flag a call starts after everything before it on the stream. */
 #define SV_ARG_OVERLAP_PREVIOUS 1u
 
+/* sv_verify_args.flags, for tests of the failure path only: every CTA also
+ * waits, with a short bound, on a barrier that nothing completes. The wait
+ * gives up as a real stalled copy would, and the call reports
+ * SV_FLAG_TIMEOUT and marks every sequence invalid, without faulting. */
+#define SV_ARG_TEST_WAIT_TIMEOUT 0x80000000u
+
 /* spec_verify with per-sequence modes, explicit sequence ids and optional
  * probability outputs. Same conventions and errors as spec_verify. */
 sv_status spec_verify_ex(const sv_verify_args* args);

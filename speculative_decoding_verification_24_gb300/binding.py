@@ -29,6 +29,7 @@ SV_FLAG_TIMEOUT = 32
 SV_FLAG_BAD_LENGTH = 64
 SV_FLAG_BAD_TREE = 128
 SV_ARG_OVERLAP_PREVIOUS = 1
+SV_ARG_TEST_WAIT_TIMEOUT = 0x80000000
 SV_ERR_SCRATCH_LIMIT = 12
 SV_LMHEAD_SCRATCH_BYTES = 32 << 20  # include/specverify.h
 
@@ -195,7 +196,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=1.0, mode
 def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, modes="sample",
                    seed=0, seq_ids=None, out_tokens=None, out_n_accepted=None, out_p_target=None,
                    out_p_draft=None, out_residual_mass=None, status_word=None, cluster_size=0,
-                   stream=None, debug=False, overlap_previous=False, draft_lens=None):
+                   stream=None, debug=False, overlap_previous=False, draft_lens=None, flags=0):
     """Verify with per-sequence modes ([B] int32 tensor, or 'greedy'/'sample'
     for all), explicit Philox sequence ids and optional debug outputs.
     debug=True allocates out_p_target, out_p_draft, out_residual_mass and
@@ -241,7 +242,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     a.out_residual_mass = _ptr(out_residual_mass)
     a.status_word = _ptr(status_word)
     a.cluster_size = int(cluster_size)
-    a.flags = SV_ARG_OVERLAP_PREVIOUS if overlap_previous else 0
+    a.flags = (SV_ARG_OVERLAP_PREVIOUS if overlap_previous else 0) | int(flags)
     a.draft_lens = _ptr(draft_lens)
     with torch.cuda.device(dev):
         a.stream = _stream(stream, dev)

@@ -124,6 +124,7 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     p.out_residual_mass = a->out_residual_mass;
     p.status_word = a->status_word;
     p.overlap_previous = (a->flags & SV_ARG_OVERLAP_PREVIOUS) != 0;
+    p.test_wait_timeout = (a->flags & SV_ARG_TEST_WAIT_TIMEOUT) != 0;
     p.draft_lens = a->draft_lens;
     cudaError_t e = sv::launch_verify_logits(p, (int)dtype_t, (int)dtype_d, cs, (cudaStream_t)a->stream);
     if (e != cudaSuccess) return fail_cuda(e);

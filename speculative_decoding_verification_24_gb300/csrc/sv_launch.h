@@ -31,6 +31,7 @@ struct VerifyParams {
     // tokens [B, N] (node tokens; node 0 the root), tree_parents [B, N].
     const int32_t* tree_parents;
     int32_t* out_last_node;    // [B] or nullptr (tree mode)
+    int test_wait_timeout;     // tests of the failure path: a bounded wait that gives up
 };
 
 // CTAs per cluster chosen from the shape when the caller asks for automatic.

@@ -622,6 +622,7 @@ struct SeqShared {
     int cstar;
     int total_chunks;
     int seq_b;                          // the sequence this cluster verifies
+    uint64_t never;                     // a barrier nothing completes (failure-path tests)
     // the final search in the CTA holding the draw
     int found, step_lp[P2_SLOTS / 32], step_hit[P2_SLOTS / 32];
     float step_tot[P2_SLOTS / 32];
@@ -1062,6 +1063,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 
     if (tid == 0) {
         for (int s = 0; s < NSTAGE; ++s) mbar_init(&sh.full[s], 1);
+        mbar_init(&sh.never, 1);
         sh.err = 0;
         sh.total_chunks = 0;
         fence_barrier_init();
@@ -1131,6 +1133,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             }
         }
     }
+    // Failure-path tests: a bounded wait on a barrier that nothing completes
+    // gives up exactly as a stalled copy's wait would.
+    if (p.test_wait_timeout && tid == 0 && !mbar_wait(&sh.never, 0, 1u << 12)) atomicExch(&sh.err, 1);
     __syncthreads();
     if (p.overlap_previous) grid_dependency_wait();
     // This CTA's partial of every row, pushed into every CTA of the cluster.
