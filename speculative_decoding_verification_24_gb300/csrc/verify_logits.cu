@@ -680,6 +680,7 @@ __device__ __forceinline__ void tree_decide(const VerifyParams& p, SeqShared& sh
         sh.valid = !invalid;
     }
     if (rank != 0) return;
+    if (p.overlap_previous) grid_dependency_wait();  // the stores below follow the previous call's
     int32_t* out = p.out_tokens + (size_t)b * N;
     if (!invalid) {
         int cur = last;
@@ -1047,8 +1048,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const TD* drf = static_cast<const TD*>(p.draft);
 
     // Programmatic dependent launch: without overlap, nothing is read before
-    // the work ahead on the stream has completed; with it, only inputs are
-    // read until then (outputs are written after the wait below pass 1).
+    // the work ahead on the stream has completed; with it, the whole call may
+    // run alongside that work, and each thread that stores to global memory
+    // first waits for it to complete, just before its stores.
     if (!p.overlap_previous) grid_dependency_wait();
     const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
     // Kb: the drafts this sequence verifies (continuous batching), 0..K
@@ -1137,7 +1139,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // gives up exactly as a stalled copy's wait would.
     if (p.test_wait_timeout && tid == 0 && !mbar_wait(&sh.never, 0, 1u << 12)) atomicExch(&sh.err, 1);
     __syncthreads();
-    if (p.overlap_previous) grid_dependency_wait();
     // This CTA's partial of every row, pushed into every CTA of the cluster.
     for (int t = tid; mode_ok && t < CS * nrows; t += NTHREADS) {
         const int dst = t / nrows, r = t % nrows;
@@ -1231,6 +1232,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             }
         }
         if (rank == 0) {
+            if (p.overlap_previous) grid_dependency_wait();  // the stores below follow the previous call's
             const int greedy_tok = (!sample && !invalid) ? as_arg(sh.merged[j]).i : -1;
             if (lane <= K) {
                 int tok = -1;
@@ -1423,11 +1425,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         __syncthreads();
         if (sh.total.hi > 0.0f || !w.use_d) break;
         // The residual summed to zero in float: fall back to P_t of row j.
-        if (rank == 0 && tid == 0 && p.status_word)
+        if (rank == 0 && tid == 0 && p.status_word) {
+            if (p.overlap_previous) grid_dependency_wait();
             atomicOr(p.status_word, (unsigned)SV_FLAG_RESIDUAL_FALLBACK);
+        }
     }
 
     if (tid == 0) {
+        if (p.overlap_previous && (rank == 0 || sh.cstar < 0)) grid_dependency_wait();
         if (sh.cstar >= 0 && isinf(sh.tc.hi) && rank == 0 && p.status_word)
             atomicOr(p.status_word, (unsigned)SV_FLAG_DRAW_EDGE);
         if (sh.cstar < 0 && rank == 0) {
@@ -1536,10 +1541,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             if (kstar >= 0 && warp == kstar) {
                 const int l = sh.step_hit[kstar];
                 const int token = st.walk(run, tw, l);
-                if (lane == l) p.out_tokens[(size_t)b * (K + 1) + j] = token;
+                if (lane == l) {
+                    if (p.overlap_previous) grid_dependency_wait();
+                    p.out_tokens[(size_t)b * (K + 1) + j] = token;
+                }
             } else if (kstar < 0 && tid == 0) {
                 int lp = -1;  // tw past the part's mass: its last positive element
                 for (int k = 0; k < STEPS; ++k) lp = max(lp, sh.step_lp[k]);
+                if (p.overlap_previous) grid_dependency_wait();
                 p.out_tokens[(size_t)b * (K + 1) + j] = lp;
             }
         }
