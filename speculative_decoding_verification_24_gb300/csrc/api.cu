@@ -98,8 +98,17 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     const int cs_min = sv::min_cluster_size(a->V, (int)es_t);
     if (cs_min == 0) return SV_ERR_SHAPE;
     if (a->cluster_size && a->cluster_size < cs_min) return SV_ERR_CONFIG;
-    int cs = a->cluster_size ? a->cluster_size
-                             : sv::auto_cluster_size(a->B, a->V, (int)es_t, sms);
+    int cs = a->cluster_size;
+    if (!cs) {
+        if (a->flags & SV_ARG_OVERLAP_PREVIOUS) {
+            // bytes of logits one sequence reads (draft rows when any may sample)
+            const long long rows_t = (long long)a->K + 1, rows_d = may_sample ? a->K : 0;
+            cs = sv::overlap_cluster_size(a->B, (rows_t * (long long)es_t + rows_d * (long long)es_d) * a->V, sms);
+        } else {
+            cs = sv::auto_cluster_size(a->B, a->V, (int)es_t, sms);
+        }
+        if (cs < cs_min) cs = cs_min;
+    }
     const int usable = sv::usable_cluster_size((int)dtype_t, (int)dtype_d, cs);
     if (usable == 0) return fail_cuda(cudaGetLastError());
     if (a->cluster_size && usable != cs) return SV_ERR_CONFIG;

@@ -1731,6 +1731,17 @@ int auto_cluster_size(int B, int V, int esize, int num_sms) {
     return cs < lo ? lo : cs;
 }
 
+// For calls that overlap the previous one: the largest power of two that
+// still gives every CTA at least 256 KB of the call's logits and keeps the
+// call within one wave of resident CTAs (two per SM), so that consecutive
+// calls can share the GPU (measured best on GB300 for the workloads).
+int overlap_cluster_size(int B, long long bytes_per_seq, int num_sms) {
+    int cs = 1;
+    while (cs < MAX_CS && bytes_per_seq / (2LL * cs) >= 256 * 1024 && (long long)B * cs * 2 <= 2LL * num_sms)
+        cs *= 2;
+    return cs;
+}
+
 cudaError_t launch_verify_logits(const VerifyParams& p, int dtype_target, int dtype_draft, int cs,
                                  cudaStream_t stream) {
     switch (combo_index(dtype_target, dtype_draft)) {
