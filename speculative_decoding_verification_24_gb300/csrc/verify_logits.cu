@@ -1231,7 +1231,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 sh.sd = j < Kb ? as_soft(sh.merged[Kb + 1 + j]) : SoftPart{-INFINITY, 0.0f};
             }
         }
-        if (rank == 0) {
+        // With overlap, a call that goes on to pass 2 stores this row at its
+        // very end instead (where its stores wait for the previous call), so
+        // that waiting holds up none of its own work.
+        if (rank == 0 && !(p.overlap_previous && sample && !invalid)) {
             if (p.overlap_previous) grid_dependency_wait();  // the stores below follow the previous call's
             const int greedy_tok = (!sample && !invalid) ? as_arg(sh.merged[j]).i : -1;
             if (lane <= K) {
@@ -1299,6 +1302,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const int rt_c0 = row_c0(sh.rows, j), rd_c0 = row_c0(sh.rows, rd_row);
     const bool resident_d = resident_t && draft_in_ring && rd.ia == sl.ia && rd.ib == sl.ib;
     int attempt = 0;
+    bool fell_back = false;
     for (;; ++attempt) {
         w.use_d = sh.use_d && attempt == 0;
         const bool ring_d = w.use_d && draft_in_ring;
@@ -1424,26 +1428,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         }
         __syncthreads();
         if (sh.total.hi > 0.0f || !w.use_d) break;
-        // The residual summed to zero in float: fall back to P_t of row j.
-        if (rank == 0 && tid == 0 && p.status_word) {
-            if (p.overlap_previous) grid_dependency_wait();
-            atomicOr(p.status_word, (unsigned)SV_FLAG_RESIDUAL_FALLBACK);
-        }
+        // The residual summed to zero in float: fall back to P_t of row j
+        // (reported at the end).
+        fell_back = true;
     }
 
-    if (tid == 0) {
-        if (p.overlap_previous && (rank == 0 || sh.cstar < 0)) grid_dependency_wait();
-        if (sh.cstar >= 0 && isinf(sh.tc.hi) && rank == 0 && p.status_word)
-            atomicOr(p.status_word, (unsigned)SV_FLAG_DRAW_EDGE);
-        if (sh.cstar < 0 && rank == 0) {
-            // No mass at all (cannot happen for a valid row): report the
-            // sequence as invalid rather than leave a slot unwritten.
-            p.out_tokens[(size_t)b * (K + 1) + j] = -1;
-            p.out_n_accepted[b] = -1;
-            if (p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_BAD_ROW);
-        }
-        if (rank == 0 && p.out_residual_mass) p.out_residual_mass[b] = sh.total.hi + sh.total.lo;
-    }
 
     if (rank == sh.cstar) {  // the CTA holding the draw (uniform over the CTA)
         if (warp == 0) {
@@ -1551,6 +1540,43 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 if (p.overlap_previous) grid_dependency_wait();
                 p.out_tokens[(size_t)b * (K + 1) + j] = lp;
             }
+        }
+    }
+
+    // Rank 0's row and flags, after the previous call's stores when calls overlap.
+    if (rank == 0 && warp == 0) {
+        if (p.overlap_previous) {
+            grid_dependency_wait();
+            // the decision's stores, deferred from the decide step (lanes
+            // other than j; position j is the draw's)
+            if (lane <= K && lane != j) p.out_tokens[(size_t)b * (K + 1) + lane] = lane < j ? x_reg : -1;
+            if (lane == 0) p.out_n_accepted[b] = j;
+            if (lane < K && (p.out_p_target || p.out_p_draft)) {
+                const float qnan = __int_as_float(0x7fc00000);
+                float pt = qnan, pd = qnan;
+                if (lane < Kb) {
+                    const SoftPart st = as_soft(sh.merged[lane]);
+                    const SoftPart sd = as_soft(sh.merged[Kb + 1 + lane]);
+                    pt = ex2(fmaf(sh.lt_x[lane], c, -st.R)) / st.s;
+                    pd = ex2(fmaf(sh.ld_x[lane], c, -sd.R)) / sd.s;
+                }
+                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = pt;
+                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = pd;
+            }
+            if (lane == 0 && p.status_word && sh.err) atomicOr(p.status_word, (unsigned)SV_FLAG_TIMEOUT);
+        }
+        if (lane == 0) {
+            if (p.status_word && fell_back) atomicOr(p.status_word, (unsigned)SV_FLAG_RESIDUAL_FALLBACK);
+            if (sh.cstar >= 0 && isinf(sh.tc.hi) && p.status_word)
+                atomicOr(p.status_word, (unsigned)SV_FLAG_DRAW_EDGE);
+            if (sh.cstar < 0) {
+                // No mass at all (cannot happen for a valid row): report the
+                // sequence as invalid rather than leave a slot unwritten.
+                p.out_tokens[(size_t)b * (K + 1) + j] = -1;
+                p.out_n_accepted[b] = -1;
+                if (p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_BAD_ROW);
+            }
+            if (p.out_residual_mass) p.out_residual_mass[b] = sh.total.hi + sh.total.lo;
         }
     }
     wr.drain(sh);
@@ -1731,12 +1757,19 @@ int auto_cluster_size(int B, int V, int esize, int num_sms) {
     return cs < lo ? lo : cs;
 }
 
-// For calls that overlap the previous one: the largest power of two that
-// still gives every CTA at least 256 KB of the call's logits and keeps the
-// call within one wave of resident CTAs (two per SM), so that consecutive
-// calls can share the GPU (measured best on GB300 for the workloads).
+// For calls that overlap the previous one. Consecutive overlapping calls
+// still finish one after another (each stores only once the previous call has
+// completed, a few microseconds per call), so a call whose logits HBM streams
+// in less than that runs on one CTA per sequence: it holds few SMs, and many
+// calls run at once. A larger call takes the largest power of two that still
+// gives every CTA at least 256 KB of its logits and keeps it within one wave
+// of resident CTAs (two per SM). Both measured best on GB300 for the
+// workloads (B=8 x 11 rows of 32000 fp32; B=64 x 9 rows of 128256 bf16).
+constexpr long long OVERLAP_SMALL_CALL_BYTES = 32LL << 20;
+
 int overlap_cluster_size(int B, long long bytes_per_seq, int num_sms) {
     int cs = 1;
+    if ((long long)B * bytes_per_seq < OVERLAP_SMALL_CALL_BYTES) return cs;
     while (cs < MAX_CS && bytes_per_seq / (2LL * cs) >= 256 * 1024 && (long long)B * cs * 2 <= 2LL * num_sms)
         cs *= 2;
     return cs;

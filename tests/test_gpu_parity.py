@@ -301,6 +301,38 @@ def test_overlapping_calls_match_serial_calls():
     assert torch.equal(shared_t, want[-1][0]) and torch.equal(shared_n, want[-1][1])
 
 
+def test_overlapping_calls_debug_outputs_match_serial_calls():
+    """Overlapped calls store the decision of a sequence that goes on to the
+    residual draw at their very end; every output, the debug ones included,
+    equals a plain call's with the same cluster size (which fixes the order
+    partials merge in), with mixed modes and per-sequence draft counts."""
+    dev = torch.device("cuda")
+    cases = [synth.make_workload("c2", seed=70 + i, device=dev, tau=1.0) for i in range(4)]
+    B, K1, _ = cases[0].target.shape
+    K = K1 - 1
+    modes = torch.tensor([i % 2 for i in range(B)], dtype=torch.int32, device=dev)
+    lens = torch.tensor([(3 * i) % (K + 1) for i in range(B)], dtype=torch.int32, device=dev)
+    keys = ("tokens", "n_accepted", "p_target", "p_draft", "residual_mass", "status_word")
+
+    def call(i, c, overlap):
+        return spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=modes, seed=i,
+                              draft_lens=lens, debug=True, overlap_previous=overlap, cluster_size=4)
+
+    want = []
+    for i, c in enumerate(cases):
+        want.append({k: v.clone() for k, v in call(i, c, False).items() if k in keys})
+        torch.cuda.synchronize()
+    got = []
+    for rep in range(3):
+        for i, c in enumerate(cases):
+            got.append((i, call(i, c, True)))
+    torch.cuda.synchronize()
+    for i, out in got:
+        for k in keys:
+            torch.testing.assert_close(out[k], want[i][k], rtol=0, atol=0, equal_nan=True, msg=k)
+    assert any(int(w["n_accepted"].min()) >= 0 for w in want)
+
+
 @pytest.mark.parametrize("name,dtype_case", [("c2", "f32"), ("c3", "bf16")])
 def test_ragged_draft_lengths(name, dtype_case):
     """Per-sequence draft counts in one launch (0..K, including 0 and K);
