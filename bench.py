@@ -408,60 +408,97 @@ def run_ours(args, rank, world, device):
 
 
 def run_e2e(args, sets, device, stream, world):
-    """Same metric through the public API with host buffers: every step copies
-    its inputs from pinned host memory, verifies, and reads the results back."""
+    """Same metric through the public API with host buffers. Every step copies
+    its inputs from pinned host memory into one of two device buffers (on a
+    copy stream, so that step i+1's copy overlaps step i's verify), verifies
+    them with spec_verify_ex and copies the results back to pinned host
+    memory. The K steps run from one CUDA graph, as a serving loop would
+    replay them; the plain eager loop on one stream is reported beside it."""
     from speculative_decoding_verification_24_gb300 import spec_verify_ex
-    import synth
 
     n_host = min(len(sets), 4)
     host = []
     for c in sets[:n_host]:
         host.append(tuple(t.cpu().pin_memory() for t in (c.target, c.draft, c.tokens, c.modes)))
     c0 = sets[0]
-    dev_t = torch.empty_like(c0.target)
-    dev_d = torch.empty_like(c0.draft)
-    dev_x = torch.empty_like(c0.tokens)
-    dev_m = torch.empty_like(c0.modes)
     B, K1, _ = c0.target.shape
-    out_t = torch.empty(B, K1, dtype=torch.int32, device=device)
-    out_n = torch.empty(B, dtype=torch.int32, device=device)
-    res_t = torch.empty(B, K1, dtype=torch.int32).pin_memory()
-    res_n = torch.empty(B, dtype=torch.int32).pin_memory()
+    bufs = [tuple(torch.empty_like(t) for t in (c0.target, c0.draft, c0.tokens, c0.modes))
+            for _ in range(2)]
+    outs = [(torch.empty(B, K1, dtype=torch.int32, device=device),
+             torch.empty(B, dtype=torch.int32, device=device)) for _ in range(2)]
+    res = [(torch.empty(B, K1, dtype=torch.int32).pin_memory(),
+            torch.empty(B, dtype=torch.int32).pin_memory()) for _ in range(2)]
     mode0 = uniform_mode(c0.modes)
-    if isinstance(mode0, torch.Tensor):
-        mode0 = dev_m
     h2d = sum(t.numel() * t.element_size() for t in host[0])
-    d2h = res_t.numel() * 4 + res_n.numel() * 4
+    d2h = res[0][0].numel() * 4 + res[0][1].numel() * 4
+    copy_stream = torch.cuda.Stream(device)
 
-    def step(i):
-        ht, hd, hx, hm = host[i % n_host]
-        dev_t.copy_(ht, non_blocking=True)
-        dev_d.copy_(hd, non_blocking=True)
-        dev_x.copy_(hx, non_blocking=True)
-        dev_m.copy_(hm, non_blocking=True)
-        spec_verify_ex(dev_t, dev_d, dev_x, c0.temperature, modes=mode0, seed=i,
-                       out_tokens=out_t, out_n_accepted=out_n, stream=stream)
-        res_t.copy_(out_t, non_blocking=True)
-        res_n.copy_(out_n, non_blocking=True)
+    def verify(i, k, on):
+        dt, dd, dx, dm = bufs[k]
+        spec_verify_ex(dt, dd, dx, c0.temperature, modes=dm if isinstance(mode0, torch.Tensor) else mode0,
+                       seed=i, out_tokens=outs[k][0], out_n_accepted=outs[k][1], stream=on)
+        res[k][0].copy_(outs[k][0], non_blocking=True)
+        res[k][1].copy_(outs[k][1], non_blocking=True)
+
+    def load(i, k):
+        for dst, src in zip(bufs[k], host[i % n_host]):
+            dst.copy_(src, non_blocking=True)
+
+    # eager, one stream: copy, verify, read back, step after step
+    def eager_step(i):
+        load(i, 0)
+        verify(i, 0, stream)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            eager_step(i)
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
     with torch.cuda.stream(stream):
         for i in range(args.steps):
-            step(i)
-    stop.record(stream)
+            eager_step(i)
+    e1.record(stream)
     torch.cuda.synchronize()
-    ms = start.elapsed_time(stop)
-    value = world * B * K1 * args.steps / (max_over_ranks(ms, device, world) / 1e3)
+    eager_ms = max_over_ranks(e0.elapsed_time(e1), device, world)
+
+    # pipelined graph of K steps: copies on copy_stream, verifies on stream
+    def pipelined(first, n):
+        copied = [torch.cuda.Event() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
+        copy_stream.wait_stream(stream)
+        for t in range(n):
+            i, k = first + t, t % 2
+            with torch.cuda.stream(copy_stream):
+                if t >= 2:
+                    copy_stream.wait_event(done[t - 2])  # buffer k is free again
+                load(i, k)
+                copied[t].record(copy_stream)
+            stream.wait_event(copied[t])
+            verify(i, k, stream)
+            done[t].record(stream)
+        stream.wait_stream(copy_stream)
+
+    with torch.cuda.stream(stream):
+        pipelined(0, max(2, args.warmup))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        pipelined(args.warmup, args.steps)
+    torch.cuda.synchronize()
+    ms = replay_ms(g, stream)  # the first replay loads the graph
+    ms = max_over_ranks(replay_ms(g, stream), device, world)
+    value = world * B * K1 * args.steps / (ms / 1e3)
     return {"value": value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "how": "pinned host inputs copied to the device, spec_verify_ex, results copied "
-                   "back, every step, on one stream; CUDA events around all steps"}
+            "h2d_gbs": h2d * args.steps / (ms / 1e3) / 1e9,
+            "eager_one_stream": {"value": world * B * K1 * args.steps / (eager_ms / 1e3),
+                                 "ms_per_step": eager_ms / args.steps},
+            "how": "every step: its inputs copied from pinned host memory into one of two "
+                   "device buffers on a copy stream, spec_verify_ex, its results copied back "
+                   "to pinned host memory; the K steps replayed from one CUDA graph (step "
+                   "i+1's copy overlaps step i's verify); CUDA events around the replay"}
 
 
 def cpu_baseline(sets, seconds):
