@@ -707,8 +707,9 @@ def run_reference(args):
 
 def profile_run(args, device):
     """--profile NAME: warmup + steps eager calls of one workload and no bench
-    line, for ncu (every launch of the verify kernel, or for c5 the LM-head
-    GEMM then the verify kernel, on inputs larger than L2)."""
+    line, for ncu (every launch of the verify kernel, launched as the bench
+    times it, with SV_ARG_OVERLAP_PREVIOUS and so the same cluster size; or
+    for c5 the LM-head GEMM then the verify kernel; inputs larger than L2)."""
     from speculative_decoding_verification_24_gb300 import (spec_verify_ex, spec_verify_lmhead,
                                                             spec_verify_lmhead_workspace_bytes)
     from speculative_decoding_verification_24_gb300.build import build
@@ -730,7 +731,7 @@ def profile_run(args, device):
         for i in range(n):
             c = sets[i % len(sets)]
             spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=uniform_mode(c.modes),
-                           seed=i)
+                           seed=i, overlap_previous=True)
     torch.cuda.synchronize()
     print(f"profile run: {args.profile}, {n} steps", flush=True)
 
