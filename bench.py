@@ -540,6 +540,13 @@ def other_workloads(args, device, l2, stream):
             except Exception as e:  # report, do not hide
                 out[name] = {"error": repr(e)}
             continue
+        if name in NEXT_ROW_NAMES:
+            try:
+                out[name] = next_row_workload(name, args, device, l2, stream)
+            except Exception as e:  # report, do not hide
+                out[name] = {"error": repr(e)}
+            torch.cuda.empty_cache()
+            continue
         try:
             sets, set_bytes = workload_sets(name, device, l2)
             steps = max(20, min(args.steps, 200))
@@ -574,6 +581,156 @@ def other_workloads(args, device, l2, stream):
         except Exception as e:  # report, do not hide
             out[name] = {"error": repr(e)}
     return out
+
+
+NEXT_ROW_NAMES = ("ragged", "tree", "lookup", "commit")
+
+
+def timed_graph_ms(step, args, steps, stream):
+    """Warm-up calls, then one CUDA graph of `steps` calls replayed twice; the
+    second replay's time (CUDA events on the launching stream)."""
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    torch.cuda.synchronize()
+    graph = capture(step, args.warmup, steps, stream)
+    replay_ms(graph, stream)
+    ms = replay_ms(graph, stream)
+    del graph
+    return ms
+
+
+def next_row_workload(name, args, device, l2, stream):
+    """The decode-loop pieces around the verify step, each on its own seeded
+    inputs (sizes in synth.NEXT_ROWS): ragged draft counts on c4's shapes,
+    greedy tree verification, prompt lookup and the commit step."""
+    import synth
+    from speculative_decoding_verification_24_gb300 import (spec_commit, spec_prompt_lookup,
+                                                            spec_verify_ex, spec_verify_tree)
+
+    cfg = synth.NEXT_ROWS[name]
+    steps = max(20, min(args.steps, 200))
+    peak, _ = measured_peaks()
+
+    def hbm(nbytes, ms):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"hbm_gbs": gbs, "frac_of_measured_peak": gbs / peak, "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS}
+
+    if name == "ragged":
+        sets, _ = workload_sets(cfg["base"], device, l2)
+        B, K1, V = sets[0].target.shape
+        K = K1 - 1
+        s = sets[0].target.element_size()
+        lens = [synth.make_draft_lens(B, K, seed=400 + k, device=device) for k in range(len(sets))]
+        out_t = torch.empty(args.warmup + steps, B, K1, dtype=torch.int32, device=device)
+        out_n = torch.empty(args.warmup + steps, B, dtype=torch.int32, device=device)
+
+        def step(i):
+            c = sets[i % len(sets)]
+            spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes="sample", seed=i,
+                           out_tokens=out_t[i], out_n_accepted=out_n[i], stream=stream,
+                           overlap_previous=True, draft_lens=lens[i % len(sets)])
+
+        ms = timed_graph_ms(step, args, steps, stream)
+        n_all = out_n.cpu().numpy()
+        nbytes, rows = 0, 0
+        for i in range(args.warmup, args.warmup + steps):
+            kb = lens[i % len(sets)].cpu().numpy().astype(np.int64)
+            n = n_all[i]
+            rows += int((kb + 1).sum())
+            nbytes += int(((2 * kb + 1) * V * s).sum())            # rows 0..Kb of both
+            nbytes += int(((n >= 0) & (n < kb)).sum()) * 2 * V * s  # residual row pair
+            nbytes += int((n == kb).sum()) * V * s                  # bonus row
+        del sets
+        return {"workload": "c4's shapes (B=256, K=8, V=151936 bf16, sample) with per-sequence "
+                            "draft counts uniform over 0..8", "steps": steps,
+                "rows_per_s": rows / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
+                "algorithmic_bytes_per_launch": nbytes / steps, **hbm(nbytes / steps, ms / steps),
+                "how": "overlapped calls (SV_ARG_OVERLAP_PREVIOUS) from one CUDA graph, inputs rotating over > 2 x L2"}
+
+    if name == "tree":
+        B, N, V = cfg["B"], cfg["N"], cfg["V"]
+        one = B * N * V * 2
+        n_sets = max(2, math.ceil(2 * l2 / one))
+        sets = [synth.make_tree_case(B, N, V, cfg["dtype"], cfg["sigma_t"], cfg["zipf_s"], cfg["p_follow"],
+                                     seed=600 + k, device=device) for k in range(n_sets)]
+        outs = (torch.empty(B, N, dtype=torch.int32, device=device), torch.empty(B, dtype=torch.int32, device=device),
+                torch.empty(B, dtype=torch.int32, device=device))
+
+        def step(i):
+            t, x, par = sets[i % n_sets]
+            spec_verify_tree(t, x, par, out_tokens=outs[0], out_n_accepted=outs[1], out_last_node=outs[2],
+                             stream=stream)
+
+        ms = timed_graph_ms(step, args, steps, stream)
+        mean_acc = float(outs[1].float().mean())
+        del sets
+        return {"workload": f"greedy tree verify: {B} trees of {N} nodes, V={V} bf16 rows "
+                            "(N(0,4^2)+Zipf(1.05); a node takes its parent's top token with p=0.6)",
+                "steps": steps, "rows_per_s": B * N * steps / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
+                "algorithmic_bytes_per_launch": one, **hbm(one, ms / steps),
+                "mean_accepted_depth_last_step": mean_acc,
+                "how": "plain calls from one CUDA graph (every row read once), inputs rotating over > 2 x L2"}
+
+    if name == "lookup":
+        B, L, vocab = cfg["B"], cfg["L_max"], cfg["vocab"]
+        tok0, lens0 = synth.make_contexts(B, L, vocab, seed=700, copy_prob=cfg["copy_prob"])
+        n_sets = max(2, math.ceil(2 * l2 / (B * L * 4)))
+        # further sets: the same structure with token ids shifted and rows rolled
+        sets = [(torch.from_numpy(np.roll((tok0 + 7 * k) % vocab, k, axis=0)).to(device),
+                 torch.from_numpy(np.roll(lens0, k)).to(device)) for k in range(n_sets)]
+        out_d = torch.empty(B, cfg["n_drafts"], dtype=torch.int32, device=device)
+        out_n = torch.empty(B, dtype=torch.int32, device=device)
+
+        def step(i):
+            ctx, ln = sets[i % n_sets]
+            spec_prompt_lookup(ctx, ln, cfg["max_ngram"], cfg["n_drafts"], out_drafts=out_d, out_n_drafts=out_n,
+                               stream=stream)
+
+        ms = timed_graph_ms(step, args, steps, stream)
+        nbytes = sum(int(sets[i % n_sets][1].clamp(min=0).sum()) * 4
+                     for i in range(args.warmup, args.warmup + steps)) / steps
+        found = int((out_n > 0).sum())
+        del sets
+        return {"workload": f"prompt lookup: {B} contexts of up to {L} tokens (vocab {vocab}, "
+                            f"lengths uniform), n-grams up to {cfg['max_ngram']}, {cfg['n_drafts']} drafts",
+                "steps": steps, "contexts_per_s": B * steps / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
+                "algorithmic_bytes_per_launch": nbytes, **hbm(nbytes, ms / steps),
+                "sequences_with_drafts_last_step": found,
+                "how": "plain calls from one CUDA graph; each context's tokens read once is the "
+                       "algorithmic traffic; inputs rotating over > 2 x L2"}
+
+    if name == "commit":
+        B, L, K = cfg["B"], cfg["L_max"], cfg["K"]
+        rng = np.random.default_rng(800)
+        ctx = torch.zeros(B, L, dtype=torch.int32, device=device)
+        start = torch.full((B,), L // 2, dtype=torch.int32, device=device)
+        lens = start.clone()
+        n_var = 8
+        toks = [torch.from_numpy(rng.integers(0, 32000, (B, K + 1)).astype(np.int32)).to(device) for _ in range(n_var)]
+        nacc = [torch.from_numpy(rng.integers(0, K + 1, B).astype(np.int32)).to(device) for _ in range(n_var)]
+        out_c = torch.empty(B, dtype=torch.int32, device=device)
+
+        def step(i):
+            spec_commit(ctx, lens, toks[i % n_var], nacc[i % n_var], out_n_committed=out_c, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                step(i)
+        torch.cuda.synchronize()
+        graph = capture(step, args.warmup, steps, stream)
+        lens.copy_(start)
+        replay_ms(graph, stream)
+        lens.copy_(start)
+        ms = replay_ms(graph, stream)
+        del graph
+        moved = B * (K + 1) * 4 * 2 + B * 4 * 3
+        return {"workload": f"commit: {B} contexts of {L} slots, K={K} (up to {K + 1} tokens appended "
+                            "per sequence)", "steps": steps, "us_per_step": ms * 1e3 / steps,
+                "calls_per_s": steps / (ms / 1e3), "bytes_per_launch": moved,
+                "bound": "launch latency (a few KB per call)",
+                "how": "plain calls from one CUDA graph"}
+    raise ValueError(name)
 
 
 def lmhead_workload(args, device, stream, n_sets=4):
@@ -746,7 +903,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4"])
-    ap.add_argument("--also", default="c3,c4,c5", help="other workloads reported as sub-results")
+    ap.add_argument("--also", default="c3,c4,c5,ragged,tree,lookup,commit",
+                    help="other workloads reported as sub-results")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -228,7 +228,7 @@ sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype,
  *   tokens [B, L_max] int32 (device): each sequence's prompt and generated
  *     text so far, in its first lengths[b] entries.
  *   lengths [B] int32 (device): a length outside [0, L_max] gives -1 drafts.
- *   1 <= max_ngram <= 16, 1 <= n_drafts <= 64.
+ *   1 <= B <= 2^28, 1 <= max_ngram <= 16, 1 <= n_drafts <= 64 (else SV_ERR_SHAPE).
  *   out_drafts [B, n_drafts] int32 (device): the drafts, -1 padded.
  *   out_n_drafts [B] int32 (device): how many drafts (0..n_drafts; fewer when
  *     the occurrence lies near the end of the sequence).

@@ -234,7 +234,7 @@ extern "C" sv_status spec_prompt_lookup(const int32_t* tokens, const int32_t* le
                                         int32_t* out_n_drafts, sv_stream_t stream) {
     if (!tokens || !lengths || !out_drafts || !out_n_drafts) return SV_ERR_NULL;
     if (B < 1 || L_max < 1 || max_ngram < 1 || max_ngram > sv::PL_MAX_NGRAM || n_drafts < 1 ||
-        n_drafts > sv::PL_MAX_DRAFTS || B > 0x7FFFFFFF / 2)
+        n_drafts > sv::PL_MAX_DRAFTS || B > 0x7FFFFFFF / 8)
         return SV_ERR_SHAPE;
     if (!aligned(tokens, 4) || !aligned(lengths, 4) || !aligned(out_drafts, 4) || !aligned(out_n_drafts, 4))
         return SV_ERR_ALIGN;

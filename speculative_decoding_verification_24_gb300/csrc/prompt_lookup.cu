@@ -3,46 +3,105 @@
 // the most recent earlier occurrence of the sequence's last n-gram, trying
 // n = max_ngram first; none when no n-gram of length 1..max_ngram recurs.
 //
-// One CTA per sequence. A window that ends at position e (e <= L-2, so it
-// ends before the last token) matches the last n tokens for every n up to
-// ml(e), the length of the common suffix of seq[..e] and seq[..L-1] (capped
-// at max_ngram). The n that wins is the largest ml over all e, and its most
-// recent window has the largest e among those: so one max-reduction of the
-// key (ml(e), e) over all positions gives both. The drafts are then
-// seq[e+1 .. e+n_drafts], cut at L.
+// A window that ends at position e (e <= L-2, so it ends before the last
+// token) matches the last n tokens for every n up to ml(e), the length of the
+// common suffix of seq[..e] and seq[..L-1] (capped at max_ngram). The n that
+// wins is the largest ml over all e, and its most recent window has the
+// largest e among those: so one max-reduction of the key (ml(e), e) over all
+// positions gives both. The drafts are then seq[e+1 .. e+n_drafts], cut at L.
+//
+// One cluster per sequence: CTA r of the cluster scans the r-th contiguous
+// part of the positions, the CTAs' keys meet in rank 0's shared memory, and
+// rank 0 writes the drafts.
+#include <cooperative_groups.h>
+
 #include <cstdint>
 
 #include "sv_device.cuh"
 #include "sv_launch.h"
 
+namespace cg = cooperative_groups;
+
 namespace sv {
 
 constexpr int PL_THREADS = 256;
+constexpr int PL_PER = 16;                        // tokens per thread and tile
+constexpr int PL_TILE = PL_THREADS * PL_PER;      // 4096 tokens per tile
+constexpr int PL_HALO = PL_MAX_NGRAM;             // tokens before a tile a window may reach
+constexpr int PL_MAX_CLUSTER = 8;
 
+// A CTA's part streams through shared memory a tile at a time: every thread
+// issues its PL_PER coalesced loads of the next tile (and the tile's halo of
+// PL_HALO earlier tokens) before the CTA scans the current one, so one load
+// latency covers a whole tile.
 __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t* tokens, const int32_t* lengths,
                                                                    int L_max, int max_ngram, int n_drafts,
                                                                    int32_t* out_drafts, int32_t* out_n) {
     __shared__ int32_t suffix[PL_MAX_NGRAM];
+    __shared__ int32_t tile[2][PL_HALO + PL_TILE];
     __shared__ long long warp_best[PL_THREADS / 32];
-    const int b = blockIdx.x;
+    __shared__ long long cta_best[PL_MAX_CLUSTER];  // rank 0: every CTA's key
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CS = (int)cluster.num_blocks();
+    const int rank = (int)cluster.block_rank();
+    const int b = (int)blockIdx.x / CS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t* seq = tokens + (size_t)b * L_max;
     int32_t* out = out_drafts + (size_t)b * n_drafts;
     const int L = __ldg(lengths + b);
     const bool valid = L >= 0 && L <= L_max;
     if (valid && tid < max_ngram && tid < L) suffix[tid] = __ldg(seq + (L - 1 - tid));
-    __syncthreads();
-    if (!valid) {
-        for (int i = tid; i < n_drafts; i += PL_THREADS) out[i] = -1;
-        if (tid == 0) out_n[b] = -1;
+    if (!valid) {  // the same for every CTA of the cluster: none takes part in a cluster barrier
+        if (rank == 0) {
+            for (int i = tid; i < n_drafts; i += PL_THREADS) out[i] = -1;
+            if (tid == 0) out_n[b] = -1;
+        }
         return;
     }
+    // windows end at e = 0 .. L-2; this CTA takes e in [p0, p1)
+    const int n_pos = L - 1 > 0 ? L - 1 : 0;
+    const int per = (n_pos + CS - 1) / CS;
+    const int p0 = min(n_pos, rank * per), p1 = min(n_pos, p0 + per);
+    const int n_tiles = (p1 - p0 + PL_TILE - 1) / PL_TILE;
+    int32_t r[PL_PER], h = 0;
+    auto load = [&](int t0) {
+#pragma unroll
+        for (int k = 0; k < PL_PER; ++k) {
+            const int i = t0 + k * PL_THREADS + tid;
+            r[k] = i < p1 ? __ldg(seq + i) : 0;
+        }
+        if (tid < PL_HALO) {
+            const int i = t0 - PL_HALO + tid;
+            h = i >= 0 ? __ldg(seq + i) : 0;
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int k = 0; k < PL_PER; ++k) tile[buf][PL_HALO + k * PL_THREADS + tid] = r[k];
+        if (tid < PL_HALO) tile[buf][tid] = h;
+    };
     long long best = -1;  // (ml << 32) | e, the largest over this thread's windows
-    for (int e = tid; e <= L - 2; e += PL_THREADS) {
-        int ml = 0;
-        while (ml < max_ngram && e - ml >= 0 && __ldg(seq + (e - ml)) == suffix[ml]) ++ml;
-        const long long key = ((long long)ml << 32) | (unsigned)e;
-        best = key > best ? key : best;
+    if (n_tiles > 0) {
+        load(p0);
+        store(0);
+    }
+    __syncthreads();
+    for (int ti = 0; ti < n_tiles; ++ti) {
+        const int t0 = p0 + ti * PL_TILE, buf = ti & 1;
+        if (ti + 1 < n_tiles) load(t0 + PL_TILE);  // in flight during the scan below
+        const int32_t* tl = tile[buf] + PL_HALO - t0;  // tl[i] = token i for t0 - PL_HALO <= i < t0 + PL_TILE
+#pragma unroll 4
+        for (int k = 0; k < PL_PER; ++k) {
+            const int e = t0 + k * PL_THREADS + tid;
+            if (e < p1) {
+                int ml = 0;
+                while (ml < max_ngram && e - ml >= 0 && tl[e - ml] == suffix[ml]) ++ml;
+                const long long key = ((long long)ml << 32) | (unsigned)e;
+                best = key > best ? key : best;
+            }
+        }
+        if (ti + 1 < n_tiles) store(buf ^ 1);  // nobody reads that buffer in this round
+        __syncthreads();
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -51,8 +110,19 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
     }
     if (lane == 0) warp_best[warp] = best;
     __syncthreads();
+    cluster.sync();  // every CTA of the cluster runs: rank 0's shared memory may be written
     if (warp == 0) {
         best = lane < PL_THREADS / 32 ? warp_best[lane] : -1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            best = other > best ? other : best;
+        }
+        if (lane == 0) cluster.map_shared_rank(cta_best, 0)[rank] = best;
+    }
+    cluster.sync();
+    if (rank == 0 && warp == 0) {
+        best = lane < CS ? cta_best[lane] : -1;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
@@ -67,12 +137,28 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
     }
 }
 
+// The cluster size: one CTA per tile of the longest possible context, at most
+// PL_MAX_CLUSTER.
 cudaError_t launch_prompt_lookup(const int32_t* tokens, const int32_t* lengths, int B, int L_max,
                                  int max_ngram, int n_drafts, int32_t* out_drafts, int32_t* out_n,
                                  cudaStream_t stream) {
-    prompt_lookup_kernel<<<B, PL_THREADS, 0, stream>>>(tokens, lengths, L_max, max_ngram, n_drafts,
-                                                       out_drafts, out_n);
-    return cudaGetLastError();
+    int cs = (L_max + PL_TILE - 1) / PL_TILE;
+    cs = cs < 1 ? 1 : cs > PL_MAX_CLUSTER ? PL_MAX_CLUSTER : cs;
+    while (cs & (cs - 1)) ++cs;  // a power of two (1, 2, 4, 8)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3((unsigned)(B * cs), 1, 1);
+    cfg.blockDim = dim3(PL_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prompt_lookup_kernel, tokens, lengths, L_max, max_ngram, n_drafts,
+                              out_drafts, out_n);
 }
 
 }  // namespace sv

@@ -40,6 +40,9 @@ def contexts(B, L_max, vocab, seed, copy_prob=0.3):
 @pytest.mark.parametrize("B,L_max,vocab,m,k", [
     (64, 512, 8, 3, 5), (64, 4096, 50, 4, 8), (32, 8192, 32000, 3, 10), (16, 300, 3, 16, 64),
     (8, 1, 5, 1, 1),
+    # one CTA per 4096-token tile, up to 8 per sequence (uneven parts, several
+    # tiles per CTA, windows that straddle a part or tile boundary)
+    (6, 20000, 7, 3, 8), (4, 40000, 100, 5, 16), (5, 12289, 3, 16, 64),
 ])
 def test_prompt_lookup_matches_oracle(B, L_max, vocab, m, k):
     tok, lens = contexts(B, L_max, vocab, seed=B + L_max + vocab)
