@@ -170,22 +170,36 @@ typedef struct {
  * probability outputs. Same conventions and errors as spec_verify. */
 sv_status spec_verify_ex(const sv_verify_args* args);
 
-/* Bytes of device workspace spec_verify_lmhead needs for these sizes. */
+/* Bytes of device workspace spec_verify_lmhead needs for these sizes:
+ * the fp32 logits B*(K+1)*V*4, then 8 bytes per target row and 128-column
+ * tile of V (ceil(V/128)*B*(K+1)*8), then 8 bytes per draft row and tile
+ * (ceil(V/128)*B*K*8), each part rounded up to 256 bytes. */
 size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V);
 
 /* Fused LM head + verify: the target rows are computed on the GPU as
  * logits[B*(K+1), V] = hidden[B*(K+1), d] . W[d, V] (bf16 inputs, fp32
  * accumulation on the tensor cores) and verified against the draft rows as
- * spec_verify does.
+ * spec_verify does. ("Speculative decoding", denimpatel.github.io
+ * interactive course, section "Memory-bound, not compute-bound": the K+1
+ * verification rows come from one forward pass that reads the head's
+ * weights once.) The GEMM's epilogue reduces each 128-column tile of every
+ * row to a softmax partial (sample) or its maximum and lowest index
+ * (greedy); the verify step merges those instead of re-reading the rows and
+ * reads one target row per sequence again only for the final draw. In
+ * sample mode the GEMM kernel also reduces the draft rows to per-tile
+ * partials. Two kernels on `stream`; the second may start while the first
+ * finishes.
  *   hidden [B, K+1, d] bf16 (device), W [d, V] bf16 (device, V contiguous),
  *   draft_logits [B, K, V] of draft_dtype (device; NULL in greedy mode),
  *   d a positive multiple of 64, V a positive multiple of 8, B * (K+1) <= 256;
  *   hidden and W 16-byte aligned. Greedy mode ignores draft_dtype.
  *   workspace: device buffer of at least
  *   spec_verify_lmhead_workspace_bytes(B, K, d, V) bytes, 256-byte aligned;
- *   it receives the fp32 target logits [B*(K+1), V] (every byte the call
- *   reads there it wrote first, so no initial contents are needed) and may
- *   be reused once the call's work on `stream` has completed.
+ *   it receives the fp32 target logits [B*(K+1), V], then the target rows'
+ *   per-tile partials [ceil(V/128), B*(K+1)] and (sample mode) the draft
+ *   rows' [ceil(V/128), B*K], 8 bytes each (every byte the call reads there
+ *   it wrote first, so no initial contents are needed); it may be reused
+ *   once the call's work on `stream` has completed.
  * Other arguments as in spec_verify. */
 sv_status spec_verify_lmhead(const void* hidden, const void* W,
                              const void* draft_logits,
@@ -253,8 +267,10 @@ sv_status spec_commit(int32_t* tokens, int32_t* lengths, int B, int L_max,
                       int32_t* out_n_committed, sv_stream_t stream);
 
 /* Capacity of the library's own device scratch used by
- * spec_verify_lmhead_noalloc: 32 MiB, i.e. B*(K+1)*V*4 <= 33554432 bytes of
- * fp32 target logits (V = 128256 allows B*(K+1) <= 65). */
+ * spec_verify_lmhead_noalloc: 32 MiB, i.e.
+ * spec_verify_lmhead_workspace_bytes(B, K, d, V) <= 33554432 (the fp32
+ * target logits and the per-tile partials; at V = 128256 that allows
+ * B <= 15 for K = 3, B <= 12 for K = 4, B <= 10 for K = 5). */
 #define SV_LMHEAD_SCRATCH_BYTES (32u << 20)
 
 /* spec_verify_lmhead without a workspace argument: it allocates nothing.
@@ -262,13 +278,14 @@ sv_status spec_commit(int32_t* tokens, int32_t* lengths, int B, int L_max,
  * allocate device memory when they verify (a C host runtime linked without
  * an allocator of its own, or a serving loop that must not call cudaMalloc
  * or cudaFree between steps, since either may synchronise the whole device).
- * The target logits go to one fixed scratch array that the library's device
- * image holds (SV_LMHEAD_SCRATCH_BYTES, 256-byte aligned, one copy per
- * device); its address is looked up once per device with that device current.
+ * The workspace (target logits and partials) is one fixed scratch array
+ * that the library's device image holds (SV_LMHEAD_SCRATCH_BYTES, 256-byte
+ * aligned, one copy per device); its address is looked up once per device
+ * with that device current.
  *   Arguments as in spec_verify_lmhead, minus the workspace.
  *   Nothing in the scratch needs to start at zero: the call writes every
  *   byte it reads there before reading it.
- *   Sizes whose logits exceed SV_LMHEAD_SCRATCH_BYTES return
+ *   Sizes whose workspace would exceed SV_LMHEAD_SCRATCH_BYTES return
  *   SV_ERR_SCRATCH_LIMIT before any work is enqueued.
  *   All calls on one device share the one scratch array: calls whose work
  *   may overlap (other streams, other host threads, another call before this

@@ -354,8 +354,9 @@ def spec_verify_lmhead(hidden, W, draft_logits, draft_tokens, temperature=1.0, m
 def spec_verify_lmhead_noalloc(hidden, W, draft_logits, draft_tokens, temperature=1.0,
                                mode="sample", seed=0, out_tokens=None, out_n_accepted=None,
                                stream=None):
-    """spec_verify_lmhead with the logits in the library's own static device
-    scratch (SV_LMHEAD_SCRATCH_BYTES): the C call allocates nothing. Calls
+    """spec_verify_lmhead with its workspace (logits and per-tile partials)
+    in the library's own static device scratch (SV_LMHEAD_SCRATCH_BYTES): the
+    C call allocates nothing. Calls
     that may overlap on one device race on that scratch; order them."""
     B, K1, d = hidden.shape
     K = K1 - 1

@@ -59,7 +59,10 @@ bool valid_cluster_request(int cs) { return cs == 0 || cs == 1 || cs == 2 || cs 
 // The verify step over logits in device memory; the target rows have type
 // dtype_t and the draft rows type dtype_d (equal, or fp32 target with bf16
 // draft rows for the LM-head path).
-static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype dtype_d) {
+// target_parts: the LM-head path's per-tile target-row partials (or NULL).
+static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype dtype_d,
+                             const float2* target_parts = nullptr, int part_tiles = 0,
+                             const float2* draft_parts = nullptr) {
     if (!a) return SV_ERR_NULL;
     if (!a->target_logits || !a->draft_tokens || !a->out_tokens || !a->out_n_accepted)
         return SV_ERR_NULL;
@@ -135,6 +138,10 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     p.overlap_previous = (a->flags & SV_ARG_OVERLAP_PREVIOUS) != 0;
     p.test_wait_timeout = (a->flags & SV_ARG_TEST_WAIT_TIMEOUT) != 0;
     p.draft_lens = a->draft_lens;
+    p.target_parts = target_parts;
+    p.part_tiles = part_tiles;
+    p.part_M = a->B * (a->K + 1);
+    p.draft_parts = draft_parts;
     cudaError_t e = sv::launch_verify_logits(p, (int)dtype_t, (int)dtype_d, cs, (cudaStream_t)a->stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return SV_OK;
@@ -181,7 +188,8 @@ extern "C" const char* sv_status_string(sv_status s) {
         case SV_ERR_CONFIG: return "requested launch configuration cannot be used";
         case SV_ERR_NOT_IMPLEMENTED: return "not implemented";
         case SV_ERR_SCRATCH_LIMIT:
-            return "the logits B*(K+1)*V*4 bytes exceed the static scratch (SV_LMHEAD_SCRATCH_BYTES)";
+            return "the LM-head workspace (logits and per-tile partials) exceeds the static scratch "
+                   "(SV_LMHEAD_SCRATCH_BYTES)";
     }
     return "unknown status";
 }
@@ -268,6 +276,17 @@ static size_t lmhead_logits_bytes(long long M, long long V) {
     return (size_t)(((M * V * 4) + 255) / 256 * 256);
 }
 
+// The LM-head verify's workspace: the fp32 logits [M, V], then one 8-byte
+// partial per row and 128-column tile ([tiles, M]), each part 256-aligned.
+static long long lmhead_tiles(long long V) { return (V + sv::LM_TILE_V - 1) / sv::LM_TILE_V; }
+static size_t lmhead_parts_bytes(long long M, long long V) {
+    return (size_t)((lmhead_tiles(V) * M * 8 + 255) / 256 * 256);
+}
+// Then (sample mode) the draft rows' partials [tiles, B*K].
+static size_t lmhead_workspace_bytes(long long B, long long K, long long V) {
+    return lmhead_logits_bytes(B * (K + 1), V) + lmhead_parts_bytes(B * (K + 1), V) + lmhead_parts_bytes(B * K, V);
+}
+
 static sv_status check_lmhead_shape(const void* hidden, const void* W, long long M, int d, int V) {
     if (!hidden || !W) return SV_ERR_NULL;
     if (M < 1 || M > 256 || d < 64 || d % 64 != 0 || V < 8 || V % 8 != 0) return SV_ERR_SHAPE;
@@ -283,7 +302,8 @@ extern "C" sv_status spec_lmhead_logits(const void* hidden, const void* W, int M
     if (!aligned(out, 4)) return SV_ERR_ALIGN;
     int sms = 0;
     if ((st = check_device(&sms)) != SV_OK) return st;
-    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, M, d, V, out, nullptr, (cudaStream_t)stream);
+    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, M, d, V, out, nullptr, 0.0f, 0, nullptr, nullptr,
+                                           (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return SV_OK;
 }
@@ -291,7 +311,7 @@ extern "C" sv_status spec_lmhead_logits(const void* hidden, const void* W, int M
 extern "C" size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V) {
     (void)d;
     if (B < 1 || K < 1 || V < 1) return 0;
-    return lmhead_logits_bytes((long long)B * (K + 1), V);
+    return lmhead_workspace_bytes(B, K, V);
 }
 
 extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const void* draft_logits,
@@ -306,7 +326,7 @@ extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const
     if (st != SV_OK) return st;
     if (draft_dtype != SV_F32 && draft_dtype != SV_BF16) return SV_ERR_DTYPE;
     if (!workspace) return SV_ERR_WORKSPACE;
-    if (workspace_bytes < lmhead_logits_bytes(M, V)) return SV_ERR_WORKSPACE;
+    if (workspace_bytes < lmhead_workspace_bytes(B, K, V)) return SV_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return SV_ERR_ALIGN;
     // validate the verify half before anything is launched
     sv_verify_args a = {};
@@ -331,10 +351,21 @@ extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const
     }
     int sms = 0;
     if ((st = check_device(&sms)) != SV_OK) return st;
-    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, (int)M, d, V, static_cast<float*>(workspace),
-                                           nullptr, (cudaStream_t)stream);
+    // the same scale as the verify kernel's: log2(e) / T, rounded once to float
+    const float c = mode == SV_SAMPLE ? (float)(1.4426950408889634 / (double)temperature) : 0.0f;
+    if (mode == SV_SAMPLE && !std::isfinite(c)) return SV_ERR_TEMPERATURE;
+    char* ws = static_cast<char*>(workspace);
+    float2* parts = reinterpret_cast<float2*>(ws + lmhead_logits_bytes(M, V));
+    float2* dparts = reinterpret_cast<float2*>(ws + lmhead_logits_bytes(M, V) + lmhead_parts_bytes(M, V));
+    sv::LmDraftParts dp{draft_logits, B * K, draft_dtype == SV_F32 ? 1 : 0, dparts};
+    const bool sample = mode == SV_SAMPLE;
+    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, (int)M, d, V, static_cast<float*>(workspace), parts, c,
+                                           sample ? 1 : 0, sample ? &dp : nullptr, nullptr, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
-    return verify_impl(&a, SV_F32, mode == SV_SAMPLE ? draft_dtype : SV_F32);
+    // the verify grid may start as the GEMM's CTAs finish; it waits for the
+    // GEMM before it reads the logits and the partials
+    return verify_impl(&a, SV_F32, sample ? draft_dtype : SV_F32, parts, (int)lmhead_tiles(V),
+                       sample ? dparts : nullptr);
 }
 
 // ---------------------------------------------------------------------------
@@ -378,7 +409,7 @@ extern "C" sv_status spec_verify_lmhead_noalloc(const void* hidden, const void* 
     if (B < 1 || K < 1 || K > 31 || V < 1) return SV_ERR_SHAPE;
     // B*(K+1) <= 256 is checked by the callee; bound the product here first
     if ((long long)B * (K + 1) > 256) return SV_ERR_SHAPE;
-    if (lmhead_logits_bytes((long long)B * (K + 1), V) > (size_t)SV_LMHEAD_SCRATCH_BYTES)
+    if (lmhead_workspace_bytes(B, K, V) > (size_t)SV_LMHEAD_SCRATCH_BYTES)
         return SV_ERR_SCRATCH_LIMIT;
     // every other argument is validated by spec_verify_lmhead before launching;
     // validate the cheap host-side ones first so that a bad call never loads

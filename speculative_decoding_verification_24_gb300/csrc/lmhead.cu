@@ -22,10 +22,21 @@
 //           committing each stage back to the producer and each finished tile
 //           to the epilogue; a tile's MMAs wait until the epilogue has drained
 //           the accumulator they reuse;
+//   warps 2-3  (sample mode of the verify step) the draft rows' softmax
+//           partials over the same tiles, read straight from global memory:
+//           they need nothing from the other warps, so they run ahead;
 //   warps 4-7  epilogue: tcgen05.ld of the finished accumulator (warp w reads
 //           TMEM lanes 32(w-4)...), one coalesced 128-byte store per column and
 //           warp, then the accumulator is handed back; it overlaps the next
 //           tile's loads and MMAs.
+// When the verify step follows (spec_verify_lmhead), the epilogue also
+// reduces every row of the tile to one softmax partial (R, s) in the base-2
+// domain, or to the row's (max, lowest index) in greedy mode: a warp's 32
+// columns are turned over through shared memory so that lane l holds row
+// c0 + l, each lane reduces its row over those columns, and the four warps'
+// partials merge in warp order. The verify kernel merges the tiles' partials
+// instead of streaming the target rows again; it re-reads one target row per
+// sequence only for the final draw.
 // Every mbarrier wait is bounded; a wait that gives up sets SV_FLAG_TIMEOUT,
 // the CTA stops issuing work, waits for what it issued and frees TMEM.
 #include <cuda.h>
@@ -33,6 +44,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <type_traits>
 
 #include "sv_device.cuh"
 #include "sv_launch.h"
@@ -44,11 +56,16 @@ constexpr int LM_BLOCK_K = 64;                           // d per stage (one 128
 constexpr int LM_A_BYTES = LM_BLOCK_V * LM_BLOCK_K * 2;  // 16 KB: two 64 x 64 boxes of W
 constexpr int LM_BOX_BYTES = 64 * LM_BLOCK_K * 2;        // 8 KB: one box of W
 constexpr int LM_MAX_STAGES = 8;
-constexpr int LM_SMEM_BUDGET = 220 * 1024;               // dynamic shared memory for the ring
+constexpr int LM_SMEM_BUDGET = 226 * 1024;               // dynamic shared memory (ring + epilogue)
 constexpr int LM_THREADS = 256;
 constexpr int LM_ACC_COLS = 256;                         // TMEM columns per accumulator
 constexpr int LM_TMEM_COLS = 2 * LM_ACC_COLS;
 constexpr uint32_t LM_WAIT_LIMIT = 1u << 24;
+constexpr int LM_EPI_WARPS = 4;
+constexpr int LM_TB_STRIDE = 33;                          // padded row: conflict-free both ways
+constexpr int LM_TB_BYTES = LM_EPI_WARPS * 32 * LM_TB_STRIDE * 4;   // per-warp 32 x 32 turn-over
+constexpr int LM_WP_BYTES = LM_EPI_WARPS * 256 * 8;                 // per-warp row partials
+constexpr int LM_EPI_BYTES = LM_TB_BYTES + LM_WP_BYTES;
 
 struct LmParams {
     int M, d, V, N;     // N: M rounded up to 16
@@ -56,6 +73,13 @@ struct LmParams {
     int tiles;          // ceil(V / LM_BLOCK_V)
     float* out;         // [M, V]
     uint32_t* status;   // optional
+    float2* parts;      // [tiles, M] per-tile row partials, or nullptr (logits only)
+    float c;            // log2(e) / temperature (soft partials)
+    int part_soft;      // 1: (R, s) softmax partials; 0: (max, lowest index)
+    // Sample mode: the draft rows' softmax partials per tile, by warps 2-3.
+    const void* draft;  // [Md, V] draft logits (fp32 or bf16), or nullptr
+    int Md, draft_f32;  // draft rows; element type
+    float2* dparts;     // [tiles, Md]
 };
 
 // tcgen05 shared-memory matrix descriptor: start address, leading and stride
@@ -125,6 +149,98 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ bool lm_error(const int* err) { return *(volatile const int*)err != 0; }
 
+// Named barrier 1 over the four epilogue warps (barrier 0 is __syncthreads).
+__device__ __forceinline__ void epi_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(LM_EPI_WARPS * 32) : "memory");
+}
+
+// The same barrier, returning the AND of every epilogue thread's v.
+__device__ __forceinline__ bool epi_barrier_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(LM_EPI_WARPS * 32)
+        : "memory");
+    return r != 0;
+}
+
+// Draft-row partials for every tile of this CTA, by one of two warps (w2):
+// lane l holds columns v0 + 4l .. v0 + 4l + 3 of a row (V is a multiple of
+// 8, so the four are inside the row or past its end together); a warp
+// reduction gives the tile's maximum, then R = ceil(max * c) and
+// s = sum 2^(l*c - R) exactly as the epilogue forms the target rows'
+// partials. Rows go in batches (32 bf16 or 16 fp32 rows per warp) whose
+// loads are in flight together: these loads compete with the W stream, and
+// only many of them in flight keep the two warps ahead of the GEMM.
+template <bool F32>
+__device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int lane, int my_tiles, const int* err) {
+    constexpr int RB = F32 ? 16 : 32;
+    using Raw = typename std::conditional<F32, uint4, uint2>::type;
+    constexpr int ESZ = F32 ? 4 : 2;
+    const bool vec = (reinterpret_cast<uintptr_t>(p.draft) & (uintptr_t)(4 * ESZ - 1)) == 0;
+    for (int li = 0; li < my_tiles && !lm_error(err); ++li) {
+        const int tile = (int)blockIdx.x + li * (int)gridDim.x;
+        const int e = tile * LM_BLOCK_V + 4 * lane;
+        const bool in = e < p.V;
+        for (int m0 = w2 * RB; m0 < p.Md; m0 += 2 * RB) {
+            Raw raw[RB];
+#pragma unroll
+            for (int k = 0; k < RB; ++k) {
+                const bool ok = in && m0 + k < p.Md;
+                const char* row = static_cast<const char*>(p.draft) + ((size_t)(m0 + k) * p.V + e) * ESZ;
+                if constexpr (F32) {
+                    raw[k] = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+                    if (ok) {
+                        if (vec) {
+                            raw[k] = ld_stream(reinterpret_cast<const uint4*>(row));
+                        } else {
+                            const uint32_t* r32 = reinterpret_cast<const uint32_t*>(row);
+                            raw[k] = make_uint4(__ldg(r32), __ldg(r32 + 1), __ldg(r32 + 2), __ldg(r32 + 3));
+                        }
+                    }
+                } else {
+                    raw[k] = make_uint2(0xFF80FF80u, 0xFF80FF80u);  // bf16 -inf pairs
+                    if (ok) {
+                        if (vec) {
+                            raw[k] = __ldg(reinterpret_cast<const uint2*>(row));
+                        } else {
+                            const unsigned short* r16 = reinterpret_cast<const unsigned short*>(row);
+                            raw[k] = make_uint2((uint32_t)__ldg(r16) | ((uint32_t)__ldg(r16 + 1) << 16),
+                                                (uint32_t)__ldg(r16 + 2) | ((uint32_t)__ldg(r16 + 3) << 16));
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < RB; ++k) {
+                float x[4];
+                if constexpr (F32) {
+                    x[0] = __uint_as_float(raw[k].x), x[1] = __uint_as_float(raw[k].y);
+                    x[2] = __uint_as_float(raw[k].z), x[3] = __uint_as_float(raw[k].w);
+                } else {
+                    x[0] = bf16_lo(raw[k].x), x[1] = bf16_hi(raw[k].x), x[2] = bf16_lo(raw[k].y), x[3] = bf16_hi(raw[k].y);
+                }
+                float mx = max_nan(max_nan(x[0], x[1]), max_nan(x[2], x[3]));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float R = ceilf(mx * p.c);
+                const float nR = R == -INFINITY ? 0.0f : -R;
+                float s = (ex2(fmaf(x[0], p.c, nR)) + ex2(fmaf(x[1], p.c, nR))) +
+                          (ex2(fmaf(x[2], p.c, nR)) + ex2(fmaf(x[3], p.c, nR)));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0 && m0 + k < p.Md)
+                    p.dparts[(size_t)tile * p.Md + m0 + k] =
+                        R == -INFINITY ? pack(SoftPart{-INFINITY, 0.0f}) : pack(SoftPart{R, s});
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(LM_THREADS, 1)
     lmhead_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
                        LmParams p) {
@@ -135,6 +251,8 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     const int b_bytes = p.N * LM_BLOCK_K * 2;
     char* a_ring = smem;                      // S x 16 KB
     char* b_ring = smem + S * LM_A_BYTES;     // S x b_bytes (b_bytes is a multiple of 2 KB)
+    float* epi_tb = reinterpret_cast<float*>(b_ring + S * b_bytes);      // LM_TB_BYTES
+    float2* epi_wp = reinterpret_cast<float2*>(b_ring + S * b_bytes + LM_TB_BYTES);  // LM_WP_BYTES
     __shared__ __align__(8) uint64_t full[LM_MAX_STAGES], empty[LM_MAX_STAGES];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
     __shared__ uint32_t tmem_base;
@@ -167,6 +285,10 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     __syncthreads();
     tmem_fence_after();
     const uint32_t tmem = tmem_base;
+    // A verify launch that follows may start on the SMs this grid leaves free
+    // as its CTAs finish; it reads nothing this grid writes before the grid
+    // has completed.
+    launch_dependents();
 
     if (warp == 0 && lane == 0) {
         // ---- TMA producer: one continuous ring over all of this CTA's tiles
@@ -236,18 +358,29 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
         // every MMA issued has completed before TMEM is released
         umma_commit(&mma_done);
         (void)mbar_wait(&mma_done, 0, LM_WAIT_LIMIT);
+    } else if ((warp == 2 || warp == 3) && p.dparts) {
+        // ---- draft rows: every row's partial over each of this CTA's tiles
+        if (p.draft_f32) draft_partials<true>(p, warp - 2, lane, my_tiles, &err);
+        else draft_partials<false>(p, warp - 2, lane, my_tiles, &err);
     } else if (warp >= 4) {
         // ---- epilogue: TMEM -> registers -> global (coalesced per column)
         const int q = warp - 4;
+        float* tb = epi_tb + q * 32 * LM_TB_STRIDE;
         for (int li = 0; li < my_tiles; ++li) {
             const int a = li & 1;
             bool ok = mbar_wait(&acc_full[a], (li >> 1) & 1, LM_WAIT_LIMIT);
             tmem_fence_after();
             if (!ok) atomicExch(&err, 1);
-            // tcgen05.ld is warp-collective: the whole warp reads or none of it
-            ok = __all_sync(0xffffffffu, ok && !lm_error(&err));
+            // One decision for all four warps (tcgen05.ld is warp-collective,
+            // and the warps meet at the partial merge below). This barrier
+            // also keeps a warp from writing the next tile's partials before
+            // every warp has merged this tile's.
+            ok = epi_barrier_and(ok && !lm_error(&err));
             if (!ok) break;
-            const int v = ((int)blockIdx.x + li * (int)gridDim.x) * LM_BLOCK_V + 32 * q + lane;
+            const int tile = (int)blockIdx.x + li * (int)gridDim.x;
+            const int vw = tile * LM_BLOCK_V + 32 * q;  // this warp's first column
+            const int v = vw + lane;
+            const int nv = p.V - vw;                     // valid columns of the warp (may be <= 0)
             const uint32_t acc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * LM_ACC_COLS);
             for (int c0 = 0; c0 < p.N; c0 += 32) {
                 uint32_t r[32];
@@ -257,9 +390,58 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                     const int m = c0 + c;
                     if (m < p.M && v < p.V) p.out[(size_t)m * p.V + v] = __uint_as_float(r[c]);
                 }
+                if (p.parts) {
+                    // turn the 32 x 32 block over: lane l then holds row c0 + l
+                    // at the warp's 32 columns, in column order
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) tb[c * LM_TB_STRIDE + lane] = __uint_as_float(r[c]);
+                    __syncwarp();
+                    float x[32];
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) x[k] = tb[lane * LM_TB_STRIDE + k];
+                    __syncwarp();  // the next block overwrites tb
+                    float2 part;
+                    if (p.part_soft) {
+                        float mx = -INFINITY;
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (k < nv) mx = max_nan(mx, x[k]);
+                        const float R = ceilf(mx * p.c);  // -inf, +inf and NaN pass through
+                        const float nR = R == -INFINITY ? 0.0f : -R;
+                        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+                        for (int k = 0; k < 32; k += 2) {
+                            if (k < nv) s0 += ex2(fmaf(x[k], p.c, nR));
+                            if (k + 1 < nv) s1 += ex2(fmaf(x[k + 1], p.c, nR));
+                        }
+                        part = R == -INFINITY ? pack(SoftPart{-INFINITY, 0.0f}) : pack(SoftPart{R, s0 + s1});
+                    } else {
+                        // the first maximum in column order; a NaN replaces any number
+                        ArgPart best{-INFINITY, INT_MAX};
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const bool take = k < nv && (x[k] > best.v || (is_nan(x[k]) && !is_nan(best.v)));
+                            if (take) best = ArgPart{x[k], vw + k};
+                        }
+                        part = pack(best);
+                    }
+                    epi_wp[q * 256 + c0 + lane] = part;  // c0 + lane < N <= 256
+                }
             }
             tmem_fence_before();
             mbar_arrive(&acc_empty[a]);
+            if (p.parts) {
+                // the four warps' partials of every row, merged in warp order
+                epi_barrier();
+                for (int m = (int)threadIdx.x - 128; m < p.M; m += LM_EPI_WARPS * 32) {
+                    float2 acc2 = epi_wp[m];
+#pragma unroll
+                    for (int w = 1; w < LM_EPI_WARPS; ++w)
+                        acc2 = p.part_soft ? pack(merge_soft(as_soft(acc2), as_soft(epi_wp[w * 256 + m])))
+                                           : pack(merge_arg(as_arg(acc2), as_arg(epi_wp[w * 256 + m])));
+                    p.parts[(size_t)tile * p.M + m] = acc2;
+                }
+            }
         }
     }
     __syncthreads();
@@ -304,15 +486,18 @@ static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, ui
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int lmhead_stages(int N) {
+// Ring stages that fit beside the epilogue's buffers (needed only when the
+// epilogue writes partials).
+static int lmhead_stages(int N, bool parts) {
     const int stage = LM_A_BYTES + N * LM_BLOCK_K * 2;
-    const int st = (LM_SMEM_BUDGET - 1024) / stage;
+    const int st = (LM_SMEM_BUDGET - 1024 - (parts ? LM_EPI_BYTES : 0)) / stage;
     return st < LM_MAX_STAGES ? st : LM_MAX_STAGES;
 }
 
 static std::atomic<int> g_lm_sms[64];
 
 cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
+                               float2* parts, float c, int part_soft, const LmDraftParts* dp,
                                uint32_t* status, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -335,15 +520,22 @@ cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, 
     p.d = d;
     p.V = V;
     p.N = (M + 15) / 16 * 16;
-    p.stages = lmhead_stages(p.N);
+    p.stages = lmhead_stages(p.N, parts != nullptr);
     p.tiles = (V + LM_BLOCK_V - 1) / LM_BLOCK_V;
     p.out = out;
     p.status = status;
+    p.parts = parts;
+    p.c = c;
+    p.part_soft = part_soft;
+    p.draft = dp ? dp->draft : nullptr;
+    p.Md = dp ? dp->Md : 0;
+    p.draft_f32 = dp ? dp->draft_f32 : 0;
+    p.dparts = dp ? dp->dparts : nullptr;
     CUtensorMap tm_w, tm_h;
     if (!encode_bf16_2d(&tm_w, W, (uint64_t)d, (uint64_t)V, 64) ||
         !encode_bf16_2d(&tm_h, hidden, (uint64_t)M, (uint64_t)d, (uint32_t)p.N))
         return cudaErrorInvalidValue;
-    const int smem = 1024 + p.stages * (LM_A_BYTES + p.N * LM_BLOCK_K * 2);
+    const int smem = 1024 + p.stages * (LM_A_BYTES + p.N * LM_BLOCK_K * 2) + (parts ? LM_EPI_BYTES : 0);
     const dim3 grid((unsigned)(p.tiles < sms ? p.tiles : sms));
     lmhead_gemm_kernel<<<grid, LM_THREADS, smem, stream>>>(tm_w, tm_h, p);
     return cudaGetLastError();

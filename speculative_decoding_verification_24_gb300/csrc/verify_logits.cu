@@ -924,19 +924,54 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
     }
 }
 
+// The 16-byte aligned span of a bf16 draft row that holds the elements of
+// fp32 target slots [q, q + n) (interior slots: every element lies in
+// [0, V), so the span stays inside the 16-byte blocks of the row's own
+// elements); `off` is the first element's byte offset in the span.
+struct DraftSpan {
+    const char* base;
+    uint32_t bytes, off;
+};
+template <typename TT, typename TD>
+__device__ __forceinline__ DraftSpan draft_span(const DrawSrc<TT, TD>& src, int q, int n) {
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src.drow) + 2 * (uintptr_t)(q * 4 - src.gt.head);
+    const uintptr_t a0 = s0 & ~(uintptr_t)15, a1 = (s0 + 8 * (uintptr_t)n + 15) & ~(uintptr_t)15;
+    return DraftSpan{reinterpret_cast<const char*>(a0), (uint32_t)(a1 - a0), (uint32_t)(s0 - a0)};
+}
+
+// Draft elements of target slot i of a pass-2 chunk, from its span in the
+// stage, widened exactly into an fp32 slot.
+__device__ __forceinline__ uint4 span_slot(const char* span, uint32_t off, int i) {
+    const char* p = span + off + 8 * i;
+    uint32_t w0, w1;
+    if ((off & 7u) == 0) {
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(smem_u32(p)));
+    } else {
+        unsigned short h[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h[k]) : "r"(smem_u32(p + 2 * k)));
+        w0 = (uint32_t)h[0] | ((uint32_t)h[1] << 16);
+        w1 = (uint32_t)h[2] | ((uint32_t)h[3] << 16);
+    }
+    return make_uint4(w0 << 16, w0 & 0xFFFF0000u, w1 << 16, w1 & 0xFFFF0000u);
+}
+
 // Issues pass-2 chunk ci (target slots, and the draft slots when they share
-// the target's alignment) as fill `fseq` of the warp.
+// the target's alignment, or the draft's span of them when the draft is bf16
+// under an fp32 target) as fill `fseq` of the warp.
 template <typename TT, typename TD>
 __device__ __forceinline__ void fill_pass2(SeqShared& sh, WarpRing& wr, char* ring, uint32_t fseq,
                                            const DrawSrc<TT, TD>& src, int ia, int ib, int ci, bool ring_d,
-                                           int lane) {
+                                           bool span_d, int lane) {
     const int q = ia + ci * P2_SLOTS;
     const int n = min(P2_SLOTS, ib - q);
-    wr.begin_fill(sh, fseq, (uint32_t)n * 16u * (ring_d ? 2u : 1u), lane);
+    const DraftSpan ds = span_d ? draft_span<TT, TD>(src, q, n) : DraftSpan{nullptr, 0u, 0u};
+    wr.begin_fill(sh, fseq, (uint32_t)n * 16u * (ring_d ? 2u : 1u) + ds.bytes, lane);
     if (lane == 0) {
         char* stage = wr.stage(ring, fseq);
         bulk_g2s(stage, src.gt.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
         if (ring_d) bulk_g2s(stage + P2_DRAFT_OFF, src.gd.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
+        if (span_d) bulk_g2s(stage + P2_DRAFT_OFF, ds.base, ds.bytes, wr.bar(sh, fseq));
     }
 }
 
@@ -1051,7 +1086,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // the work ahead on the stream has completed; with it, the whole call may
     // run alongside that work, and each thread that stores to global memory
     // first waits for it to complete, just before its stores.
-    if (!p.overlap_previous) grid_dependency_wait();
+    const bool fused = p.target_parts != nullptr;
+    if (!p.overlap_previous && !fused) grid_dependency_wait();
     const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
     // Kb: the drafts this sequence verifies (continuous batching), 0..K
     const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
@@ -1070,9 +1106,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         sh.total_chunks = 0;
         fence_barrier_init();
     }
+    // (LM-head path: the target rows, and the draft rows when their partials
+    // come from the GEMM too, take no pass-1 chunks and no edge slots)
+    const bool fused_d = fused && p.draft_parts != nullptr;
     if (mode_ok && tid < nrows)
-        sh.rows[tid] = tid <= Kb ? make_row_info<TT>(target_row(tgt, b, K, V, tid), V, rank, CS)
-                                 : make_row_info<TD>(draft_row(drf, b, K, V, tid - Kb - 1), V, rank, CS);
+        sh.rows[tid] = (tid <= Kb ? fused : fused_d)
+                           ? RowInfo{nullptr, 0, 0, 0, -1, -1, 0}
+                           : tid <= Kb ? make_row_info<TT>(target_row(tgt, b, K, V, tid), V, rank, CS)
+                                       : make_row_info<TD>(draft_row(drf, b, K, V, tid - Kb - 1), V, rank, CS);
     for (int t = tid; t < NCW * MAX_ROWS; t += NTHREADS) {
         const int w = t / MAX_ROWS, r = t % MAX_ROWS;
         sh.warp_part[w][r] = use_soft ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
@@ -1139,6 +1180,48 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // gives up exactly as a stalled copy's wait would.
     if (p.test_wait_timeout && tid == 0 && !mbar_wait(&sh.never, 0, 1u << 12)) atomicExch(&sh.err, 1);
     __syncthreads();
+    if (fused) grid_dependency_wait();  // the GEMM grid ahead has completed; its stores are visible
+    if (fused && mode_ok) {
+        // This CTA's share of every row computed by the GEMM is the merge of
+        // its contiguous run of the tiles' partials: lanes take every 32nd
+        // tile in order (four loads in flight), then a butterfly merges the
+        // lanes (the merges are symmetric, so every lane ends with the same
+        // bits).
+        int t0, t1;
+        split_range(p.part_tiles, rank, CS, t0, t1);
+        const float2 empty = use_soft ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+        const int n_fused = fused_d ? nrows : Kb + 1;
+        const int Md = p.B * K;
+        for (int r = warp; r < n_fused; r += NCW) {
+            const bool tr = r <= Kb;
+            const float2* col = tr ? p.target_parts + (size_t)b * (K + 1) + r
+                                   : p.draft_parts + (size_t)b * K + (r - Kb - 1);
+            const size_t stride = tr ? (size_t)p.part_M : (size_t)Md;
+            float2 acc = empty;
+            for (int t = t0 + lane; t < t1; t += 4 * 32) {
+                float2 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = t + 32 * u < t1 ? __ldcg(col + (size_t)(t + 32 * u) * stride) : empty;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    acc = use_soft ? pack(merge_soft(as_soft(acc), as_soft(v[u]))) : pack(merge_arg(as_arg(acc), as_arg(v[u])));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float2 other = make_float2(__shfl_xor_sync(FULL, acc.x, o), __shfl_xor_sync(FULL, acc.y, o));
+                acc = use_soft ? pack(merge_soft(as_soft(acc), as_soft(other))) : pack(merge_arg(as_arg(acc), as_arg(other)));
+            }
+            if (lane == 0) sh.edge_part[r] = acc;
+        }
+        // the target logits at the draft tokens, read directly (every CTA)
+        if constexpr (sizeof(TT) == 4) {
+            if (sample && warp == 0 && lane < Kb && x_reg >= 0 && x_reg < V)
+                sh.lt_x[lane] = __ldcg(target_row(tgt, b, K, V, lane) + x_reg);
+        }
+        if (fused_d && sample && warp == 1 && lane < Kb && x_reg >= 0 && x_reg < V)
+            sh.ld_x[lane] = load_logit<TD>(draft_row(drf, b, K, V, lane), x_reg);
+        __syncthreads();
+    }
     // This CTA's partial of every row, pushed into every CTA of the cluster.
     for (int t = tid; mode_ok && t < CS * nrows; t += NTHREADS) {
         const int dst = t / nrows, r = t % nrows;
@@ -1281,6 +1364,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     split_range(src.gt.nslot, rank, CS, qa, qb);
     const WarpSlots sl = warp_slots<TT>(src.gt, V, qa, qb);
     const bool draft_in_ring = src.same_slots;
+    // bf16 draft under fp32 target: the draft streams as the aligned span of
+    // each chunk's elements (8 bytes per target slot, at most 1040 of the
+    // stage's 2048-byte draft half)
+    constexpr bool SPAN_TYPES = sizeof(TT) == 4 && sizeof(TD) == 2;
+    static_assert(!SPAN_TYPES || 8 * P2_SLOTS + 16 <= STAGE_BYTES - P2_DRAFT_OFF, "draft span must fit");
+    const uint32_t span_off = SPAN_TYPES ? draft_span<TT, TD>(src, sl.ia, 0).off : 0u;
     DrawRows w;
     w.c = c;
     w.ntR = -sh.st.R;
@@ -1296,7 +1385,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // STAGE_SLOTS + q - ia): row j's slices are read back from shared memory
     // instead of HBM.
     const RowInfo rt = sh.rows[j];
-    const bool resident_t = total_chunks <= NSTAGE && rt.ia == sl.ia && rt.ib == sl.ib;
+    const bool resident_t = !fused && total_chunks <= NSTAGE && rt.ia == sl.ia && rt.ib == sl.ib;
     const int rd_row = sh.use_d ? Kb + 1 + j : j;
     const RowInfo rd = sh.rows[rd_row];
     const int rt_c0 = row_c0(sh.rows, j), rd_c0 = row_c0(sh.rows, rd_row);
@@ -1306,11 +1395,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     for (;; ++attempt) {
         w.use_d = sh.use_d && attempt == 0;
         const bool ring_d = w.use_d && draft_in_ring;
-        const bool resident = resident_t && (!ring_d || resident_d);
+        const bool span_d = SPAN_TYPES && w.use_d;
+        const bool resident = resident_t && (!ring_d || resident_d) && !span_d;
         if (!sh.err) {
             for (int jj = 0; !resident && jj < NBUF; ++jj) {
                 const int ci = warp + NCW * jj;
-                if (ci < n_chunks) fill_pass2<TT, TD>(sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, lane);
+                if (ci < n_chunks) fill_pass2<TT, TD>(sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, span_d, lane);
             }
             for (int ci = warp; ci < n_chunks; ci += NCW) {
                 const int q = sl.ia + ci * P2_SLOTS;
@@ -1339,12 +1429,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                         if (i < n) {
                             dt[kk] = lds128(stage + i * 16);
                             if (ring_d) dd[kk] = lds128(stage + P2_DRAFT_OFF + i * 16);
+                            if (span_d) dd[kk] = span_slot(stage + P2_DRAFT_OFF, span_off, i);
                         }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (ci + NBUF * NCW < n_chunks)
-                        fill_pass2<TT, TD>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, lane);
+                        fill_pass2<TT, TD>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, span_d,
+                                           lane);
                     ++seq;
                 }
                 // the chunk's draw mass: per lane over its slots, then one warp sum
@@ -1352,7 +1444,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 #pragma unroll
                 for (int kk = 0; kk < STEPS; ++kk) {
                     const int i = kk * 32 + lane;
-                    if (w.use_d && !draft_in_ring && i < n)
+                    if (w.use_d && !draft_in_ring && !span_d && i < n)
                         dd[kk] = load_elems_as<TT, TD>(src.drow, V, (q + i) * Elem<TT>::E - src.gt.head);
 #pragma unroll
                     for (int k2 = 0; k2 < Elem<TT>::E / 2; ++k2)
@@ -1687,7 +1779,7 @@ static cudaError_t launch_ms(const VerifyParams& p, int cs, cudaStream_t stream)
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream, launch_smem<TT, TD, MS>(p.B, cs));
-    if (p.overlap_previous) {
+    if (p.overlap_previous || p.target_parts) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 2;

@@ -115,9 +115,13 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 
 def test_lmhead_workspace_size(lib):
-    # fp32 logits of B * (K+1) rows, rounded up to 256 bytes
-    assert lib.spec_verify_lmhead_workspace_bytes(32, 5, 4096, 128256) == 32 * 6 * 128256 * 4
-    assert lib.spec_verify_lmhead_workspace_bytes(1, 1, 64, 8) == 256
+    # fp32 logits of B * (K+1) rows, then one 8-byte partial per target row
+    # and 128-column tile, then one per draft row and tile, each rounded up
+    # to 256 bytes
+    assert (lib.spec_verify_lmhead_workspace_bytes(32, 5, 4096, 128256)
+            == 32 * 6 * 128256 * 4 + 1002 * 192 * 8 + 1002 * 160 * 8)
+    assert lib.spec_verify_lmhead_workspace_bytes(1, 1, 64, 8) == 256 + 256 + 256
+    assert lib.spec_verify_lmhead_workspace_bytes(3, 4, 64, 1000) == 60160 + 1024 + 768
     assert lib.spec_verify_lmhead_workspace_bytes(0, 1, 64, 8) == 0
 
 

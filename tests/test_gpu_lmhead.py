@@ -106,6 +106,47 @@ def greedy_ties(ref_logits, B, K1, delta):
     return ((top2[..., 1] - top2[..., 0]) < 2 * delta + 1e-12).any(axis=1)
 
 
+def workspace_parts(ws, M, V):
+    """The per-tile row partials the fused call leaves after its fp32 logits:
+    [ceil(V/128), M, 2] float32 (sample: R, s; greedy: the maximum and, as
+    int32 bits, its index)."""
+    off = (M * V * 4 + 255) // 256 * 256
+    tiles = (V + 127) // 128
+    return ws[off:off + tiles * M * 8].view(torch.float32).reshape(tiles, M, 2).cpu().numpy()
+
+
+def expected_parts(logits, V, mode, T):
+    """Each row's partial over each 128-column tile, from its definition:
+    sample R = ceil(max(l) * c) with c = log2(e)/T (both products rounded to
+    float32, as the scale is a float32) and s = sum 2^(l*c - R) in float64;
+    greedy the largest logit and its lowest index."""
+    M = logits.shape[0]
+    tiles = (V + 127) // 128
+    pad = np.full((M, tiles * 128), -np.inf)
+    pad[:, :V] = logits
+    blk = pad.reshape(M, tiles, 128).transpose(1, 0, 2)  # [tiles, M, 128]
+    if mode == "sample":
+        c32 = np.float32(1.4426950408889634 / T)
+        mx = blk.max(axis=2).astype(np.float32)
+        R = np.ceil(mx * c32).astype(np.float64)
+        s = np.exp2(blk * np.float64(c32) - R[..., None]).sum(axis=2)
+        return R, s
+    idx = blk.argmax(axis=2)  # first occurrence
+    return blk.max(axis=2), idx + 128 * np.arange(tiles)[:, None]
+
+
+def check_parts(ws, logits, V, mode, T):
+    got = workspace_parts(ws, logits.shape[0], V)
+    if mode == "sample":
+        R, s = expected_parts(logits, V, mode, T)
+        assert np.array_equal(got[..., 0].astype(np.float64), R)
+        np.testing.assert_allclose(got[..., 1], s, rtol=1e-5)
+    else:
+        v, i = expected_parts(logits, V, mode, T)
+        assert np.array_equal(got[..., 0].astype(np.float64), v)
+        assert np.array_equal(got[..., 1].copy().view(np.int32), i)
+
+
 def run_lmhead_case(case, seed, mode):
     B, K1, d = case.hidden.shape
     K, V = K1 - 1, case.W.shape[1]
@@ -119,6 +160,8 @@ def run_lmhead_case(case, seed, mode):
     # the fused call's logits are the standalone GEMM's, bit for bit
     ws_logits = ws[:B * K1 * V * 4].view(torch.float32).reshape(B * K1, V)
     assert torch.equal(ws_logits, logits)
+    # the epilogue's per-tile partials are the reductions of those logits
+    check_parts(ws, logits.cpu().numpy().astype(np.float64), V, mode, case.temperature)
     ref_logits = orc.lmhead_logits(bits(case.hidden.reshape(B * K1, d)), bits(case.W))
     delta = float(np.abs(logits.cpu().numpy().astype(np.float64) - ref_logits).max())
     ref = orc.verify(ref_logits.reshape(B, K1, V), bits(case.draft) if mode == "sample" else None,
@@ -152,3 +195,38 @@ def test_verify_lmhead_small_ragged_vocab():
     got_t, got_n, ref, _, delta = run_lmhead_case(case, 11, "sample")
     ties = near_ties(ref, accept_rel=ACCEPT_TIE_REL + 2.2 * delta, draw_abs=DRAW_TIE_ABS + 4.4 * delta)
     check(compare(got_t, got_n, ref, ties=ties), delta)
+
+
+@pytest.mark.parametrize("mode,B,K,d,V,T", [
+    ("greedy", 8, 4, 128, 1000, 1.0), ("greedy", 32, 5, 64, 8200, 1.0), ("sample", 6, 3, 64, 1000, 4.0),
+    ("sample", 20, 7, 128, 3000, 6.0),
+])
+def test_verify_lmhead_exact_logits(mode, B, K, d, V, T):
+    # small-integer operands: the GEMM's logits are exact, so the tile
+    # partials are checked against the oracle's own logits, and greedy
+    # argmax ties (frequent with integer logits) must resolve to the lowest
+    # index exactly as the oracle's do
+    g = torch.Generator().manual_seed(B * 131 + V)
+    hidden = torch.randint(-1, 2, (B, K + 1, d), generator=g).to(torch.bfloat16)
+    W = torch.randint(-1, 2, (d, V), generator=g).to(torch.bfloat16)
+    ref_logits = orc.lmhead_logits(bits(hidden.reshape(B * (K + 1), d)), bits(W))
+    draft = (torch.from_numpy(ref_logits.reshape(B, K + 1, V)[:, :K]).float()
+             + torch.randn(B, K, V, generator=g) * 1.5).to(torch.bfloat16)
+    p = torch.softmax(draft.float() / T, dim=-1).reshape(B * K, V)
+    tokens = torch.multinomial(p, 1, generator=g).reshape(B, K).to(torch.int32)
+    if mode == "greedy":  # drafts that often match the target argmax
+        top = torch.from_numpy(ref_logits.reshape(B, K + 1, V)[:, :K].argmax(axis=2)).to(torch.int32)
+        tokens = torch.where(torch.rand(B, K, generator=g) < 0.7, top, tokens)
+    ws = torch.empty(spec_verify_lmhead_workspace_bytes(B, K, d, V), dtype=torch.uint8, device="cuda")
+    out_t, out_n = spec_verify_lmhead(hidden.cuda(), W.cuda(), draft.cuda() if mode == "sample" else None,
+                                      tokens.cuda(), T, mode=mode, seed=7, workspace=ws)
+    torch.cuda.synchronize()
+    check_parts(ws, ref_logits, V, mode, T)
+    ref = orc.verify(ref_logits.reshape(B, K + 1, V), bits(draft) if mode == "sample" else None,
+                     tokens.numpy(), T, 1 if mode == "sample" else 0, seed=7)
+    ties = near_ties(ref) if mode == "sample" else None
+    res = compare(out_t.cpu().numpy(), out_n.cpu().numpy(), ref, ties=ties)
+    if mode == "greedy":
+        assert np.array_equal(out_t.cpu().numpy(), ref["tokens"]) and np.array_equal(out_n.cpu().numpy(), ref["n_accepted"])
+    else:
+        check(res, 0.0)
