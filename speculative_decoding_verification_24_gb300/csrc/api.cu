@@ -103,7 +103,9 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     if (a->cluster_size && a->cluster_size < cs_min) return SV_ERR_CONFIG;
     int cs = a->cluster_size;
     if (!cs) {
-        if (a->flags & SV_ARG_OVERLAP_PREVIOUS) {
+        if (target_parts) {
+            cs = sv::fused_cluster_size(a->B, sms);
+        } else if (a->flags & SV_ARG_OVERLAP_PREVIOUS) {
             // bytes of logits one sequence reads (draft rows when any may sample)
             const long long rows_t = (long long)a->K + 1, rows_d = may_sample ? a->K : 0;
             cs = sv::overlap_cluster_size(a->B, (rows_t * (long long)es_t + rows_d * (long long)es_d) * a->V, sms);

@@ -110,6 +110,25 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// The same load with an L2 eviction policy (W streams through L2 once per
+// call: marked evict-first, it does not push out the logits and partials the
+// verify step reads next).
+__device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -294,6 +313,7 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
         // ---- TMA producer: one continuous ring over all of this CTA's tiles
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_h)) : "memory");
+        const uint64_t w_policy = policy_evict_first();
         int it = 0;
         for (int li = 0; li < my_tiles && !lm_error(&err); ++li) {
             const int v0 = ((int)blockIdx.x + li * (int)gridDim.x) * LM_BLOCK_V;
@@ -309,8 +329,8 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                 }
                 mbar_arrive_expect_tx(&full[s], stage_tx);
                 char* a = a_ring + s * LM_A_BYTES;
-                tma_load_2d(a, &tm_w, v0, ks * LM_BLOCK_K, &full[s]);
-                if (second_box) tma_load_2d(a + LM_BOX_BYTES, &tm_w, v0 + 64, ks * LM_BLOCK_K, &full[s]);
+                tma_load_2d_hint(a, &tm_w, v0, ks * LM_BLOCK_K, &full[s], w_policy);
+                if (second_box) tma_load_2d_hint(a + LM_BOX_BYTES, &tm_w, v0 + 64, ks * LM_BLOCK_K, &full[s], w_policy);
                 tma_load_2d(b_ring + s * b_bytes, &tm_h, ks * LM_BLOCK_K, 0, &full[s]);
             }
         }

@@ -50,6 +50,9 @@ int auto_cluster_size(int B, int V, int esize, int num_sms);
 // Cluster size for a call that overlaps the previous one on its stream.
 int overlap_cluster_size(int B, long long bytes_per_seq, int num_sms);
 
+// Cluster size for the LM-head path's verify launch.
+int fused_cluster_size(int B, int num_sms);
+
 // Smallest cluster size whose per-CTA slice of a row fits the kernel's
 // bookkeeping (0: the row is too long for any cluster size).
 int min_cluster_size(int V, int esize);

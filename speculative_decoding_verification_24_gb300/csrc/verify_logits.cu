@@ -1180,8 +1180,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // gives up exactly as a stalled copy's wait would.
     if (p.test_wait_timeout && tid == 0 && !mbar_wait(&sh.never, 0, 1u << 12)) atomicExch(&sh.err, 1);
     __syncthreads();
+    // the draft logits at the draft tokens are inputs: read before the wait
+    float ld_early = 0.0f;
+    if (fused_d && sample && warp == 1 && lane < Kb && x_reg >= 0 && x_reg < V)
+        ld_early = load_logit<TD>(draft_row(drf, b, K, V, lane), x_reg);
     if (fused) grid_dependency_wait();  // the GEMM grid ahead has completed; its stores are visible
     if (fused && mode_ok) {
+        // the target logits at the draft tokens: in flight during the merge
+        float lt_early = 0.0f;
+        if constexpr (sizeof(TT) == 4) {
+            if (sample && warp == 0 && lane < Kb && x_reg >= 0 && x_reg < V)
+                lt_early = __ldcg(target_row(tgt, b, K, V, lane) + x_reg);
+        }
         // This CTA's share of every row computed by the GEMM is the merge of
         // its contiguous run of the tiles' partials: lanes take every 32nd
         // tile in order (four loads in flight), then a butterfly merges the
@@ -1192,34 +1202,50 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         const float2 empty = use_soft ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
         const int n_fused = fused_d ? nrows : Kb + 1;
         const int Md = p.B * K;
-        for (int r = warp; r < n_fused; r += NCW) {
+        // a warp takes rows warp and warp + NCW together, so that both rows'
+        // loads are in flight at once
+        auto col_of = [&](int r, size_t& stride) -> const float2* {
             const bool tr = r <= Kb;
-            const float2* col = tr ? p.target_parts + (size_t)b * (K + 1) + r
-                                   : p.draft_parts + (size_t)b * K + (r - Kb - 1);
-            const size_t stride = tr ? (size_t)p.part_M : (size_t)Md;
-            float2 acc = empty;
+            stride = tr ? (size_t)p.part_M : (size_t)Md;
+            return tr ? p.target_parts + (size_t)b * (K + 1) + r : p.draft_parts + (size_t)b * K + (r - Kb - 1);
+        };
+        auto merge2 = [&](float2 a, float2 c) -> float2 {
+            return use_soft ? pack(merge_soft(as_soft(a), as_soft(c))) : pack(merge_arg(as_arg(a), as_arg(c)));
+        };
+        for (int r0 = warp; r0 < n_fused; r0 += 2 * NCW) {
+            const int r1 = r0 + NCW;
+            size_t s0, s1;
+            const float2* c0 = col_of(r0, s0);
+            const float2* c1 = r1 < n_fused ? col_of(r1, s1) : c0;
+            if (r1 >= n_fused) s1 = s0;
+            float2 acc0 = empty, acc1 = empty;
             for (int t = t0 + lane; t < t1; t += 4 * 32) {
-                float2 v[4];
+                float2 v0[4], v1[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = t + 32 * u < t1 ? __ldcg(col + (size_t)(t + 32 * u) * stride) : empty;
+                for (int u = 0; u < 4; ++u) {
+                    const bool in = t + 32 * u < t1;
+                    v0[u] = in ? __ldcg(c0 + (size_t)(t + 32 * u) * s0) : empty;
+                    v1[u] = in && r1 < n_fused ? __ldcg(c1 + (size_t)(t + 32 * u) * s1) : empty;
+                }
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    acc = use_soft ? pack(merge_soft(as_soft(acc), as_soft(v[u]))) : pack(merge_arg(as_arg(acc), as_arg(v[u])));
+                for (int u = 0; u < 4; ++u) {
+                    acc0 = merge2(acc0, v0[u]);
+                    acc1 = merge2(acc1, v1[u]);
+                }
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-                const float2 other = make_float2(__shfl_xor_sync(FULL, acc.x, o), __shfl_xor_sync(FULL, acc.y, o));
-                acc = use_soft ? pack(merge_soft(as_soft(acc), as_soft(other))) : pack(merge_arg(as_arg(acc), as_arg(other)));
+                acc0 = merge2(acc0, make_float2(__shfl_xor_sync(FULL, acc0.x, o), __shfl_xor_sync(FULL, acc0.y, o)));
+                acc1 = merge2(acc1, make_float2(__shfl_xor_sync(FULL, acc1.x, o), __shfl_xor_sync(FULL, acc1.y, o)));
             }
-            if (lane == 0) sh.edge_part[r] = acc;
+            if (lane == 0) {
+                sh.edge_part[r0] = acc0;
+                if (r1 < n_fused) sh.edge_part[r1] = acc1;
+            }
         }
-        // the target logits at the draft tokens, read directly (every CTA)
-        if constexpr (sizeof(TT) == 4) {
-            if (sample && warp == 0 && lane < Kb && x_reg >= 0 && x_reg < V)
-                sh.lt_x[lane] = __ldcg(target_row(tgt, b, K, V, lane) + x_reg);
-        }
-        if (fused_d && sample && warp == 1 && lane < Kb && x_reg >= 0 && x_reg < V)
-            sh.ld_x[lane] = load_logit<TD>(draft_row(drf, b, K, V, lane), x_reg);
+        // the logits at the draft tokens, for the decision (every CTA)
+        if (sizeof(TT) == 4 && sample && warp == 0 && lane < Kb && x_reg >= 0 && x_reg < V) sh.lt_x[lane] = lt_early;
+        if (fused_d && sample && warp == 1 && lane < Kb && x_reg >= 0 && x_reg < V) sh.ld_x[lane] = ld_early;
         __syncthreads();
     }
     // This CTA's partial of every row, pushed into every CTA of the cluster.
@@ -1864,6 +1890,17 @@ int overlap_cluster_size(int B, long long bytes_per_seq, int num_sms) {
     if ((long long)B * bytes_per_seq < OVERLAP_SMALL_CALL_BYTES) return cs;
     while (cs < MAX_CS && bytes_per_seq / (2LL * cs) >= 256 * 1024 && (long long)B * cs * 2 <= 2LL * num_sms)
         cs *= 2;
+    return cs;
+}
+
+// For the LM-head path, whose verify streams only the final draw's rows: the
+// largest power of two (at most 8) that keeps every CTA of the launch on its
+// own SM. Its CTAs may start while the GEMM's last CTAs run; clusters of 8
+// placed then left later clusters without room until the first ones ended
+// (measured on GB300 for B = 32), which one CTA per SM avoids.
+int fused_cluster_size(int B, int num_sms) {
+    int cs = 1;
+    while (cs < 8 && (long long)B * cs * 2 <= num_sms) cs *= 2;
     return cs;
 }
 

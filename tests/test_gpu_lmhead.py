@@ -230,3 +230,47 @@ def test_verify_lmhead_exact_logits(mode, B, K, d, V, T):
         assert np.array_equal(out_t.cpu().numpy(), ref["tokens"]) and np.array_equal(out_n.cpu().numpy(), ref["n_accepted"])
     else:
         check(res, 0.0)
+
+
+def misaligned_copy(x, elems):
+    """x on the GPU, starting `elems` elements past a 256-byte aligned base
+    (the rows keep that misalignment: V is a multiple of 8)."""
+    n = x.numel()
+    buf = torch.empty(n + 64, dtype=x.dtype, device="cuda")
+    view = buf[elems:elems + n].view(x.shape)
+    view.copy_(x.cuda())
+    assert view.data_ptr() % 16 == (elems * x.element_size()) % 16
+    return view
+
+
+@pytest.mark.parametrize("draft_dtype,offset", [
+    (torch.float32, 0),   # fp32 draft rows: 16-byte loads in the GEMM's draft warps
+    (torch.float32, 1),   # fp32 draft 4 bytes off 16: element loads; draft row with its own slot geometry
+    (torch.bfloat16, 1),  # bf16 draft 2 bytes off: element loads, and a draft span read 2 bytes in
+    (torch.bfloat16, 2),  # bf16 draft 4 bytes off
+    (torch.bfloat16, 4),  # bf16 draft 8 bytes off: 8-byte loads still aligned, span 8 bytes in
+])
+def test_verify_lmhead_draft_layouts(draft_dtype, offset):
+    case = synth.make_lmhead_case(B=5, K=4, V=3000, d=128, seed=40 + offset, w_sigma=0.1)
+    B, K1, d = case.hidden.shape
+    K, V = K1 - 1, case.W.shape[1]
+    draft = case.draft.to(draft_dtype)
+    draft_dev = misaligned_copy(draft, offset)
+    hidden, W, tokens = case.hidden.cuda(), case.W.cuda(), case.tokens.cuda()
+    ws = torch.empty(spec_verify_lmhead_workspace_bytes(B, K, d, V), dtype=torch.uint8, device="cuda")
+    out_t, out_n = spec_verify_lmhead(hidden, W, draft_dev, tokens, case.temperature, seed=9, workspace=ws)
+    logits = spec_lmhead_logits(hidden, W)
+    torch.cuda.synchronize()
+    # the draft rows' partials (after the target rows') are their reductions
+    M, Md, tiles = B * K1, B * K, (V + 127) // 128
+    off = (M * V * 4 + 255) // 256 * 256 + (tiles * M * 8 + 255) // 256 * 256
+    got = ws[off:off + tiles * Md * 8].view(torch.float32).reshape(tiles, Md, 2).cpu().numpy()
+    R, s = expected_parts(draft.float().reshape(Md, V).numpy().astype(np.float64), V, "sample", case.temperature)
+    assert np.array_equal(got[..., 0].astype(np.float64), R)
+    np.testing.assert_allclose(got[..., 1], s, rtol=1e-5)
+    ref_logits = orc.lmhead_logits(bits(case.hidden.reshape(B * K1, d)), bits(case.W))
+    delta = float(np.abs(logits.cpu().numpy().astype(np.float64) - ref_logits).max())
+    ref = orc.verify(ref_logits.reshape(B, K1, V), bits(draft), case.tokens.numpy(), case.temperature, 1,
+                     seed=9)
+    ties = near_ties(ref, accept_rel=ACCEPT_TIE_REL + 2.2 * delta, draw_abs=DRAW_TIE_ABS + 4.4 * delta)
+    check(compare(out_t.cpu().numpy(), out_n.cpu().numpy(), ref, ties=ties), delta)
