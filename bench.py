@@ -795,6 +795,13 @@ def lmhead_workload(args, device, stream, n_sets=4):
     res.update({
         "rows_per_s": M / (f_ms / 1e3), "us_per_step": f_ms * 1e3,
         "gemm_us": g_ms * 1e3, "verify_us": (f_ms - g_ms) * 1e3,
+        "verify_us_means": "the fused step minus the GEMM alone (spec_lmhead_logits): the epilogue's "
+                           "tile partials, the draft rows' partials and the verify launch after the GEMM",
+        "fused_step_w_stream": {
+            "achieved": w_bytes / (f_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": w_bytes / (f_ms / 1e3) / 1e9 / peak, "peak_source": peak_src,
+            "what": "the whole fused step (GEMM with epilogue partials, then the verify) against the "
+                    "W-streaming roofline (d*V*2 bytes per step)"},
         "mean_tokens_per_verify": float((n_all + 1).mean()),
         "roofline": {
             "bound": "hbm", "kernel": "sv::lmhead_gemm_kernel",
