@@ -200,6 +200,12 @@ def test_verify_lmhead_small_ragged_vocab():
 @pytest.mark.parametrize("mode,B,K,d,V,T", [
     ("greedy", 8, 4, 128, 1000, 1.0), ("greedy", 32, 5, 64, 8200, 1.0), ("sample", 6, 3, 64, 1000, 4.0),
     ("sample", 20, 7, 128, 3000, 6.0),
+    # M = 256 rows (the largest N; two rows per epilogue thread in the tile
+    # merge) and 63 rows per sequence in the verify launch's merge
+    ("greedy", 8, 31, 64, 1000, 1.0), ("sample", 8, 31, 64, 1000, 4.0),
+    # the smallest call, and a last tile of 8 columns (one W box, two lanes
+    # of the draft warps)
+    ("sample", 1, 1, 64, 8, 1.0), ("greedy", 2, 3, 64, 136, 1.0), ("sample", 2, 3, 64, 136, 2.0),
 ])
 def test_verify_lmhead_exact_logits(mode, B, K, d, V, T):
     # small-integer operands: the GEMM's logits are exact, so the tile
