@@ -14,11 +14,11 @@
 //
 // Persistent CTAs, one per SM, each taking the 128-column tiles t = block,
 // block + grid, ...:
-//   warp 0  TMA producer: per 64-wide step of d, two 64x64 boxes of W and one
-//           64 x N box of hidden (128-byte swizzle) into an S-stage ring that
+//   warp 0  TMA producer: per LM_BLOCK_K-deep step of d, two 64-column boxes of W and one
+//           LM_BLOCK_K x N box of hidden (128-byte / 64-byte swizzle) into an S-stage ring that
 //           runs on across tiles; stages complete on mbarriers;
 //   warp 1  allocates TMEM (two 128-lane x 256-column accumulators) and one
-//           thread issues tcgen05.mma (kind::f16, 4 per stage, K = 16 each),
+//           thread issues tcgen05.mma (kind::f16, LM_BLOCK_K / 16 per stage, K = 16 each),
 //           committing each stage back to the producer and each finished tile
 //           to the epilogue; a tile's MMAs wait until the epilogue has drained
 //           the accumulator they reuse;
@@ -52,10 +52,18 @@
 namespace sv {
 
 constexpr int LM_BLOCK_V = 128;                          // columns of V per tile (MMA M)
-constexpr int LM_BLOCK_K = 64;                           // d per stage (one 128-byte row of bf16)
-constexpr int LM_A_BYTES = LM_BLOCK_V * LM_BLOCK_K * 2;  // 16 KB: two 64 x 64 boxes of W
-constexpr int LM_BOX_BYTES = 64 * LM_BLOCK_K * 2;        // 8 KB: one box of W
-constexpr int LM_MAX_STAGES = 8;
+// d per stage. 64: one 128-byte row of bf16 per hidden row. (32, the same
+// ring bytes in twice as many stages with 64-byte swizzled hidden rows,
+// measured 1.6x slower on GB300.)
+constexpr int LM_BLOCK_K = 64;
+constexpr int LM_A_BYTES = LM_BLOCK_V * LM_BLOCK_K * 2;  // two 64-column boxes of W
+constexpr int LM_BOX_BYTES = 64 * LM_BLOCK_K * 2;        // one box of W
+constexpr int LM_MAX_STAGES = 12;
+// hidden rows are K-major with LM_BLOCK_K * 2 bytes per row: 128-byte (64)
+// or 64-byte (32) swizzle; descriptor layout codes 2 and 4
+constexpr int LM_B_ROW_BYTES = LM_BLOCK_K * 2;
+constexpr uint32_t LM_B_LAYOUT = LM_B_ROW_BYTES == 128 ? 2u : 4u;
+static_assert(LM_B_ROW_BYTES == 128 || LM_B_ROW_BYTES == 64, "hidden rows of 64 or 128 bytes");
 constexpr int LM_SMEM_BUDGET = 226 * 1024;               // dynamic shared memory (ring + epilogue)
 constexpr int LM_THREADS = 256;
 constexpr int LM_ACC_COLS = 256;                         // TMEM columns per accumulator
@@ -83,14 +91,15 @@ struct LmParams {
 };
 
 // tcgen05 shared-memory matrix descriptor: start address, leading and stride
-// byte offsets (all >> 4), descriptor version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// byte offsets (all >> 4), descriptor version 1, swizzle layout code
+// (2: 128-byte, 4: 64-byte).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)layout << 61;
     return d;
 }
 
@@ -269,7 +278,7 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
     const int S = p.stages;
     const int b_bytes = p.N * LM_BLOCK_K * 2;
     char* a_ring = smem;                      // S x 16 KB
-    char* b_ring = smem + S * LM_A_BYTES;     // S x b_bytes (b_bytes is a multiple of 2 KB)
+    char* b_ring = smem + S * LM_A_BYTES;     // S x b_bytes (b_bytes is a multiple of 1 KB)
     float* epi_tb = reinterpret_cast<float*>(b_ring + S * b_bytes);      // LM_TB_BYTES
     float2* epi_wp = reinterpret_cast<float2*>(b_ring + S * b_bytes + LM_TB_BYTES);  // LM_WP_BYTES
     __shared__ __align__(8) uint64_t full[LM_MAX_STAGES], empty[LM_MAX_STAGES];
@@ -362,11 +371,13 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
                 const uint32_t b0 = smem_u32(b_ring + s * b_bytes);
 #pragma unroll
                 for (int kk = 0; kk < LM_BLOCK_K / 16; ++kk) {
-                    // A (MN-major): 16 rows of d = two 8-row swizzle atoms (2 KB);
-                    //   LBO = the second 64-wide block of V (the second box), SBO = 8 rows.
-                    // B (K-major): 16 elements of d = 32 bytes inside the 128-byte row.
-                    const uint64_t ad = umma_desc_sw128(a0 + kk * 2048, LM_BOX_BYTES, 1024);
-                    const uint64_t bd = umma_desc_sw128(b0 + kk * 32, 16, 1024);
+                    // A (MN-major, 128-byte swizzle): 16 rows of d = two 8-row
+                    //   swizzle atoms (2 KB); LBO = the second 64-wide block of V
+                    //   (the second box), SBO = 8 rows.
+                    // B (K-major): 16 elements of d = 32 bytes inside the row;
+                    //   SBO = 8 rows of the swizzle atom.
+                    const uint64_t ad = umma_desc(a0 + kk * 2048, LM_BOX_BYTES, 1024, 2u);
+                    const uint64_t bd = umma_desc(b0 + kk * 32, 16, 8 * LM_B_ROW_BYTES, LM_B_LAYOUT);
                     umma_bf16(acc, ad, bd, idesc, (ks | kk) != 0);
                 }
                 umma_commit(&empty[s]);  // the stage is free once these MMAs completed
@@ -491,19 +502,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box [box_rows, 64]
-// (64 bf16 = 128 bytes inner), 128-byte swizzle, zero fill out of bounds.
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box [box_rows,
+// box_cols] with box_cols * 2 bytes inner (128: 128-byte swizzle, 64: 64-byte
+// swizzle), zero fill out of bounds.
 static bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                           uint32_t box_rows) {
+                           uint32_t box_rows, uint32_t box_cols) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode();
     if (!encode) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw = box_cols * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Ring stages that fit beside the epilogue's buffers (needed only when the
@@ -552,8 +565,8 @@ cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, 
     p.draft_f32 = dp ? dp->draft_f32 : 0;
     p.dparts = dp ? dp->dparts : nullptr;
     CUtensorMap tm_w, tm_h;
-    if (!encode_bf16_2d(&tm_w, W, (uint64_t)d, (uint64_t)V, 64) ||
-        !encode_bf16_2d(&tm_h, hidden, (uint64_t)M, (uint64_t)d, (uint32_t)p.N))
+    if (!encode_bf16_2d(&tm_w, W, (uint64_t)d, (uint64_t)V, LM_BLOCK_K, 64) ||
+        !encode_bf16_2d(&tm_h, hidden, (uint64_t)M, (uint64_t)d, (uint32_t)p.N, LM_BLOCK_K))
         return cudaErrorInvalidValue;
     const int smem = 1024 + p.stages * (LM_A_BYTES + p.N * LM_BLOCK_K * 2) + (parts ? LM_EPI_BYTES : 0);
     const dim3 grid((unsigned)(p.tiles < sms ? p.tiles : sms));
