@@ -3,7 +3,7 @@
 Each CUDA source compiles to an object in parallel, then nvcc links the
 shared library next to this file. The CUDA runtime is linked statically, so
 the library loads on a machine without a GPU (for the ABI tests) and needs
-nothing but the driver on a GPU machine.
+nothing but the driver on a machine with a GPU.
 """
 from __future__ import annotations
 
