@@ -106,9 +106,7 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
         if (target_parts) {
             cs = sv::fused_cluster_size(a->B, sms);
         } else if (a->flags & SV_ARG_OVERLAP_PREVIOUS) {
-            // bytes of logits one sequence reads (draft rows when any may sample)
-            const long long rows_t = (long long)a->K + 1, rows_d = may_sample ? a->K : 0;
-            cs = sv::overlap_cluster_size(a->B, (rows_t * (long long)es_t + rows_d * (long long)es_d) * a->V, sms);
+            cs = sv::overlap_cluster_size();
         } else {
             cs = sv::auto_cluster_size(a->B, a->V, (int)es_t, sms);
         }

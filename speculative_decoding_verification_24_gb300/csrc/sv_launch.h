@@ -48,7 +48,7 @@ struct VerifyParams {
 int auto_cluster_size(int B, int V, int esize, int num_sms);
 
 // Cluster size for a call that overlaps the previous one on its stream.
-int overlap_cluster_size(int B, long long bytes_per_seq, int num_sms);
+int overlap_cluster_size();
 
 // Cluster size for the LM-head path's verify launch.
 int fused_cluster_size(int B, int num_sms);

@@ -1879,23 +1879,14 @@ int auto_cluster_size(int B, int V, int esize, int num_sms) {
     return cs < lo ? lo : cs;
 }
 
-// For calls that overlap the previous one. Consecutive overlapping calls
-// still finish one after another (each stores only once the previous call has
-// completed, a few microseconds per call), so a call whose logits HBM streams
-// in less than that runs on one CTA per sequence: it holds few SMs, and many
-// calls run at once. A larger call takes the largest power of two that still
-// gives every CTA at least 256 KB of its logits and keeps it within one wave
-// of resident CTAs (two per SM). Both measured best on GB300 for the
-// workloads (B=8 x 11 rows of 32000 fp32; B=64 x 9 rows of 128256 bf16).
-constexpr long long OVERLAP_SMALL_CALL_BYTES = 32LL << 20;
-
-int overlap_cluster_size(int B, long long bytes_per_seq, int num_sms) {
-    int cs = 1;
-    if ((long long)B * bytes_per_seq < OVERLAP_SMALL_CALL_BYTES) return cs;
-    while (cs < MAX_CS && bytes_per_seq / (2LL * cs) >= 256 * 1024 && (long long)B * cs * 2 <= 2LL * num_sms)
-        cs *= 2;
-    return cs;
-}
+// For calls that overlap the previous one: one CTA per sequence. Consecutive
+// overlapping calls finish one after another (each stores only once the
+// previous call has completed, about 2 us per call), so what sets the rate is
+// how many calls' copies are in flight: few CTAs per call, two per SM, let
+// many calls run at once. Measured best on GB300 against clusters of 2-8 for
+// B=8 x 11 rows of 32000 fp32 and B=64 x (5 or 9) rows of 128256 bf16
+// (22.3 us per call against 26.1 us with clusters of 4).
+int overlap_cluster_size() { return 1; }
 
 // For the LM-head path, whose verify streams only the final draw's rows: the
 // largest power of two (at most 8) that keeps every CTA of the launch on its
