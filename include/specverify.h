@@ -157,7 +157,10 @@ typedef struct {
  * enqueued just before it on `stream`, so the call may start reading them
  * while that work (typically the previous verify call) is still running. Its
  * outputs are still written only after that work has completed. Without the
- * flag a call starts after everything before it on the stream. */
+ * flag a call starts after everything before it on the stream. Such a call
+ * runs one CTA per sequence (unless cluster_size asks otherwise), two per SM,
+ * so that consecutive calls share the GPU; a lone call without the flag
+ * spreads each sequence over a cluster of CTAs instead. */
 #define SV_ARG_OVERLAP_PREVIOUS 1u
 
 /* sv_verify_args.flags, for tests of the failure path only: every CTA also
