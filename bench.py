@@ -168,6 +168,29 @@ def workload_sets(name: str, device, l2_bytes: int):
     return sets, set_bytes
 
 
+def acceptance(name: str, n_all: np.ndarray, first: int, count: int, n_sets: int, K: int) -> dict:
+    """Mean tokens per verify (accepted drafts + 1) and the fraction of
+    sequences that accepted draft i, i = 0..K-1, over the timed steps; for c2
+    per draft-noise level tau (the input sets cycle over the three)."""
+    from synth.workloads import WORKLOADS
+
+    def stats(rows):
+        rows = rows[rows >= 0]
+        if rows.size == 0:
+            return {}
+        return {"sequences": int(rows.size), "mean_tokens_per_verify": float((rows + 1).mean()),
+                "accepted_at_position": [float((rows > i).mean()) for i in range(K)]}
+
+    steps = list(range(first, first + count))
+    out = {"all": stats(n_all[steps].reshape(-1))}
+    if name == "c2":
+        taus = list(WORKLOADS["c2"]["tau"])
+        for t_i, tau in enumerate(taus):
+            sel = [i for i in steps if (i % n_sets) % len(taus) == t_i]
+            out[f"tau={tau}"] = stats(n_all[sel].reshape(-1))
+    return out
+
+
 def describe(name: str) -> str:
     return {
         "c1": "B=1 K=4 V=1000 fp32, N(0,3^2)+Zipf(1.1) target, draft=target+N(0,1), T=1",
@@ -399,6 +422,7 @@ def run_ours(args, rank, world, device):
                    "how": "the same graph of K steps launched without SV_ARG_OVERLAP_PREVIOUS: "
                           "each call starts after the previous one has completed"},
     }
+    result["acceptance"] = acceptance(args.workload, n_all, args.warmup, args.steps, len(sets), K1 - 1)
     result["e2e"] = run_e2e(args, sets, device, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(sets, args.cpu_seconds)
