@@ -276,8 +276,10 @@ static size_t lmhead_logits_bytes(long long M, long long V) {
     return (size_t)(((M * V * 4) + 255) / 256 * 256);
 }
 
-// The LM-head verify's workspace: the fp32 logits [M, V], then one 8-byte
-// partial per row and 128-column tile ([tiles, M]), each part 256-aligned.
+// The LM-head verify's workspace: the fp32 logits [M, V], then room for one
+// 8-byte partial per row and 128-column tile ([tiles, M]; the GEMM, one CTA
+// per SM over at most that many tiles, uses the first rows), each part
+// 256-aligned.
 static long long lmhead_tiles(long long V) { return (V + sv::LM_TILE_V - 1) / sv::LM_TILE_V; }
 static size_t lmhead_parts_bytes(long long M, long long V) {
     return (size_t)((lmhead_tiles(V) * M * 8 + 255) / 256 * 256);
@@ -359,13 +361,14 @@ extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const
     float2* dparts = reinterpret_cast<float2*>(ws + lmhead_logits_bytes(M, V) + lmhead_parts_bytes(M, V));
     sv::LmDraftParts dp{draft_logits, B * K, draft_dtype == SV_F32 ? 1 : 0, dparts};
     const bool sample = mode == SV_SAMPLE;
+    int gemm_ctas = 0;
     cudaError_t e = sv::launch_lmhead_gemm(hidden, W, (int)M, d, V, static_cast<float*>(workspace), parts, c,
-                                           sample ? 1 : 0, sample ? &dp : nullptr, nullptr, (cudaStream_t)stream);
+                                           sample ? 1 : 0, sample ? &dp : nullptr, nullptr, (cudaStream_t)stream,
+                                           &gemm_ctas);
     if (e != cudaSuccess) return fail_cuda(e);
     // the verify grid may start as the GEMM's CTAs finish; it waits for the
-    // GEMM before it reads the logits and the partials
-    return verify_impl(&a, SV_F32, sample ? draft_dtype : SV_F32, parts, (int)lmhead_tiles(V),
-                       sample ? dparts : nullptr);
+    // GEMM before it reads the logits and the partials (one per row and CTA)
+    return verify_impl(&a, SV_F32, sample ? draft_dtype : SV_F32, parts, gemm_ctas, sample ? dparts : nullptr);
 }
 
 // ---------------------------------------------------------------------------

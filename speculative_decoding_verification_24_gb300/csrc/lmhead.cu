@@ -33,10 +33,12 @@
 // reduces every row of the tile to one softmax partial (R, s) in the base-2
 // domain, or to the row's (max, lowest index) in greedy mode: a warp's 32
 // columns are turned over through shared memory so that lane l holds row
-// c0 + l, each lane reduces its row over those columns, and the four warps'
-// partials merge in warp order. The verify kernel merges the tiles' partials
-// instead of streaming the target rows again; it re-reads one target row per
-// sequence only for the final draw.
+// c0 + l, each lane reduces its row over those columns, the four warps'
+// partials merge in warp order, and each row's partial merges into the
+// CTA's running partial of that row (its tiles in order), written once at the
+// end. The verify kernel merges the CTAs' partials instead of streaming the
+// target rows again; it re-reads one target row per sequence only for the
+// final draw.
 // Every mbarrier wait is bounded; a wait that gives up sets SV_FLAG_TIMEOUT,
 // the CTA stops issuing work, waits for what it issued and frees TMEM.
 #include <cuda.h>
@@ -70,6 +72,7 @@ constexpr int LM_ACC_COLS = 256;                         // TMEM columns per acc
 constexpr int LM_TMEM_COLS = 2 * LM_ACC_COLS;
 constexpr uint32_t LM_WAIT_LIMIT = 1u << 24;
 constexpr int LM_EPI_WARPS = 4;
+constexpr int LM_MAX_ROWS = 256;                          // M = B*(K+1) and B*K at most
 constexpr int LM_TB_STRIDE = 33;                          // padded row: conflict-free both ways
 constexpr int LM_TB_BYTES = LM_EPI_WARPS * 32 * LM_TB_STRIDE * 4;   // per-warp 32 x 32 turn-over
 constexpr int LM_WP_BYTES = LM_EPI_WARPS * 256 * 8;                 // per-warp row partials
@@ -81,13 +84,13 @@ struct LmParams {
     int tiles;          // ceil(V / LM_BLOCK_V)
     float* out;         // [M, V]
     uint32_t* status;   // optional
-    float2* parts;      // [tiles, M] per-tile row partials, or nullptr (logits only)
+    float2* parts;      // [grid, M] each CTA's row partials over its tiles, or nullptr (logits only)
     float c;            // log2(e) / temperature (soft partials)
     int part_soft;      // 1: (R, s) softmax partials; 0: (max, lowest index)
     // Sample mode: the draft rows' softmax partials per tile, by warps 2-3.
     const void* draft;  // [Md, V] draft logits (fp32 or bf16), or nullptr
     int Md, draft_f32;  // draft rows; element type
-    float2* dparts;     // [tiles, Md]
+    float2* dparts;     // [grid, Md]
 };
 
 // tcgen05 shared-memory matrix descriptor: start address, leading and stride
@@ -196,25 +199,36 @@ __device__ __forceinline__ bool epi_barrier_and(bool v) {
     return r != 0;
 }
 
-// Draft-row partials for every tile of this CTA, by one of two warps (w2):
-// lane l holds columns v0 + 4l .. v0 + 4l + 3 of a row (V is a multiple of
-// 8, so the four are inside the row or past its end together); a warp
-// reduction gives the tile's maximum, then R = ceil(max * c) and
-// s = sum 2^(l*c - R) exactly as the epilogue forms the target rows'
-// partials. Rows go in batches (32 bf16 or 16 fp32 rows per warp) whose
-// loads are in flight together: these loads compete with the W stream, and
-// only many of them in flight keep the two warps ahead of the GEMM.
+// Draft-row partials over this CTA's tiles, by one of two warps (w2): lane l
+// holds columns v0 + 4l .. v0 + 4l + 3 of a row (V is a multiple of 8, so the
+// four are inside the row or past its end together); a warp reduction gives
+// the tile's maximum, then R = ceil(max * c) and s = sum 2^(l*c - R) exactly
+// as the epilogue forms the target rows' partials. Rows go in batches (32
+// bf16 or 16 fp32 rows per warp) whose loads are in flight together: these
+// loads compete with the W stream, and only many of them in flight keep the
+// two warps ahead of the GEMM. Lane k keeps the running partial of row k of
+// each of its batches across the tiles (in tile order) and writes it once,
+// at the end: one partial per row and CTA.
 template <bool F32>
 __device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int lane, int my_tiles, const int* err) {
     constexpr int RB = F32 ? 16 : 32;
+    constexpr int MAXB = (LM_MAX_ROWS + 2 * RB - 1) / (2 * RB);  // batches per warp
     using Raw = typename std::conditional<F32, uint4, uint2>::type;
     constexpr int ESZ = F32 ? 4 : 2;
     const bool vec = (reinterpret_cast<uintptr_t>(p.draft) & (uintptr_t)(4 * ESZ - 1)) == 0;
-    for (int li = 0; li < my_tiles && !lm_error(err); ++li) {
+    const float2 empty = pack(SoftPart{-INFINITY, 0.0f});
+    float2 run[MAXB];  // indexed at run time: a few bytes of local memory per lane
+#pragma unroll
+    for (int bi = 0; bi < MAXB; ++bi) run[bi] = empty;
+    int li = 0;
+    for (; li < my_tiles && !lm_error(err); ++li) {
         const int tile = (int)blockIdx.x + li * (int)gridDim.x;
         const int e = tile * LM_BLOCK_V + 4 * lane;
         const bool in = e < p.V;
-        for (int m0 = w2 * RB; m0 < p.Md; m0 += 2 * RB) {
+#pragma unroll 1
+        for (int bi = 0; bi < MAXB; ++bi) {
+            const int m0 = w2 * RB + bi * 2 * RB;
+            if (m0 >= p.Md) break;
             Raw raw[RB];
 #pragma unroll
             for (int k = 0; k < RB; ++k) {
@@ -243,6 +257,7 @@ __device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int la
                     }
                 }
             }
+            float2 mine = empty;  // lane k: row m0 + k of this batch
 #pragma unroll
             for (int k = 0; k < RB; ++k) {
                 float x[4];
@@ -261,11 +276,18 @@ __device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int la
                           (ex2(fmaf(x[2], p.c, nR)) + ex2(fmaf(x[3], p.c, nR)));
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0 && m0 + k < p.Md)
-                    p.dparts[(size_t)tile * p.Md + m0 + k] =
-                        R == -INFINITY ? pack(SoftPart{-INFINITY, 0.0f}) : pack(SoftPart{R, s});
+                if (lane == k) mine = R == -INFINITY ? empty : pack(SoftPart{R, s});
             }
+            run[bi] = pack(merge_soft(as_soft(run[bi]), as_soft(mine)));
         }
+    }
+    // an unfinished CTA (a wait that gave up) reports NaN: its rows are invalid
+    const bool done = li == my_tiles;
+#pragma unroll
+    for (int bi = 0; bi < MAXB; ++bi) {
+        const int m = w2 * RB + bi * 2 * RB + lane;
+        if (lane < RB && m < p.Md)
+            p.dparts[(size_t)blockIdx.x * p.Md + m] = done ? run[bi] : make_float2(__int_as_float(0x7fc00000), 0.0f);
     }
 }
 
@@ -397,7 +419,12 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
         // ---- epilogue: TMEM -> registers -> global (coalesced per column)
         const int q = warp - 4;
         float* tb = epi_tb + q * 32 * LM_TB_STRIDE;
-        for (int li = 0; li < my_tiles; ++li) {
+        // thread t's running partials of rows t and t + 128 over this CTA's
+        // tiles (merged in tile order; written once, at the end)
+        const float2 empty = p.part_soft ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
+        float2 run0 = empty, run1 = empty;
+        int li = 0;
+        for (; li < my_tiles; ++li) {
             const int a = li & 1;
             bool ok = mbar_wait(&acc_full[a], (li >> 1) & 1, LM_WAIT_LIMIT);
             tmem_fence_after();
@@ -464,14 +491,31 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
             if (p.parts) {
                 // the four warps' partials of every row, merged in warp order
                 epi_barrier();
-                for (int m = (int)threadIdx.x - 128; m < p.M; m += LM_EPI_WARPS * 32) {
-                    float2 acc2 = epi_wp[m];
 #pragma unroll
-                    for (int w = 1; w < LM_EPI_WARPS; ++w)
-                        acc2 = p.part_soft ? pack(merge_soft(as_soft(acc2), as_soft(epi_wp[w * 256 + m])))
-                                           : pack(merge_arg(as_arg(acc2), as_arg(epi_wp[w * 256 + m])));
-                    p.parts[(size_t)tile * p.M + m] = acc2;
+                for (int h = 0; h < 2; ++h) {
+                    const int m = (int)threadIdx.x - 128 + h * 128;
+                    if (m < p.M) {
+                        float2 acc2 = epi_wp[m];
+#pragma unroll
+                        for (int w = 1; w < LM_EPI_WARPS; ++w)
+                            acc2 = p.part_soft ? pack(merge_soft(as_soft(acc2), as_soft(epi_wp[w * 256 + m])))
+                                               : pack(merge_arg(as_arg(acc2), as_arg(epi_wp[w * 256 + m])));
+                        float2& run = h == 0 ? run0 : run1;
+                        run = p.part_soft ? pack(merge_soft(as_soft(run), as_soft(acc2)))
+                                          : pack(merge_arg(as_arg(run), as_arg(acc2)));
+                    }
                 }
+            }
+        }
+        if (p.parts) {
+            // one partial per row and CTA; an unfinished CTA (a wait that
+            // gave up) reports NaN, so the verify marks its rows invalid
+            const bool done = li == my_tiles;
+            const float2 nan2 = make_float2(__int_as_float(0x7fc00000), 0.0f);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = (int)threadIdx.x - 128 + h * 128;
+                if (m < p.M) p.parts[(size_t)blockIdx.x * p.M + m] = done ? (h == 0 ? run0 : run1) : nan2;
             }
         }
     }
@@ -531,7 +575,7 @@ static std::atomic<int> g_lm_sms[64];
 
 cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
                                float2* parts, float c, int part_soft, const LmDraftParts* dp,
-                               uint32_t* status, cudaStream_t stream) {
+                               uint32_t* status, cudaStream_t stream, int* grid_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -570,6 +614,7 @@ cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, 
         return cudaErrorInvalidValue;
     const int smem = 1024 + p.stages * (LM_A_BYTES + p.N * LM_BLOCK_K * 2) + (parts ? LM_EPI_BYTES : 0);
     const dim3 grid((unsigned)(p.tiles < sms ? p.tiles : sms));
+    if (grid_out) *grid_out = (int)grid.x;
     lmhead_gemm_kernel<<<grid, LM_THREADS, smem, stream>>>(tm_w, tm_h, p);
     return cudaGetLastError();
 }

@@ -32,14 +32,14 @@ struct VerifyParams {
     const int32_t* tree_parents;
     int32_t* out_last_node;    // [B] or nullptr (tree mode)
     int test_wait_timeout;     // tests of the failure path: a bounded wait that gives up
-    // LM-head path: the target rows' statistics come as per-tile partials
-    // from the GEMM epilogue (parts[tile * part_M + b * (K+1) + i], part_tiles
-    // tiles), written by the grid launched just before this one on the
-    // stream; the target rows are then read only for the logits at the draft
-    // tokens and the final draw, after that grid has completed.
+    // LM-head path: the target rows' statistics come as partials from the
+    // GEMM epilogue, one per row and GEMM CTA (parts[cta * part_M + b * (K+1)
+    // + i], part_tiles CTAs), written by the grid launched just before this
+    // one on the stream; the target rows are then read only for the logits at
+    // the draft tokens and the final draw, after that grid has completed.
     const float2* target_parts;
     int part_tiles, part_M;
-    // With target_parts: the draft rows' partials too (parts[tile * B*K +
+    // With target_parts: the draft rows' partials too (parts[cta * B*K +
     // b * K + i]), or nullptr (the draft rows are streamed in pass 1).
     const float2* draft_parts;
 };
@@ -79,11 +79,12 @@ cudaError_t launch_prompt_lookup(const int32_t* tokens, const int32_t* lengths, 
 cudaError_t launch_commit(int32_t* tokens, int32_t* lengths, int B, int L_max, const int32_t* out_tokens,
                           const int32_t* n_accepted, int K, int32_t* out_n_committed, cudaStream_t stream);
 
-// With parts != nullptr the epilogue also writes every row's partial per
-// 128-column tile (parts[tile * M + m]): base-2 softmax partials (R, s) at
-// scale c = log2(e) / T when part_soft, else (max, lowest index).
-// With dp != nullptr (sample mode) two otherwise idle warps also write the
-// draft rows' softmax partials per tile (dparts[tile * Md + m]).
+// With parts != nullptr the epilogue also reduces every row over each
+// 128-column tile and merges the tiles of each CTA in tile order, writing one
+// partial per row and CTA (parts[cta * M + m], *grid_out CTAs): base-2
+// softmax partials (R, s) at scale c = log2(e) / T when part_soft, else
+// (max, lowest index). With dp != nullptr (sample mode) two otherwise idle
+// warps do the same for the draft rows (dparts[cta * Md + m]).
 constexpr int LM_TILE_V = 128;
 struct LmDraftParts {
     const void* draft;  // [Md, V], fp32 or bf16
@@ -92,6 +93,6 @@ struct LmDraftParts {
 };
 cudaError_t launch_lmhead_gemm(const void* hidden, const void* W, int M, int d, int V, float* out,
                                float2* parts, float c, int part_soft, const LmDraftParts* dp,
-                               uint32_t* status, cudaStream_t stream);
+                               uint32_t* status, cudaStream_t stream, int* grid_out = nullptr);
 
 }  // namespace sv

@@ -1193,10 +1193,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 lt_early = __ldcg(target_row(tgt, b, K, V, lane) + x_reg);
         }
         // This CTA's share of every row computed by the GEMM is the merge of
-        // its contiguous run of the tiles' partials: lanes take every 32nd
-        // tile in order (four loads in flight), then a butterfly merges the
-        // lanes (the merges are symmetric, so every lane ends with the same
-        // bits).
+        // its contiguous run of the GEMM CTAs' partials: lanes take every
+        // 32nd one in order (four loads in flight), then a butterfly merges
+        // the lanes (the merges are symmetric, so every lane ends with the
+        // same bits).
         int t0, t1;
         split_range(p.part_tiles, rank, CS, t0, t1);
         const float2 empty = use_soft ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});

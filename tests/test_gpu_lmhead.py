@@ -106,33 +106,48 @@ def greedy_ties(ref_logits, B, K1, delta):
     return ((top2[..., 1] - top2[..., 0]) < 2 * delta + 1e-12).any(axis=1)
 
 
-def workspace_parts(ws, M, V):
-    """The per-tile row partials the fused call leaves after its fp32 logits:
-    [ceil(V/128), M, 2] float32 (sample: R, s; greedy: the maximum and, as
-    int32 bits, its index)."""
-    off = (M * V * 4 + 255) // 256 * 256
+def gemm_ctas(V):
+    """The LM-head GEMM runs one CTA per SM over the 128-column tiles (at most
+    one CTA per tile); CTA b computes tiles b, b + G, b + 2G, ..."""
     tiles = (V + 127) // 128
-    return ws[off:off + tiles * M * 8].view(torch.float32).reshape(tiles, M, 2).cpu().numpy()
+    return min(tiles, torch.cuda.get_device_properties(0).multi_processor_count)
+
+
+def workspace_parts(ws, M, V):
+    """The target rows' partials the fused call leaves after its fp32 logits,
+    one per GEMM CTA and row: [G, M, 2] float32 (sample: R, s; greedy: the
+    maximum and, as int32 bits, its index)."""
+    off = (M * V * 4 + 255) // 256 * 256
+    G = gemm_ctas(V)
+    return ws[off:off + G * M * 8].view(torch.float32).reshape(G, M, 2).cpu().numpy()
 
 
 def expected_parts(logits, V, mode, T):
-    """Each row's partial over each 128-column tile, from its definition:
-    sample R = ceil(max(l) * c) with c = log2(e)/T (both products rounded to
-    float32, as the scale is a float32) and s = sum 2^(l*c - R) in float64;
-    greedy the largest logit and its lowest index."""
+    """Each GEMM CTA's partial of every row over the columns of its tiles,
+    from the definition: sample R = ceil(max(l) * c) with c = log2(e)/T (both
+    products rounded to float32, as the scale is a float32) and
+    s = sum 2^(l*c - R) in float64; greedy the largest logit and its lowest
+    index."""
     M = logits.shape[0]
     tiles = (V + 127) // 128
+    G = gemm_ctas(V)
     pad = np.full((M, tiles * 128), -np.inf)
     pad[:, :V] = logits
-    blk = pad.reshape(M, tiles, 128).transpose(1, 0, 2)  # [tiles, M, 128]
-    if mode == "sample":
-        c32 = np.float32(1.4426950408889634 / T)
-        mx = blk.max(axis=2).astype(np.float32)
-        R = np.ceil(mx * c32).astype(np.float64)
-        s = np.exp2(blk * np.float64(c32) - R[..., None]).sum(axis=2)
-        return R, s
-    idx = blk.argmax(axis=2)  # first occurrence
-    return blk.max(axis=2), idx + 128 * np.arange(tiles)[:, None]
+    blk = pad.reshape(M, tiles, 128)
+    c32 = np.float32(1.4426950408889634 / T)
+    first = np.zeros((G, M))
+    second = np.zeros((G, M)) if mode == "sample" else np.zeros((G, M), dtype=np.int64)
+    for b in range(G):
+        cols = blk[:, b::G, :].reshape(M, -1)  # its tiles in order: increasing column index
+        if mode == "sample":
+            R = np.ceil(cols.max(axis=1).astype(np.float32) * c32).astype(np.float64)
+            first[b] = R
+            second[b] = np.exp2(cols * np.float64(c32) - R[:, None]).sum(axis=1)
+        else:
+            loc = cols.argmax(axis=1)  # first occurrence
+            first[b] = cols.max(axis=1)
+            second[b] = (b + G * (loc // 128)) * 128 + loc % 128
+    return first, second
 
 
 def check_parts(ws, logits, V, mode, T):
@@ -268,9 +283,9 @@ def test_verify_lmhead_draft_layouts(draft_dtype, offset):
     logits = spec_lmhead_logits(hidden, W)
     torch.cuda.synchronize()
     # the draft rows' partials (after the target rows') are their reductions
-    M, Md, tiles = B * K1, B * K, (V + 127) // 128
+    M, Md, tiles, G = B * K1, B * K, (V + 127) // 128, gemm_ctas(V)
     off = (M * V * 4 + 255) // 256 * 256 + (tiles * M * 8 + 255) // 256 * 256
-    got = ws[off:off + tiles * Md * 8].view(torch.float32).reshape(tiles, Md, 2).cpu().numpy()
+    got = ws[off:off + G * Md * 8].view(torch.float32).reshape(G, Md, 2).cpu().numpy()
     R, s = expected_parts(draft.float().reshape(Md, V).numpy().astype(np.float64), V, "sample", case.temperature)
     assert np.array_equal(got[..., 0].astype(np.float64), R)
     np.testing.assert_allclose(got[..., 1], s, rtol=1e-5)
