@@ -50,10 +50,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+# Sources of the kernels the traffic record covers (the verify kernel, the
+# LM-head GEMM and the launch decisions made for them); the drafting and
+# commit kernels of the decode loop are not in it.
+TRAFFIC_SOURCES = ("api.cu", "lmhead.cu", "sv_device.cuh", "sv_launch.h", "verify_logits.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_24_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in TRAFFIC_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

@@ -185,13 +185,13 @@ size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V);
  * spec_verify does. ("Speculative decoding", denimpatel.github.io
  * interactive course, section "Memory-bound, not compute-bound": the K+1
  * verification rows come from one forward pass that reads the head's
- * weights once.) The GEMM's epilogue reduces each 128-column tile of every
- * row to a softmax partial (sample) or its maximum and lowest index
- * (greedy); the verify step merges those instead of re-reading the rows and
- * reads one target row per sequence again only for the final draw. In
- * sample mode the GEMM kernel also reduces the draft rows to per-tile
- * partials. Two kernels on `stream`; the second may start while the first
- * finishes.
+ * weights once.) The GEMM's epilogue reduces every row over the 128-column
+ * tiles each of its CTAs computes to a softmax partial (sample) or its
+ * maximum and lowest index (greedy); the verify step merges those instead of
+ * re-reading the rows and reads one target row per sequence again only for
+ * the final draw. In sample mode the GEMM kernel also reduces the draft rows
+ * the same way. Two kernels on `stream`; the second may start while the
+ * first finishes.
  *   hidden [B, K+1, d] bf16 (device), W [d, V] bf16 (device, V contiguous),
  *   draft_logits [B, K, V] of draft_dtype (device; NULL in greedy mode),
  *   d a positive multiple of 64, V a positive multiple of 8, B * (K+1) <= 256;
@@ -199,10 +199,10 @@ size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V);
  *   workspace: device buffer of at least
  *   spec_verify_lmhead_workspace_bytes(B, K, d, V) bytes, 256-byte aligned;
  *   it receives the fp32 target logits [B*(K+1), V], then the target rows'
- *   per-tile partials [ceil(V/128), B*(K+1)] and (sample mode) the draft
- *   rows' [ceil(V/128), B*K], 8 bytes each (every byte the call reads there
- *   it wrote first, so no initial contents are needed); it may be reused
- *   once the call's work on `stream` has completed.
+ *   partials (one per row and GEMM CTA, room for ceil(V/128) CTAs) and
+ *   (sample mode) the draft rows', 8 bytes each (every byte the call reads
+ *   there it wrote first, so no initial contents are needed); it may be
+ *   reused once the call's work on `stream` has completed.
  * Other arguments as in spec_verify. */
 sv_status spec_verify_lmhead(const void* hidden, const void* W,
                              const void* draft_logits,
