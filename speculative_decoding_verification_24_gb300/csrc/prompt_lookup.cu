@@ -15,6 +15,7 @@
 // rank 0 writes the drafts.
 #include <cooperative_groups.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "sv_device.cuh"
@@ -48,27 +49,20 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int32_t* seq = tokens + (size_t)b * L_max;
     int32_t* out = out_drafts + (size_t)b * n_drafts;
-    const int L = __ldg(lengths + b);
-    const bool valid = L >= 0 && L <= L_max;
-    if (valid && tid < max_ngram && tid < L) suffix[tid] = __ldg(seq + (L - 1 - tid));
-    if (!valid) {  // the same for every CTA of the cluster: none takes part in a cluster barrier
-        if (rank == 0) {
-            for (int i = tid; i < n_drafts; i += PL_THREADS) out[i] = -1;
-            if (tid == 0) out_n[b] = -1;
-        }
-        return;
-    }
-    // windows end at e = 0 .. L-2; this CTA takes e in [p0, p1)
-    const int n_pos = L - 1 > 0 ? L - 1 : 0;
-    const int per = (n_pos + CS - 1) / CS;
-    const int p0 = min(n_pos, rank * per), p1 = min(n_pos, p0 + per);
-    const int n_tiles = (p1 - p0 + PL_TILE - 1) / PL_TILE;
+    // The parts are cut from the window ends the buffer allows (0 .. L_max-2),
+    // not the sequence's own, so that the first tile's loads go out before
+    // the length has arrived; the scan then stops at the sequence's last
+    // window end, L-2. (Loads past the sequence stay inside its row of the
+    // buffer and are never compared.)
+    const int n_buf = L_max - 1 > 0 ? L_max - 1 : 0;
+    const int per = (n_buf + CS - 1) / CS;
+    const int p0 = min(n_buf, rank * per), p1_buf = min(n_buf, p0 + per);
     int32_t r[PL_PER], h = 0;
-    auto load = [&](int t0) {
+    auto load = [&](int t0, int lim) {
 #pragma unroll
         for (int k = 0; k < PL_PER; ++k) {
             const int i = t0 + k * PL_THREADS + tid;
-            r[k] = i < p1 ? __ldg(seq + i) : 0;
+            r[k] = i < lim ? __ldg(seq + i) : 0;
         }
         if (tid < PL_HALO) {
             const int i = t0 - PL_HALO + tid;
@@ -80,21 +74,42 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
         for (int k = 0; k < PL_PER; ++k) tile[buf][PL_HALO + k * PL_THREADS + tid] = r[k];
         if (tid < PL_HALO) tile[buf][tid] = h;
     };
-    long long best = -1;  // (ml << 32) | e, the largest over this thread's windows
-    if (n_tiles > 0) {
-        load(p0);
-        store(0);
+    if (p0 < p1_buf) load(p0, p1_buf);  // in flight while the length arrives
+    const int L = __ldg(lengths + b);
+    const bool valid = L >= 0 && L <= L_max;
+    if (valid && tid < max_ngram && tid < L) suffix[tid] = __ldg(seq + (L - 1 - tid));
+    if (!valid) {  // the same for every CTA of the cluster: none takes part in a cluster barrier
+        if (rank == 0) {
+            for (int i = tid; i < n_drafts; i += PL_THREADS) out[i] = -1;
+            if (tid == 0) out_n[b] = -1;
+        }
+        return;
     }
+    // Every CTA of the cluster has started once this phase of the cluster
+    // barrier completes; its wait comes just before rank 0's shared memory is
+    // written, by which time it has long completed.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    // windows end at e = 0 .. L-2; this CTA takes e in [p0, p1)
+    const int n_pos = L - 1 > 0 ? L - 1 : 0;
+    const int p1 = max(p0, min(p1_buf, n_pos));
+    const int n_tiles = (p1 - p0 + PL_TILE - 1) / PL_TILE;
+    // (ml << 32) | e, the largest over this thread's windows. A window whose
+    // last token differs from the sequence's last has ml = 0, and the largest
+    // such key is this CTA's last window end, p1 - 1: so only windows that
+    // match the last token need the rest of the comparison.
+    long long best = (tid == 0 && p1 > p0) ? (long long)(p1 - 1) : -1;
+    if (n_tiles > 0) store(0);
     __syncthreads();
+    const int32_t s0 = n_tiles > 0 ? suffix[0] : 0;
     for (int ti = 0; ti < n_tiles; ++ti) {
         const int t0 = p0 + ti * PL_TILE, buf = ti & 1;
-        if (ti + 1 < n_tiles) load(t0 + PL_TILE);  // in flight during the scan below
+        if (ti + 1 < n_tiles) load(t0 + PL_TILE, p1);  // in flight during the scan below
         const int32_t* tl = tile[buf] + PL_HALO - t0;  // tl[i] = token i for t0 - PL_HALO <= i < t0 + PL_TILE
-#pragma unroll 4
+#pragma unroll
         for (int k = 0; k < PL_PER; ++k) {
             const int e = t0 + k * PL_THREADS + tid;
-            if (e < p1) {
-                int ml = 0;
+            if (e < p1 && tl[e] == s0) {
+                int ml = 1;
                 while (ml < max_ngram && e - ml >= 0 && tl[e - ml] == suffix[ml]) ++ml;
                 const long long key = ((long long)ml << 32) | (unsigned)e;
                 best = key > best ? key : best;
@@ -110,7 +125,6 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
     }
     if (lane == 0) warp_best[warp] = best;
     __syncthreads();
-    cluster.sync();  // every CTA of the cluster runs: rank 0's shared memory may be written
     if (warp == 0) {
         best = lane < PL_THREADS / 32 ? warp_best[lane] : -1;
 #pragma unroll
@@ -118,8 +132,9 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
             const long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
             best = other > best ? other : best;
         }
-        if (lane == 0) cluster.map_shared_rank(cta_best, 0)[rank] = best;
     }
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA has started
+    if (warp == 0 && lane == 0) cluster.map_shared_rank(cta_best, 0)[rank] = best;
     cluster.sync();
     if (rank == 0 && warp == 0) {
         best = lane < CS ? cta_best[lane] : -1;
@@ -137,14 +152,38 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
     }
 }
 
+// CTAs of the lookup kernel that fit on the GPU at once (per device, cached).
+static std::atomic<int> g_pl_resident[64];
+
+static int pl_resident_ctas() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = g_pl_resident[dev].load(std::memory_order_acquire);
+    if (n == 0) {
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prompt_lookup_kernel, PL_THREADS, 0) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        n = per_sm * sms;
+        g_pl_resident[dev].store(n, std::memory_order_release);
+    }
+    return n;
+}
+
 // The cluster size: one CTA per tile of the longest possible context, at most
-// PL_MAX_CLUSTER.
+// PL_MAX_CLUSTER, and no more than keeps the whole grid resident at once (a
+// CTA then scans several tiles, the next one's loads in flight during the
+// scan of the current one).
 cudaError_t launch_prompt_lookup(const int32_t* tokens, const int32_t* lengths, int B, int L_max,
                                  int max_ngram, int n_drafts, int32_t* out_drafts, int32_t* out_n,
                                  cudaStream_t stream) {
     int cs = (L_max + PL_TILE - 1) / PL_TILE;
     cs = cs < 1 ? 1 : cs > PL_MAX_CLUSTER ? PL_MAX_CLUSTER : cs;
     while (cs & (cs - 1)) ++cs;  // a power of two (1, 2, 4, 8)
+    const int resident = pl_resident_ctas();
+    while (cs > 1 && resident > 0 && (long long)B * cs > resident) cs >>= 1;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     cfg.gridDim = dim3((unsigned)(B * cs), 1, 1);
