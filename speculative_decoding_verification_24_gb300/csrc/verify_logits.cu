@@ -1038,6 +1038,11 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     constexpr bool CAN_SAMPLE = (MS & MS_SAMPLE) != 0, CAN_GREEDY = (MS & MS_GREEDY) != 0;
     extern __shared__ __align__(128) char ring[];
     __shared__ SeqShared sh;
+    // The next call on the stream may launch as soon as every CTA of this one
+    // has started (its stores still wait for this one to complete): first
+    // thing, so that consecutive calls launch at the hardware's pace rather
+    // than one prologue apart.
+    launch_dependents();
     cg::cluster_group cluster = cg::this_cluster();
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -1138,9 +1143,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     }
     __syncthreads();
     const int total_chunks = mode_ok ? sh.total_chunks : 0;
-    // The next call on the stream may launch once every CTA of this one has
-    // started: its first pass then overlaps this call wherever SMs have room.
-    launch_dependents();
 
     WarpRing wr{warp, 0u, 0u};
     uint32_t seq = 0;  // chunks this warp has handled, over both passes
