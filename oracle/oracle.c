@@ -169,10 +169,11 @@ static void row_softmax(const void* base, int dtype, size_t row_off, int V,
 }
 
 /* Inverse CDF in index order: the smallest k with sum_{v<=k} r_v > t, where
- * t = u2 * sum_v r_v. Writes the distance from t to the nearer edge of the
- * chosen token's interval (in the units of r) to *margin. */
+ * t = u2 * sum_v r_v. Writes the distances from t down to the lower and up to
+ * the upper edge of the chosen token's interval (in the units of r) to
+ * edges[0], edges[1], and the smaller of the two to *margin. */
 static int inverse_cdf(const double* r, int V, double u2, double* total_out,
-                       double* margin) {
+                       double* margin, double edges[2]) {
     double total = 0.0;
     for (int v = 0; v < V; ++v) total += r[v];
     double t = u2 * total;
@@ -185,12 +186,15 @@ static int inverse_cdf(const double* r, int V, double u2, double* total_out,
         if (cum > t) {
             double d0 = t - prev, d1 = cum - t;
             *margin = d0 < d1 ? d0 : d1;
+            edges[0] = d0;
+            edges[1] = d1;
             *total_out = total;
             return v;
         }
     }
     /* Only reachable through rounding: take the last token with mass. */
     *margin = 0.0;
+    edges[0] = edges[1] = 0.0;
     *total_out = total;
     return last_positive;
 }
@@ -199,6 +203,7 @@ static int inverse_cdf(const double* r, int V, double u2, double* total_out,
 typedef struct {
     double accept_margin; /* min over tested positions of |u*P_d - P_t| / P_d */
     double draw_margin;   /* distance of t to the chosen interval's edges     */
+    double draw_edges[2]; /* t's distances to the lower and the upper edge    */
     double residual_mass; /* sum of the distribution the final draw used      */
     int fallback;         /* 1 when a zero residual fell back to P_t          */
 } seq_extra;
@@ -216,6 +221,7 @@ static int verify_sequence(const void* tgt, size_t tgt_off, const void* drf,
                            double* Pt, double* Pd, double* r) {
     ex->accept_margin = INFINITY;
     ex->draw_margin = INFINITY;
+    ex->draw_edges[0] = ex->draw_edges[1] = NAN;
     ex->residual_mass = NAN;
     ex->fallback = 0;
     for (int i = 0; i <= K; ++i) tokens[i] = -1;
@@ -281,11 +287,11 @@ static int verify_sequence(const void* tgt, size_t tgt_off, const void* drf,
             ex->fallback = 1;
             for (int v = 0; v < V; ++v) r[v] = Pt[v];
         }
-        token = inverse_cdf(r, V, u2[j], &total, &margin);
+        token = inverse_cdf(r, V, u2[j], &total, &margin, ex->draw_edges);
     } else {
         /* All K accepted: the bonus token comes from P_t of row K. */
         row_softmax(tgt, dtype_t, tgt_off + (size_t)K * V, V, T, Pt);
-        token = inverse_cdf(Pt, V, u2[K], &total, &margin);
+        token = inverse_cdf(Pt, V, u2[K], &total, &margin, ex->draw_edges);
     }
     ex->draw_margin = margin;
     ex->residual_mass = total;
@@ -302,7 +308,9 @@ static int verify_sequence(const void* tgt, size_t tgt_off, const void* drf,
  *   ids seq_ids [B] (NULL means id = b).
  *   Outputs: out_tokens [B, K+1], out_n_accepted [B]; optional (NULL to
  *   skip): out_p_target / out_p_draft [B, K], out_residual_mass [B],
- *   out_accept_margin [B], out_draw_margin [B], out_fallback [B].
+ *   out_accept_margin [B], out_draw_margin [B], out_fallback [B],
+ *   out_draw_edges [B, 2] (t's distances to the chosen interval's lower and
+ *   upper edges; NaN for greedy or invalid sequences).
  * Returns 0, or -1 if a work buffer could not be allocated. */
 int oracle_verify(const void* target, const void* draft,
                   const int32_t* draft_tokens, int B, int K, int V,
@@ -313,7 +321,7 @@ int oracle_verify(const void* target, const void* draft,
                   double* out_p_target, double* out_p_draft,
                   double* out_residual_mass, double* out_accept_margin,
                   double* out_draw_margin, int32_t* out_fallback,
-                  const int32_t* draft_lens) {
+                  const int32_t* draft_lens, double* out_draw_edges) {
     double* Pt = (double*)malloc(sizeof(double) * (size_t)V);
     double* Pd = (double*)malloc(sizeof(double) * (size_t)V);
     double* r = (double*)malloc(sizeof(double) * (size_t)V);
@@ -350,6 +358,7 @@ int oracle_verify(const void* target, const void* draft,
             j = -1;
             ex.accept_margin = INFINITY;
             ex.draw_margin = INFINITY;
+            ex.draw_edges[0] = ex.draw_edges[1] = NAN;
             ex.residual_mass = NAN;
             ex.fallback = 0;
         } else {
@@ -364,6 +373,10 @@ int oracle_verify(const void* target, const void* draft,
         if (out_accept_margin) out_accept_margin[b] = ex.accept_margin;
         if (out_draw_margin) out_draw_margin[b] = ex.draw_margin;
         if (out_fallback) out_fallback[b] = ex.fallback;
+        if (out_draw_edges) {
+            out_draw_edges[2 * (size_t)b] = ex.draw_edges[0];
+            out_draw_edges[2 * (size_t)b + 1] = ex.draw_edges[1];
+        }
     }
     free(Pt); free(Pd); free(r); free(u); free(u2);
     return 0;

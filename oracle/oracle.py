@@ -48,7 +48,7 @@ def _bind(path: str):
     lib.oracle_verify.argtypes = [
         P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_double, P, ctypes.c_uint64, P, P, ctypes.c_int, ctypes.c_int,
-        P, P, P, P, P, P, P, P, P]
+        P, P, P, P, P, P, P, P, P, P]
     lib.oracle_verify_tree.restype = ctypes.c_int
     lib.oracle_verify_tree.argtypes = [P, ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, P, P, P]
@@ -147,6 +147,7 @@ def verify(target, draft, draft_tokens, temperature=1.0, modes=SAMPLE, seed=0, s
         "residual_mass": np.full(B, np.nan),
         "accept_margin": np.full(B, np.inf),
         "draw_margin": np.full(B, np.inf),
+        "draw_edges": np.full((B, 2), np.nan),
         "fallback": np.zeros(B, dtype=np.int32),
     }
     b0, b1 = (0, B) if seq_range is None else seq_range
@@ -157,7 +158,7 @@ def verify(target, draft, draft_tokens, temperature=1.0, modes=SAMPLE, seed=0, s
             float(temperature), _ptr(modes_arr), ctypes.c_uint64(seed), _ptr(ids), _ptr(uni),
             lo, hi, _ptr(out["tokens"]), _ptr(out["n_accepted"]), _ptr(out["p_target"]),
             _ptr(out["p_draft"]), _ptr(out["residual_mass"]), _ptr(out["accept_margin"]),
-            _ptr(out["draw_margin"]), _ptr(out["fallback"]), _ptr(lens))
+            _ptr(out["draw_margin"]), _ptr(out["fallback"]), _ptr(lens), _ptr(out["draw_edges"]))
         if rc != 0:
             raise MemoryError("oracle_verify could not allocate its work buffers")
 
