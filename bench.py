@@ -153,9 +153,14 @@ class ClockSampler:
 # ----------------------------------------------------------------- workloads
 
 
-def workload_sets(name: str, device, l2_bytes: int):
-    """Seeded input sets for a workload, enough that they exceed 2 x L2."""
-    import synth
+BASE_SEED = {"c1": 0, "c2": 2, "c3": 3, "c4": 4}
+RANK_SEED_STRIDE = 1000  # rank r's sets are seeded base + k + 1000 r: its own shard's data
+
+
+def n_input_sets(name: str, l2_bytes: int) -> tuple:
+    """How many seeded input sets a workload rotates over (together more
+    than twice the L2, so that every step reads its logits from HBM), and the
+    bytes of one set."""
     from synth.workloads import WORKLOADS
 
     w = WORKLOADS[name]
@@ -163,15 +168,30 @@ def workload_sets(name: str, device, l2_bytes: int):
     B, K, V = w["B"], w["K"], w["V"]
     set_bytes = B * (2 * K + 1) * V * esize
     n_sets = max(2, math.ceil(2 * l2_bytes / set_bytes))
-    taus = list(w["tau"]) if name == "c2" else [None]
+    if name == "c2":  # the sets cycle over the three draft-noise levels
+        n_sets = int(math.ceil(n_sets / len(w["tau"])) * len(w["tau"]))
+    return n_sets, set_bytes
+
+
+def make_input_set(name: str, k: int, device, rank: int = 0):
+    """Input set k of a workload on `device` (the same generator and seed
+    whatever the arm, so both arms read identical logits)."""
+    import synth
+    from synth.workloads import WORKLOADS
+
+    tau = None
     if name == "c2":
-        n_sets = int(math.ceil(n_sets / len(taus)) * len(taus))
-    sets = []
-    for k in range(n_sets):
+        taus = list(WORKLOADS["c2"]["tau"])
         tau = taus[k % len(taus)]
-        sets.append(synth.make_workload(name, seed={"c1": 0, "c2": 2, "c3": 3, "c4": 4}[name] + k,
-                                        device=device, tau=tau))
-    return sets, set_bytes
+    return synth.make_workload(name, seed=BASE_SEED[name] + k + RANK_SEED_STRIDE * rank,
+                               device=device, tau=tau)
+
+
+def workload_sets(name: str, device, l2_bytes: int, rank: int = 0):
+    """Seeded input sets for a workload, enough that they exceed 2 x L2.
+    Each rank gets its own sets (its shard of the global batch)."""
+    n_sets, set_bytes = n_input_sets(name, l2_bytes)
+    return [make_input_set(name, k, device, rank) for k in range(n_sets)], set_bytes
 
 
 def acceptance(name: str, n_all: np.ndarray, first: int, count: int, n_sets: int, K: int) -> dict:
@@ -250,6 +270,37 @@ def max_over_ranks(x: float, device, world: int) -> float:
     return float(t.item())
 
 
+def sum_over_ranks(x: float, device, world: int) -> float:
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def job_rates(rows: float, nbytes: float, ms: float, device, world: int) -> dict:
+    """Whole-job rates of one timed region: the rows and algorithmic bytes of
+    every rank over the slowest rank's time (each rank's own bytes depend on
+    its own accept counts, so they are summed, not multiplied by N)."""
+    ms_max = max_over_ranks(ms, device, world)
+    rows_all = sum_over_ranks(rows, device, world)
+    bytes_all = sum_over_ranks(nbytes, device, world)
+    return {"ms_max": ms_max, "rows_per_s": rows_all / (ms_max / 1e3),
+            "gbs": bytes_all / (ms_max / 1e3) / 1e9, "rows": rows_all, "bytes": bytes_all}
+
+
+def bench_config(name: str, B: int, K: int, V: int, n_sets: int, set_bytes: int, l2: int,
+                 world: int) -> dict:
+    """The workload description both arms print (identical by construction)."""
+    return {
+        "workload": f"{name}: {describe(name)}",
+        "B": B, "K": K, "V": V, "rows_per_step": B * (K + 1),
+        "l2": f"inputs rotate over {n_sets} seeded sets "
+              f"({n_sets * set_bytes / 2**20:.0f} MiB > 2 x L2 of {l2 / 2**20:.0f} MiB)",
+        "parallelism": f"dp x{world}: each rank verifies its own shard of sequences "
+                       "(global Philox ids), no collective on the data path",
+    }
+
+
 # ----------------------------------------------------------------- our arm
 
 
@@ -265,6 +316,9 @@ def uniform_mode(modes: torch.Tensor):
 
 
 def time_device(sets, steps, warmup, stream, seed0=0, rank=0, overlap=True):
+    """Warm-up calls of a workload, and the step function that the timed graph
+    captures. Step i verifies input set i % len(sets) with seed seed0 + i and
+    writes its own rows of out_tok / out_n (kept for the parity check)."""
     from speculative_decoding_verification_24_gb300 import spec_verify_ex
 
     B, K1, _ = sets[0].target.shape
@@ -285,7 +339,7 @@ def time_device(sets, steps, warmup, stream, seed0=0, rank=0, overlap=True):
         for i in range(warmup):
             step(i)
     torch.cuda.synchronize()
-    return step, out_n
+    return step, out_tok, out_n
 
 
 def capture(step, first, count, stream):
@@ -298,35 +352,69 @@ def capture(step, first, count, stream):
     return g
 
 
-def replay_ms(graph, stream):
+def replay_ms(graph, stream, label=None):
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    if label:
+        torch.cuda.nvtx.range_push(label)
     with torch.cuda.stream(stream):
         start.record(stream)
         graph.replay()
         stop.record(stream)
     torch.cuda.synchronize()
+    if label:
+        torch.cuda.nvtx.range_pop()
     return start.elapsed_time(stop)
 
 
+# Timed steps of each sub-result: fixed, whatever --steps the headline runs
+# (a sub-result's figure must not move with the headline's step count).
+SUB_STEPS = {"c2": 200, "c3": 200, "c4": 100, "c5": 50, "ragged": 100, "tree": 100, "lookup": 200,
+             "commit": 200}
+
+HOW_OVERLAPPED = ("independent batches back to back: one CUDA graph of the steps, each launched "
+                  "with SV_ARG_OVERLAP_PREVIOUS (programmatic dependent launch: a step streams its "
+                  "inputs while the previous step finishes and writes its outputs after that step "
+                  "has completed); CUDA events on the launching stream around the replay")
+HOW_SERIAL = ("one call at a time, as a decode loop whose next verify depends on this one's "
+              "tokens: the same graph of steps launched without SV_ARG_OVERLAP_PREVIOUS, so "
+              "each call starts after the previous one has completed")
+
+
+def logits_timing(sets, steps, warmup, stream, device, world, rank, label):
+    """Both timings of a logits workload over the same steps and seeds:
+    overlapped (independent batches back to back) and serial (one call at a
+    time). Returns the two times, the outputs of the overlapped run and
+    whether the serial run emitted the same tokens (it must: same inputs,
+    same seeds)."""
+    step, out_tok, out_n = time_device(sets, steps, warmup, stream, rank=rank)
+    graph = capture(step, warmup, steps, stream)
+    replay_ms(graph, stream)  # warm replay: same launches, same inputs
+    res = {"step": step, "graph": graph, "out_tok": out_tok, "out_n": out_n}
+    res["ms"] = replay_ms(graph, stream, f"{label} overlapped x{steps}")
+    s_step, s_tok, s_n = time_device(sets, steps, warmup, stream, rank=rank, overlap=False)
+    s_graph = capture(s_step, warmup, steps, stream)
+    replay_ms(s_graph, stream)
+    res["serial_ms"] = replay_ms(s_graph, stream, f"{label} serial x{steps}")
+    del s_graph
+    sl = slice(warmup, warmup + steps)
+    res["serial_identical"] = bool(torch.equal(out_tok[sl], s_tok[sl]) and torch.equal(out_n[sl], s_n[sl]))
+    return res
+
+
 def run_ours(args, rank, world, device):
-    from speculative_decoding_verification_24_gb300 import spec_verify_ex
     from speculative_decoding_verification_24_gb300.build import build
 
     build()
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
-    sets, set_bytes = workload_sets(args.workload, device, l2)
+    sets, set_bytes = workload_sets(args.workload, device, l2, rank)
     case0 = sets[0]
     B, K1, V = case0.target.shape
     rows_per_step = B * K1
     stream = torch.cuda.Stream(device)
-    step, out_n = time_device(sets, args.steps, args.warmup, stream, rank=rank)
-
-    # The timed steps replay from one CUDA graph (launch overhead of the
-    # Python binding off the device timeline); the eager number is reported too.
-    graph = capture(step, args.warmup, args.steps, stream)
-    replay_ms(graph, stream)  # warm replay: same launches, same inputs
+    t = logits_timing(sets, args.steps, args.warmup, stream, device, world, rank, args.workload)
+    graph = t["graph"]
 
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
@@ -339,12 +427,13 @@ def run_ours(args, rank, world, device):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.mark()
-    ms = replay_ms(graph, stream)
+    ms = replay_ms(graph, stream, f"timed: {args.workload} x{args.steps}")
     sampler.mark()
     if world > 1:
         torch.distributed.barrier()
     time.sleep(0.25)
     clocks = sampler.stop()
+    del graph, t["graph"]
 
     # eager launches from Python, for comparison (not the headline)
     e_start = torch.cuda.Event(enable_timing=True)
@@ -353,33 +442,27 @@ def run_ours(args, rank, world, device):
     e_start.record(stream)
     with torch.cuda.stream(stream):
         for i in range(args.warmup, args.warmup + args.steps):
-            step(i)
+            t["step"](i)
     e_stop.record(stream)
     torch.cuda.synchronize()
-    eager_ms = e_start.elapsed_time(e_stop)
-
-    # the same steps with no overlap between calls (each waits for the last)
-    serial_step, _ = time_device(sets, args.steps, args.warmup, stream, rank=rank, overlap=False)
-    serial_graph = capture(serial_step, args.warmup, args.steps, stream)
-    replay_ms(serial_graph, stream)
-    serial_ms = max_over_ranks(replay_ms(serial_graph, stream), device, world)
-    del serial_graph
+    eager_ms = max_over_ranks(e_start.elapsed_time(e_stop), device, world)
 
     # exact algorithmic bytes of every timed step, from its own outputs
-    n_all = out_n.cpu().numpy()
-    bytes_alg = sum(alg_bytes(sets[i % len(sets)], n_all[i])
-                    for i in range(args.warmup, args.warmup + args.steps))
-    bytes_min = sum(min_bytes(sets[i % len(sets)])
-                    for i in range(args.warmup, args.warmup + args.steps))
-    ms_max = max_over_ranks(ms, device, world)
-    value = world * rows_per_step * args.steps / (ms_max / 1e3)
-    gbs = bytes_alg / (ms / 1e3) / 1e9
+    n_all = t["out_n"].cpu().numpy()
+    timed = range(args.warmup, args.warmup + args.steps)
+    bytes_alg = sum(alg_bytes(sets[i % len(sets)], n_all[i]) for i in timed)
+    bytes_min = sum(min_bytes(sets[i % len(sets)]) for i in timed)
+    job = job_rates(rows_per_step * args.steps, bytes_alg, ms, device, world)
+    serial = job_rates(rows_per_step * args.steps, bytes_alg, t["serial_ms"], device, world)
+    ms_max = job["ms_max"]
+    gbs = job["gbs"]
     peak, peak_src = measured_peaks()
     traffic, traffic_note = profiled_traffic(args.workload)
+    cfg = bench_config(args.workload, B, K1 - 1, V, len(sets), set_bytes, l2, world)
 
     result = {
         "metric": "verify rows/s",
-        "value": value,
+        "value": job["rows_per_s"],
         "unit": "rows/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -388,27 +471,21 @@ def run_ours(args, rank, world, device):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32" if case0.target.dtype == torch.float32 else "bf16 in, f32 arithmetic",
+        "dtype": "f32",
+        "input_dtype": "f32" if case0.target.dtype == torch.float32 else "bf16",
         "data": "synthetic (seeded generators in synth/; no dataset or weights)",
-        "config": {
-            "workload": f"{args.workload}: {describe(args.workload)}",
-            "B": B, "K": K1 - 1, "V": V, "rows_per_step": rows_per_step,
-            "l2": f"inputs rotate over {len(sets)} seeded sets "
-                  f"({len(sets) * set_bytes / 2**20:.0f} MiB > 2 x L2 of {l2 / 2**20:.0f} MiB)",
-            "parallelism": f"dp x{world}: each rank verifies its own shard of sequences "
-                           "(global Philox ids), no collective on the data path",
-        },
+        "config": cfg,
         "hbm_gbs": gbs,
-        "hbm_bytes_per_step": bytes_alg / args.steps,
+        "hbm_bytes_per_step": job["bytes"] / args.steps / world,
         "roofline": {
             "bound": "hbm",
             "kernel": "sv::verify_logits_kernel",
-            "achieved": gbs,
+            "achieved": gbs / world,
             "peak": peak,
             "unit": "GB/s",
-            "frac": gbs / peak,
+            "frac": gbs / world / peak,
             "peak_source": peak_src,
-            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
+            "frac_of_nominal_8tbs": gbs / world / NOMINAL_HBM_GBS,
             "traffic": None if traffic is None else traffic,
             "traffic_note": traffic_note,
             "algorithmic_bytes_per_launch": bytes_alg / args.steps,
@@ -417,27 +494,29 @@ def run_ours(args, rank, world, device):
         },
         "gpu_launches": args.steps,
         "clocks": clocks,
-        "timing": "one CUDA graph of the K steps, replayed between CUDA events on the "
-                  "launching stream; each step is launched with SV_ARG_OVERLAP_PREVIOUS "
-                  "(programmatic dependent launch: a step may stream its inputs while the "
-                  "previous step finishes; it writes its outputs after that step completes)",
+        "timing": "value: " + HOW_OVERLAPPED,
+        "serial": {"ms_per_step": serial["ms_max"] / args.steps,
+                   "rows_per_s": serial["rows_per_s"],
+                   "hbm_gbs": serial["gbs"],
+                   "frac_of_measured_peak": serial["gbs"] / world / peak,
+                   "frac_of_nominal_8tbs": serial["gbs"] / world / NOMINAL_HBM_GBS,
+                   "outputs_identical_to_overlapped": t["serial_identical"],
+                   "how": HOW_SERIAL},
         "eager_rows_per_s": world * rows_per_step * args.steps / (eager_ms / 1e3),
-        "serial": {"ms_per_step": serial_ms / args.steps,
-                   "rows_per_s": world * rows_per_step * args.steps / (serial_ms / 1e3),
-                   "hbm_gbs": bytes_alg / (serial_ms / 1e3) / 1e9,
-                   "how": "the same graph of K steps launched without SV_ARG_OVERLAP_PREVIOUS: "
-                          "each call starts after the previous one has completed"},
     }
     result["acceptance"] = acceptance(args.workload, n_all, args.warmup, args.steps, len(sets), K1 - 1)
-    result["e2e"] = run_e2e(args, sets, device, stream, world)
+    result["e2e"] = run_e2e(args, sets, device, stream, world, rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(sets, args.cpu_seconds)
+        base, check = oracle_leg(sets, t["out_tok"], t["out_n"], args.warmup, args.steps,
+                                 args.cpu_seconds, rank)
+        result["cpu_baseline"] = base
+        result["parity"] = check
     if rank == 0 and not args.no_extra and world == 1:
         result["other_workloads"] = other_workloads(args, device, l2, stream)
     return result
 
 
-def run_e2e(args, sets, device, stream, world):
+def run_e2e(args, sets, device, stream, world, rank=0):
     """Same metric through the public API with host buffers. Every step copies
     its inputs from pinned host memory into one of two device buffers (on a
     copy stream, so that step i+1's copy overlaps step i's verify), verifies
@@ -447,6 +526,7 @@ def run_e2e(args, sets, device, stream, world):
     from speculative_decoding_verification_24_gb300 import spec_verify_ex
 
     n_host = min(len(sets), 4)
+    seq_ids = shard_seq_ids(rank, sets[0].target.shape[0], device)
     host = []
     for c in sets[:n_host]:
         host.append(tuple(t.cpu().pin_memory() for t in (c.target, c.draft, c.tokens, c.modes)))
@@ -466,7 +546,7 @@ def run_e2e(args, sets, device, stream, world):
     def verify(i, k, on):
         dt, dd, dx, dm = bufs[k]
         spec_verify_ex(dt, dd, dx, c0.temperature, modes=dm if isinstance(mode0, torch.Tensor) else mode0,
-                       seed=i, out_tokens=outs[k][0], out_n_accepted=outs[k][1], stream=on)
+                       seed=i, seq_ids=seq_ids, out_tokens=outs[k][0], out_n_accepted=outs[k][1], stream=on)
         res[k][0].copy_(outs[k][0], non_blocking=True)
         res[k][1].copy_(outs[k][1], non_blocking=True)
 
@@ -518,7 +598,7 @@ def run_e2e(args, sets, device, stream, world):
         pipelined(args.warmup, args.steps)
     torch.cuda.synchronize()
     ms = replay_ms(g, stream)  # the first replay loads the graph
-    ms = max_over_ranks(replay_ms(g, stream), device, world)
+    ms = max_over_ranks(replay_ms(g, stream, "timed: e2e"), device, world)
     value = world * B * K1 * args.steps / (ms / 1e3)
     return {"value": value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
@@ -531,35 +611,80 @@ def run_e2e(args, sets, device, stream, world):
                    "i+1's copy overlaps step i's verify); CUDA events around the replay"}
 
 
-def cpu_baseline(sets, seconds):
-    """The oracle as it stands on the host cores, over a bounded sample."""
+def oracle_leg(sets, out_tok, out_n, first, count, seconds, rank=0, target_of=None):
+    """The cpu_baseline leg: the oracle as it stands, timed on the host cores
+    (threads over sequences) on the timed steps of the GPU run, in order and
+    with the same seeds and sequence ids, until about `seconds` of oracle
+    time; then its outputs for those steps compared with the GPU's.
+
+    Returns (cpu_baseline, parity). parity counts the sequences checked, the
+    exact matches and the near-ties, split into accept-test ties and draw
+    ties (bands in oracle/parity.py), and must show no mismatch outside them.
+    target_of(i) optionally gives step i's target rows (the LM-head path
+    verifies the GPU's own fp32 logits)."""
     from oracle import oracle as orc
+    from oracle import parity as par
     from synth.workloads import to_numpy_logits
 
     cores = os.cpu_count() or 1
-    rows = 0
-    used = 1
-    host = [(to_numpy_logits(c.target), to_numpy_logits(c.draft), c.tokens.cpu().numpy(),
-             c.modes.cpu().numpy(), c.temperature) for c in sets[:8]]
-    calls = 0
+    host = {}
+    tok_all = out_tok.cpu().numpy()
+    n_all = out_n.cpu().numpy()
+    rows = calls = used = 0
     el = 0.0
-    while el < seconds:  # cycle over the input sets until the sample is long enough
-        tgt, drf, tok, modes, T = host[calls % len(host)]
+    tot = {"steps_checked": 0, "sequences": 0, "exact": 0, "accept_near_ties": 0, "draw_near_ties": 0,
+           "near_tie_mismatches": 0, "mismatches": 0}
+    first_bad = []
+    for t in range(count):
+        if el >= seconds:
+            break
+        i = first + t
+        k = i % len(sets)
+        c = sets[k]
+        if k not in host:
+            host[k] = (to_numpy_logits(c.draft), c.tokens.cpu().numpy(), c.modes.cpu().numpy())
+        drf, tok, modes = host[k]
+        tgt = to_numpy_logits(c.target) if target_of is None else target_of(i)
         B, K1, _ = tgt.shape
         threads = min(cores, B)
         used = max(used, threads)
+        ids = shard_seq_ids(rank, B, "cpu").numpy().astype(np.uint64)
         t1 = time.perf_counter()
-        orc.verify(tgt, drf, tok, T, modes, seed=calls, threads=threads)
+        ref = orc.verify(tgt, drf, tok, c.temperature, modes, seed=i, seq_ids=ids, threads=threads)
         el += time.perf_counter() - t1
         rows += B * K1
         calls += 1
-    return {"value": rows / el, "unit": "rows/s", "cores": used, "kind": "oracle",
-            "sample": f"{calls} verify calls of the workload's batches ({rows} rows), "
-                      f"{el:.1f} s of oracle time, threads over sequences"}
+        acc_tie = ref["accept_margin"] < par.ACCEPT_TIE_REL
+        draw_tie = ~acc_tie & par.near_ties(ref)
+        cmp = par.compare(tok_all[i], n_all[i], ref, ties=acc_tie | draw_tie)
+        tot["steps_checked"] += 1
+        tot["sequences"] += cmp["sequences"]
+        tot["accept_near_ties"] += int(acc_tie.sum())
+        tot["draw_near_ties"] += int(draw_tie.sum())
+        tot["near_tie_mismatches"] += cmp["near_tie_mismatches"]
+        tot["mismatches"] += cmp["mismatches"]
+        tot["exact"] += cmp["sequences"] - cmp["near_tie_mismatches"] - cmp["mismatches"]
+        first_bad += [dict(step=i, **m) for m in cmp["first_mismatches"]][:3 - len(first_bad)]
+    base = {"value": rows / el if el > 0 else None, "unit": "rows/s", "cores": used, "kind": "oracle",
+            "sample": f"the first {calls} timed steps ({rows} rows), same inputs, seeds and sequence "
+                      f"ids as the GPU run; {el:.1f} s of oracle time, threads over sequences"}
+    tot["near_tie_fraction"] = (tot["accept_near_ties"] + tot["draw_near_ties"]) / max(1, tot["sequences"])
+    tot["bands"] = {"accept": f"|u*P_d(x) - P_t(x)| < {par.ACCEPT_TIE_REL:g} * P_d(x)",
+                    "draw": f"t within {par.DRAW_TIE_ABS:g} of an edge of the chosen token's "
+                            "cumulative interval (probability units)"}
+    tot["how"] = ("the oracle (double precision, own Philox) on the GPU's timed steps; tokens and "
+                  "accept counts compared exactly outside the near-tie bands")
+    if first_bad:
+        tot["first_mismatches"] = first_bad
+    return base, tot
+
+
+SUB_ORACLE_SECONDS = 3.0  # oracle time per sub-result's parity check
 
 
 def other_workloads(args, device, l2, stream):
-    """The other logits workloads measured the same way (sub-results)."""
+    """The other workloads, each measured the same way over its own fixed
+    number of steps (SUB_STEPS), with the oracle's check of its outputs."""
     out = {}
     for name in args.also:
         if name == args.workload:
@@ -569,6 +694,7 @@ def other_workloads(args, device, l2, stream):
                 out[name] = lmhead_workload(args, device, stream)
             except Exception as e:  # report, do not hide
                 out[name] = {"error": repr(e)}
+            torch.cuda.empty_cache()
             continue
         if name in NEXT_ROW_NAMES:
             try:
@@ -579,18 +705,11 @@ def other_workloads(args, device, l2, stream):
             continue
         try:
             sets, set_bytes = workload_sets(name, device, l2)
-            steps = max(20, min(args.steps, 200))
-            step, out_n = time_device(sets, steps, args.warmup, stream)
-            graph = capture(step, args.warmup, steps, stream)
-            replay_ms(graph, stream)
-            ms = replay_ms(graph, stream)
-            del graph
-            serial_step, _ = time_device(sets, steps, args.warmup, stream, overlap=False)
-            graph = capture(serial_step, args.warmup, steps, stream)
-            replay_ms(graph, stream)
-            serial_ms = replay_ms(graph, stream)
-            del graph
-            n_all = out_n.cpu().numpy()
+            steps = SUB_STEPS[name]
+            t = logits_timing(sets, steps, args.warmup, stream, device, 1, 0, name)
+            del t["graph"]
+            ms, serial_ms = t["ms"], t["serial_ms"]
+            n_all = t["out_n"].cpu().numpy()
             ba = sum(alg_bytes(sets[i % len(sets)], n_all[i])
                      for i in range(args.warmup, args.warmup + steps))
             B, K1, V = sets[0].target.shape
@@ -603,10 +722,19 @@ def other_workloads(args, device, l2, stream):
                          "rows_per_s": B * K1 * steps / (ms / 1e3), "us_per_step": ms * 1e3 / steps,
                          "hbm_gbs": gbs, "frac_of_measured_peak": gbs / peak,
                          "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
-                         "serial_us_per_step": serial_ms * 1e3 / steps,
-                         "serial_frac_of_measured_peak": ba / (serial_ms / 1e3) / 1e9 / peak,
+                         "how": HOW_OVERLAPPED,
+                         "serial": {"us_per_step": serial_ms * 1e3 / steps,
+                                    "rows_per_s": B * K1 * steps / (serial_ms / 1e3),
+                                    "frac_of_measured_peak": ba / (serial_ms / 1e3) / 1e9 / peak,
+                                    "frac_of_nominal_8tbs": ba / (serial_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                                    "outputs_identical_to_overlapped": t["serial_identical"],
+                                    "how": HOW_SERIAL},
+                         "acceptance": acceptance(name, n_all, args.warmup, steps, len(sets), K1 - 1),
                          "input_sets": len(sets)}
-            del sets
+            if not args.no_cpu_baseline:
+                out[name]["cpu_baseline"], out[name]["parity"] = oracle_leg(
+                    sets, t["out_tok"], t["out_n"], args.warmup, steps, SUB_ORACLE_SECONDS)
+            del sets, t
             torch.cuda.empty_cache()
         except Exception as e:  # report, do not hide
             out[name] = {"error": repr(e)}
@@ -639,7 +767,7 @@ def next_row_workload(name, args, device, l2, stream):
                                                             spec_verify_ex, spec_verify_tree)
 
     cfg = synth.NEXT_ROWS[name]
-    steps = max(20, min(args.steps, 200))
+    steps = SUB_STEPS[name]
     peak, _ = measured_peaks()
 
     def hbm(nbytes, ms):
@@ -780,7 +908,7 @@ def lmhead_workload(args, device, stream, n_sets=4):
     B, K1, d = base.hidden.shape
     K, V = K1 - 1, W.shape[1]
     M = B * K1
-    steps = max(20, min(args.steps, 100))
+    steps = SUB_STEPS["c5"]
     ws = torch.empty(spec_verify_lmhead_workspace_bytes(B, K, d, V), dtype=torch.uint8, device=device)
     out_t = torch.empty(steps + args.warmup, B, K1, dtype=torch.int32, device=device)
     out_n = torch.empty(steps + args.warmup, B, dtype=torch.int32, device=device)
@@ -846,6 +974,16 @@ def lmhead_workload(args, device, stream, n_sets=4):
                    "note": "M = B*(K+1) = 192 rows make the product HBM-bound by design"},
         "gpu_launches_per_step": 2,
     })
+    if not args.no_cpu_baseline:
+        # the last timed step, checked against the oracle run on the GPU's
+        # own fp32 logits (still in the workspace) and the same draft rows
+        last = args.warmup + steps - 1
+        gpu_logits = ws[:M * V * 4].view(torch.float32).reshape(B, K1, V)
+        res["cpu_baseline"], res["parity"] = oracle_leg(
+            sets, out_t, out_n, last, 1, SUB_ORACLE_SECONDS, target_of=lambda i: gpu_logits.cpu().numpy())
+        res["parity"]["how"] = ("the oracle on the last timed step's fp32 logits as the GEMM wrote "
+                                "them (the workspace) and the same bf16 draft rows; tokens and accept "
+                                "counts compared exactly outside the near-tie bands")
     del sets, ws, logits
     torch.cuda.empty_cache()
     return res
@@ -855,47 +993,67 @@ def lmhead_workload(args, device, stream, n_sets=4):
 
 
 def run_reference(args):
-    """The oracle, as it stands, timed on the host cores on this workload."""
-    import synth
+    """The reference arm: the oracle, as it stands, timed on the host cores on
+    this workload. It reads the same input sets as the GPU arm (same
+    generator, seeds and device), cycles over them step by step with the same
+    seeds, and verifies a bounded sample of each batch (its first n_seq
+    sequences) so that the whole run stays within a few minutes."""
     from oracle import oracle as orc
     from synth.workloads import to_numpy_logits
 
     orc.build()
-    c = synth.make_workload(args.workload, seed=2, device="cpu", tau=1.0 if args.workload == "c2" else None)
-    tgt, drf = to_numpy_logits(c.target), to_numpy_logits(c.draft)
-    tok, modes = c.tokens.numpy(), c.modes.numpy()
-    B, K1, V = c.target.shape
+    gen_dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    l2 = 129 * 2**20
+    if gen_dev.type == "cuda":
+        l2 = int(getattr(torch.cuda.get_device_properties(gen_dev), "L2_cache_size", 0) or l2)
+    n_sets, set_bytes = n_input_sets(args.workload, l2)
+    host = []
+    for k in range(n_sets):
+        c = make_input_set(args.workload, k, gen_dev)
+        host.append((to_numpy_logits(c.target), to_numpy_logits(c.draft), c.tokens.cpu().numpy(),
+                     c.modes.cpu().numpy(), c.temperature))
+        del c
+    if gen_dev.type == "cuda":
+        torch.cuda.empty_cache()
+    B, K1, V = host[0][0].shape
     cores = os.cpu_count() or 1
     threads = min(cores, B)
-    # each step verifies a bounded sample of the batch so the run stays short
-    budget_s = 0.2
+    ids = np.arange(B, dtype=np.uint64)
+
+    def call(i, n_seq):
+        tgt, drf, tok, modes, T = host[i % n_sets]
+        orc.verify(tgt, drf, tok, T, modes, seed=i, seq_ids=ids, threads=min(threads, n_seq),
+                   seq_range=(0, n_seq))
+
+    # size the per-step sample from one timed call of a few sequences
+    budget_s = 1.0
+    probe = min(B, threads)
     t0 = time.perf_counter()
-    orc.verify(tgt, drf, tok, c.temperature, modes, seed=0, threads=threads)
-    one = time.perf_counter() - t0
-    n_seq = B if one <= budget_s else max(1, int(B * budget_s / one))
-    rng = (0, n_seq)
+    call(0, probe)
+    per_seq = (time.perf_counter() - t0) / probe * min(threads, B)
+    n_seq = B if per_seq * B / threads <= budget_s else max(1, int(budget_s * threads / per_seq))
+    n_seq = min(B, max(n_seq, 1))
     for i in range(args.warmup):
-        orc.verify(tgt, drf, tok, c.temperature, modes, seed=i, threads=threads, seq_range=rng)
+        call(i, n_seq)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        orc.verify(tgt, drf, tok, c.temperature, modes, seed=i, threads=min(threads, n_seq),
-                   seq_range=rng)
+    for i in range(args.warmup, args.warmup + args.steps):
+        call(i, n_seq)
     el = time.perf_counter() - t0
     value = n_seq * K1 * args.steps / el
-    sample = f"{n_seq} of {B} sequences per step ({n_seq * K1} rows), {args.steps} steps"
+    sample = (f"the first {n_seq} of {B} sequences of each step's batch ({n_seq * K1} rows), "
+              f"{args.steps} steps over the same input sets and seeds as the GPU arm")
     return {
         "impl": "reference", "metric": "verify rows/s", "value": value, "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators in synth/)",
-        "config": {"workload": f"{args.workload}: {describe(args.workload)}", "B": B,
-                   "K": K1 - 1, "V": V},
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators in synth/; no dataset or weights)",
+        "config": bench_config(args.workload, B, K1 - 1, V, n_sets, set_bytes, l2, args.gpus),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": min(threads, n_seq),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "note": "the reference arm is the plain C double-precision oracle (the pages print no "
-                "implementation of the verify step to install)",
+                "implementation of the verify step to install); under torchrun rank 0 alone runs it",
     }
 
 
@@ -936,11 +1094,11 @@ def profile_run(args, device):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c2", choices=["c1", "c2", "c3", "c4"])
-    ap.add_argument("--also", default="c3,c4,c5,ragged,tree,lookup,commit",
+    ap.add_argument("--workload", default="c4", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--also", default="c2,c3,c4,c5,ragged,tree,lookup,commit",
                     help="other workloads reported as sub-results")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -151,6 +151,14 @@ typedef struct {
                                     0..Kb and draft rows 0..Kb-1 of its block and
                                     writes -1 / NaN past Kb; a value outside
                                     [0, K] makes the sequence invalid            */
+    float* out_draw_edges;       /* [B, 2] float (device) or NULL: for a sample
+                                    sequence, the distances from the final draw's
+                                    target t = u2 * (total mass) down to the lower
+                                    and up to the upper edge of the chosen token's
+                                    cumulative interval, in probability units, as
+                                    the kernel computed them (0, 0 when rounding
+                                    left t at or past the total); NaN for greedy
+                                    or invalid sequences                          */
 } sv_verify_args;
 
 /* sv_verify_args.flags: the inputs of this call are not written by the work
@@ -289,7 +297,9 @@ sv_status spec_commit(int32_t* tokens, int32_t* lengths, int B, int L_max,
  *   Nothing in the scratch needs to start at zero: the call writes every
  *   byte it reads there before reading it.
  *   Sizes whose workspace would exceed SV_LMHEAD_SCRATCH_BYTES return
- *   SV_ERR_SCRATCH_LIMIT before any work is enqueued.
+ *   SV_ERR_SCRATCH_LIMIT before any work is enqueued. The limit is the
+ *   mode-independent spec_verify_lmhead_workspace_bytes(B, K, d, V), which
+ *   counts room for the draft rows' partials even in greedy mode.
  *   All calls on one device share the one scratch array: calls whose work
  *   may overlap (other streams, other host threads, another call before this
  *   one's work on `stream` has completed unless both are on the same stream)

@@ -10,18 +10,23 @@ Near-tie bands:
                 position (the band the verify step's specification gives);
   final draw    the draw's target t lies within DRAW_TIE_ABS of an edge of the
                 chosen token's cumulative interval, in probability units (the
-                pages' distributions sum to one). The float32 path computes each
-                probability with a relative error of a few 1e-7 (one ex2.approx,
-                one FMA rounding, one multiply by 1/S, plus the error of S);
-                the residual's cumulative sums and u2 * total then move by at
-                most ~4 such errors, so 2e-6 bounds the float32 discrepancy.
+                pages' distributions sum to one). The band is set from a
+                measurement, not a model: the kernel reports its own distances
+                from t to both edges of the token it chose, and over every
+                sample sequence of the GPU parity suite (about 10^4 sequences:
+                c1-c4, all cluster sizes, temperatures 0.05-10, misaligned and
+                ragged rows) they differ from the oracle's by at most
+                2.47e-7. The band is twice that. It is absolute, not relative
+                to the draw's total mass S_r: the error comes from the rows'
+                probabilities (each with its own float32 normaliser), so it
+                does not shrink with the residual's mass.
 """
 from __future__ import annotations
 
 import numpy as np
 
 ACCEPT_TIE_REL = 1e-6
-DRAW_TIE_ABS = 2e-6
+DRAW_TIE_ABS = 5e-7
 PROB_RTOL = 1e-5
 
 

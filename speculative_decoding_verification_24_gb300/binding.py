@@ -74,6 +74,7 @@ class sv_verify_args(ctypes.Structure):
         ("stream", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
         ("draft_lens", ctypes.c_void_p),
+        ("out_draw_edges", ctypes.c_void_p),
     ]
 
 
@@ -196,11 +197,12 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=1.0, mode
 def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, modes="sample",
                    seed=0, seq_ids=None, out_tokens=None, out_n_accepted=None, out_p_target=None,
                    out_p_draft=None, out_residual_mass=None, status_word=None, cluster_size=0,
-                   stream=None, debug=False, overlap_previous=False, draft_lens=None, flags=0):
+                   stream=None, debug=False, overlap_previous=False, draft_lens=None, flags=0,
+                   out_draw_edges=None):
     """Verify with per-sequence modes ([B] int32 tensor, or 'greedy'/'sample'
     for all), explicit Philox sequence ids and optional debug outputs.
-    debug=True allocates out_p_target, out_p_draft, out_residual_mass and
-    status_word. overlap_previous=True sets SV_ARG_OVERLAP_PREVIOUS (the
+    debug=True allocates out_p_target, out_p_draft, out_residual_mass,
+    out_draw_edges and status_word. overlap_previous=True sets SV_ARG_OVERLAP_PREVIOUS (the
     inputs are not written by the work just before this call on the stream).
     draft_lens: optional [B] int32 device tensor of per-sequence draft counts.
     Returns a dict of the output tensors."""
@@ -221,6 +223,8 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
             out_residual_mass = torch.empty(B, dtype=torch.float32, device=dev)
         if status_word is None:
             status_word = torch.zeros(1, dtype=torch.int32, device=dev)
+        if out_draw_edges is None:
+            out_draw_edges = torch.empty(B, 2, dtype=torch.float32, device=dev)
     a.target_logits = _ptr(target_logits)
     a.draft_logits = _ptr(draft_logits)
     a.draft_tokens = _ptr(draft_tokens)
@@ -244,13 +248,14 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     a.cluster_size = int(cluster_size)
     a.flags = (SV_ARG_OVERLAP_PREVIOUS if overlap_previous else 0) | int(flags)
     a.draft_lens = _ptr(draft_lens)
+    a.out_draw_edges = _ptr(out_draw_edges)
     with torch.cuda.device(dev):
         a.stream = _stream(stream, dev)
         st = _load().spec_verify_ex(ctypes.byref(a))
     _check(st, "spec_verify_ex")
     return {"tokens": out_tokens, "n_accepted": out_n_accepted, "p_target": out_p_target,
             "p_draft": out_p_draft, "residual_mass": out_residual_mass,
-            "status_word": status_word}
+            "draw_edges": out_draw_edges, "status_word": status_word}
 
 
 def spec_verify_tree(target_logits, tree_tokens, tree_parents, out_tokens=None, out_n_accepted=None,

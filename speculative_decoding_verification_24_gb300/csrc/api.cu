@@ -88,6 +88,7 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
         (a->out_p_target && !aligned(a->out_p_target, 4)) ||
         (a->out_p_draft && !aligned(a->out_p_draft, 4)) ||
         (a->out_residual_mass && !aligned(a->out_residual_mass, 4)) ||
+        (a->out_draw_edges && !aligned(a->out_draw_edges, 4)) ||
         (a->status_word && !aligned(a->status_word, 4)))
         return SV_ERR_ALIGN;
     if (!valid_cluster_request(a->cluster_size)) return SV_ERR_CONFIG;
@@ -134,6 +135,7 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     p.out_p_target = a->out_p_target;
     p.out_p_draft = a->out_p_draft;
     p.out_residual_mass = a->out_residual_mass;
+    p.out_draw_edges = a->out_draw_edges;
     p.status_word = a->status_word;
     p.overlap_previous = (a->flags & SV_ARG_OVERLAP_PREVIOUS) != 0;
     p.test_wait_timeout = (a->flags & SV_ARG_TEST_WAIT_TIMEOUT) != 0;
@@ -196,7 +198,7 @@ extern "C" const char* sv_status_string(sv_status s) {
 
 extern "C" int sv_last_cuda_error(void) { return g_last_cuda_error; }
 
-extern "C" int sv_version(void) { return 100; }
+extern "C" int sv_version(void) { return 101; }
 
 extern "C" size_t sv_verify_args_size(void) { return sizeof(sv_verify_args); }
 
@@ -386,7 +388,9 @@ static __device__ __align__(256) unsigned char g_lmhead_scratch[SV_LMHEAD_SCRATC
 static std::atomic<void*> g_scratch_addr[kMaxDevices];
 
 // The scratch's device address on the current device, looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached. The first lookup on a device
+// checks its compute capability first, so that a device this library was not
+// built for reports SV_ERR_ARCH instead of failing to load the image.
 static sv_status scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -394,6 +398,9 @@ static sv_status scratch_address(void** out) {
     if (dev < 0 || dev >= kMaxDevices) return SV_ERR_ARCH;
     void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
     if (!p) {
+        int sms = 0;
+        const sv_status st = check_device(&sms);
+        if (st != SV_OK) return st;
         e = cudaGetSymbolAddress(&p, g_lmhead_scratch);
         if (e != cudaSuccess) return fail_cuda(e);
         if (!p) return fail_cuda(cudaErrorInvalidSymbol);
@@ -421,8 +428,6 @@ extern "C" sv_status spec_verify_lmhead_noalloc(const void* hidden, const void* 
     if (st != SV_OK) return st;
     if (!draft_tokens || !out_tokens || !out_n_accepted) return SV_ERR_NULL;
     void* scratch = nullptr;
-    int sms = 0;
-    if ((st = check_device(&sms)) != SV_OK) return st;
     if ((st = scratch_address(&scratch)) != SV_OK) return st;
     return spec_verify_lmhead(hidden, W, draft_logits, draft_tokens, B, K, d, V, draft_dtype,
                               temperature, mode, seed, scratch, (size_t)SV_LMHEAD_SCRATCH_BYTES,

@@ -24,6 +24,7 @@ struct VerifyParams {
     float* out_p_target;       // [B, K] or nullptr
     float* out_p_draft;        // [B, K] or nullptr
     float* out_residual_mass;  // [B] or nullptr
+    float* out_draw_edges;     // [B, 2] or nullptr: the draw target's distances to its interval's edges
     uint32_t* status_word;     // or nullptr
     int overlap_previous;      // inputs not written by the previous work on the stream
     const int32_t* draft_lens; // [B] per-sequence draft counts (0..K) or nullptr (all K)

@@ -561,16 +561,26 @@ struct DrawStep {
 
     // The element of lane l's slot where the cumulative mass from `run`
     // (the masses before this lane) first exceeds tw; its last positive
-    // element if rounding leaves tw past it.
-    __device__ __forceinline__ int walk(ff run, ff tw, int l) const {
+    // element if rounding leaves tw past it. d0, d1: tw's distances to the
+    // chosen element's lower and upper cumulative edges (0, 0 in the
+    // rounding case).
+    __device__ __forceinline__ int walk(ff run, ff tw, int l, float& d0, float& d1) const {
         ff cum = ff_add(run, l == 0 ? 0.0f : prev);
         int tok = -1, lastp = -1;
+        d0 = 0.0f;
+        d1 = 0.0f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
             if (m[e] > 0.0f) {
                 lastp = i0 + e;
+                const ff below = cum;
                 cum = ff_add(cum, m[e]);
-                if (tok < 0 && ff_gt(cum, tw)) tok = i0 + e;
+                if (tok < 0 && ff_gt(cum, tw)) {
+                    tok = i0 + e;
+                    const ff a = ff_add(tw, ff_neg(below)), z = ff_add(cum, ff_neg(tw));
+                    d0 = a.hi + a.lo;
+                    d1 = z.hi + z.lo;
+                }
             }
         }
         return tok < 0 ? lastp : tok;
@@ -1364,6 +1374,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             }
             if (lane == 0 && (!sample || invalid) && p.out_residual_mass)
                 p.out_residual_mass[b] = __int_as_float(0x7fc00000);
+            if (lane < 2 && (!sample || invalid) && p.out_draw_edges)
+                p.out_draw_edges[2 * (size_t)b + lane] = __int_as_float(0x7fc00000);
             if (lane == 0 && p.status_word && invalid)
                 atomicOr(p.status_word, !len_ok        ? (unsigned)SV_FLAG_BAD_LENGTH
                                         : !mode_ok     ? (unsigned)SV_FLAG_BAD_MODE
@@ -1649,16 +1661,25 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 if (sh.step_hit[k] >= 0) kstar = k;
             if (kstar >= 0 && warp == kstar) {
                 const int l = sh.step_hit[kstar];
-                const int token = st.walk(run, tw, l);
+                float d0, d1;
+                const int token = st.walk(run, tw, l, d0, d1);
                 if (lane == l) {
                     if (p.overlap_previous) grid_dependency_wait();
                     p.out_tokens[(size_t)b * (K + 1) + j] = token;
+                    if (p.out_draw_edges) {
+                        p.out_draw_edges[2 * (size_t)b] = d0;
+                        p.out_draw_edges[2 * (size_t)b + 1] = d1;
+                    }
                 }
             } else if (kstar < 0 && tid == 0) {
                 int lp = -1;  // tw past the part's mass: its last positive element
                 for (int k = 0; k < STEPS; ++k) lp = max(lp, sh.step_lp[k]);
                 if (p.overlap_previous) grid_dependency_wait();
                 p.out_tokens[(size_t)b * (K + 1) + j] = lp;
+                if (p.out_draw_edges) {
+                    p.out_draw_edges[2 * (size_t)b] = 0.0f;
+                    p.out_draw_edges[2 * (size_t)b + 1] = 0.0f;
+                }
             }
         }
     }
@@ -1694,6 +1715,10 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 // sequence as invalid rather than leave a slot unwritten.
                 p.out_tokens[(size_t)b * (K + 1) + j] = -1;
                 p.out_n_accepted[b] = -1;
+                if (p.out_draw_edges) {
+                    p.out_draw_edges[2 * (size_t)b] = __int_as_float(0x7fc00000);
+                    p.out_draw_edges[2 * (size_t)b + 1] = __int_as_float(0x7fc00000);
+                }
                 if (p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_BAD_ROW);
             }
             if (p.out_residual_mass) p.out_residual_mass[b] = sh.total.hi + sh.total.lo;

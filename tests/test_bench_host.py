@@ -50,3 +50,24 @@ def test_algorithmic_bytes_by_hand():
     assert bench.alg_bytes(Case, np.array([2, 1, 4])) == base + 2 * row + row
     # an invalid sample sequence takes no second pass
     assert bench.alg_bytes(Case, np.array([-1, 0, 4])) == base + row
+
+
+def test_both_arms_describe_the_workload_identically():
+    # the reference arm and the GPU arm build their config from one function
+    a = bench.bench_config("c4", 256, 8, 151936, 2, 1_476_000_000, 126 * 2**20, 1)
+    b = bench.bench_config("c4", 256, 8, 151936, 2, 1_476_000_000, 126 * 2**20, 1)
+    assert a == b and a["workload"].startswith("c4:") and a["rows_per_step"] == 256 * 9
+
+
+def test_input_sets_exceed_twice_l2():
+    l2 = 126 * 2**20
+    for name in ("c2", "c3", "c4"):
+        n, one = bench.n_input_sets(name, l2)
+        assert n >= 2 and n * one > 2 * l2
+    n2, _ = bench.n_input_sets("c2", l2)
+    assert n2 % 3 == 0  # the c2 sets cycle over three draft-noise levels
+
+
+def test_sub_results_have_fixed_step_counts():
+    for name in ("c2", "c3", "c5", "ragged", "tree", "lookup", "commit"):
+        assert bench.SUB_STEPS[name] >= 50

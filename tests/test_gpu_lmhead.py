@@ -16,9 +16,11 @@ the accept test |u*P_d - P_t| and the draw's distance to an interval edge
 move by at most 2*delta/T relative (every logit moves by <= delta, the
 log-normaliser by <= delta), and a greedy argmax by a top-2 gap < 2*delta.
 That worst-case band is wide next to the probability intervals of a flat
-V = 128256 distribution (logit spread ~1.3), so most draws fall inside it;
-what keeps the check sharp is that decisions inside the band must still
-agree on all but max(1, 1%) of the sequences, as on the logits path.
+V = 128256 distribution (logit spread ~1.3), so most draws fall inside it.
+This comparison checks the GEMM's accuracy. The decisions themselves are
+pinned by a second one: the oracle runs on the very fp32 logits the GEMM
+wrote (and the same draft rows), and the fused verify must then agree with
+it exactly outside the ordinary near-tie bands, as on the logits path.
 """
 import numpy as np
 import pytest
@@ -94,6 +96,22 @@ def test_gemm_c_loop_agrees_with_matrix_product():
     a = orc.lmhead_logits(bits(hidden), bits(W))
     b = orc.lmhead_logits(bits(hidden), bits(W), use_c=True)
     np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-13)
+
+
+def log_ties(label, res, ref):
+    import json
+    import os
+    path = os.environ.get("SV_PARITY_LOG")
+    if not path:
+        return
+    acc = int((ref["accept_margin"] < ACCEPT_TIE_REL).sum())
+    dm = ref["draw_margin"][np.isfinite(ref["draw_margin"])]
+    with open(path, "a") as f:
+        f.write(json.dumps({"case": label, "sequences": res["sequences"], "near_ties": res["near_ties"],
+                            "accept_near_ties": acc, "draw_near_ties": res["near_ties"] - acc,
+                            "near_tie_mismatches": res["near_tie_mismatches"],
+                            "mismatches": res["mismatches"],
+                            "draw_margins": sorted(float(x) for x in dm)}) + "\n")
 
 
 def check(res, delta):
@@ -182,34 +200,57 @@ def run_lmhead_case(case, seed, mode):
     ref = orc.verify(ref_logits.reshape(B, K1, V), bits(case.draft) if mode == "sample" else None,
                      case.tokens.numpy(), case.temperature, 1 if mode == "sample" else 0, seed=seed,
                      threads=16)
-    return out_t.cpu().numpy(), out_n.cpu().numpy(), ref, ref_logits, delta
+    # the oracle on the GPU's own fp32 logits: the fused verify must decide
+    # exactly as the oracle does on those values (ordinary near-tie bands)
+    ref_gpu = orc.verify(ws_logits.cpu().numpy().reshape(B, K1, V),
+                         bits(case.draft) if mode == "sample" else None, case.tokens.numpy(),
+                         case.temperature, 1 if mode == "sample" else 0, seed=seed, threads=16)
+    return out_t.cpu().numpy(), out_n.cpu().numpy(), ref, ref_logits, delta, ref_gpu
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2, 4])
 def test_verify_lmhead_full_workload_sample(seed):
     case = synth.make_workload("c5", seed=seed)
     B, K1, _ = case.hidden.shape
-    got_t, got_n, ref, _, delta = run_lmhead_case(case, seed, "sample")
+    got_t, got_n, ref, _, delta, ref_gpu = run_lmhead_case(case, seed, "sample")
     T = case.temperature
     assert delta < 1e-3, delta
+    # GEMM accuracy: against the oracle on exact logits, bands widened by
+    # the measured logit error
     ties = near_ties(ref, accept_rel=ACCEPT_TIE_REL + 2.2 * delta / T,
                      draw_abs=DRAW_TIE_ABS + 4.4 * delta / T)
     check(compare(got_t, got_n, ref, ties=ties), delta)
     assert (ref["n_accepted"] >= 0).all()
+    # every decision at full size: against the oracle on the GPU's logits,
+    # the ordinary bands, the same cap on near-ties as the logits path
+    res = compare(got_t, got_n, ref_gpu)
+    check(res, 0.0)
+    log_ties(f"c5 seed={seed}", res, ref_gpu)
+    # c5's rows are nearly flat (logit spread ~1.3 over V = 128256), so the
+    # chosen token's residual interval is only a few 1e-6 wide and the draw
+    # band (measured on the logits path) covers a large share of draws: up to
+    # 8 of 32 in the measured seeds. Those are counted, and must still agree
+    # but for max(1, 1%) of the sequences.
+    assert res["near_ties"] <= 0.35 * res["sequences"], res
+    assert (ref_gpu["n_accepted"] >= 0).all()
 
 
 def test_verify_lmhead_greedy():
     case = synth.make_workload("c5", seed=3)
     B, K1, _ = case.hidden.shape
-    got_t, got_n, ref, ref_logits, delta = run_lmhead_case(case, 3, "greedy")
+    got_t, got_n, ref, ref_logits, delta, ref_gpu = run_lmhead_case(case, 3, "greedy")
     check(compare(got_t, got_n, ref, ties=greedy_ties(ref_logits, B, K1, delta)), delta)
+    # on the GPU's own logits greedy has no near-ties: equal maxima resolve
+    # to the lowest index on both sides
+    assert np.array_equal(got_t, ref_gpu["tokens"]) and np.array_equal(got_n, ref_gpu["n_accepted"])
 
 
 def test_verify_lmhead_small_ragged_vocab():
     case = synth.make_lmhead_case(B=3, K=4, V=1000, d=192, seed=11)
-    got_t, got_n, ref, _, delta = run_lmhead_case(case, 11, "sample")
+    got_t, got_n, ref, _, delta, ref_gpu = run_lmhead_case(case, 11, "sample")
     ties = near_ties(ref, accept_rel=ACCEPT_TIE_REL + 2.2 * delta, draw_abs=DRAW_TIE_ABS + 4.4 * delta)
     check(compare(got_t, got_n, ref, ties=ties), delta)
+    check(compare(got_t, got_n, ref_gpu), 0.0)
 
 
 @pytest.mark.parametrize("mode,B,K,d,V,T", [

@@ -13,7 +13,7 @@ import torch
 
 import synth
 from oracle import oracle as orc
-from oracle.parity import compare, compare_probabilities, near_ties
+from oracle.parity import ACCEPT_TIE_REL, DRAW_TIE_ABS, compare, compare_probabilities, near_ties
 from speculative_decoding_verification_24_gb300 import binding, spec_verify, spec_verify_ex
 from speculative_decoding_verification_24_gb300.build import build
 from synth.workloads import to_numpy_logits
@@ -23,22 +23,43 @@ pytestmark = pytest.mark.gpu
 THREADS = min(16, os.cpu_count() or 1)
 # Flagged near-ties depend on how much mass the distributions put in tokens
 # narrower than the rounding band; actual disagreements inside the band are
-# what the float32 arithmetic can cause, and must stay rare.
-MAX_TIE_FRACTION = 0.10
+# what the float32 arithmetic can cause, and must stay rare. The cap on
+# near-ties applies to a whole workload (every call of a case together):
+# one call of c2 holds only 8 sequences, too few for a fraction to mean much.
+MAX_TIE_FRACTION = 0.05
 MAX_TIE_MISMATCH_FRACTION = 0.01
 PARITY_LOG = os.environ.get("SV_PARITY_LOG")
 
 
-def log_case(label, res, worst_t, worst_d):
+def log_case(label, res, worst_t, worst_d, edge, acc_ties):
     if not PARITY_LOG:
         return
     import json
     with open(PARITY_LOG, "a") as f:
         f.write(json.dumps({"case": label, "sequences": res["sequences"],
-                            "near_ties": res["near_ties"],
+                            "near_ties": res["near_ties"], "accept_near_ties": acc_ties,
+                            "draw_near_ties": res["near_ties"] - acc_ties,
                             "near_tie_mismatches": res["near_tie_mismatches"],
                             "mismatches": res["mismatches"], "worst_rel_p_target": worst_t,
-                            "worst_rel_p_draft": worst_d}) + "\n")
+                            "worst_rel_p_draft": worst_d, **edge}) + "\n")
+
+
+def draw_edge_error(g, ref):
+    """How far the kernel's float32 arithmetic moves the final draw: over the
+    sample sequences on which GPU and oracle agree, the largest difference
+    between the GPU's and the oracle's distances from the draw target t to
+    the chosen token's lower and upper cumulative edges (probability units),
+    and that difference relative to the draw's total mass."""
+    ge = np.asarray(g["draw_edges"], dtype=np.float64)
+    re = ref["draw_edges"]
+    same = ((g["n_accepted"] == ref["n_accepted"]) & (g["tokens"] == ref["tokens"]).all(axis=1)
+            & np.isfinite(re).all(axis=1) & np.isfinite(ge).all(axis=1))
+    if not same.any():
+        return {"draw_edge_seqs": 0, "draw_edge_err": 0.0, "draw_edge_rel_err": 0.0}
+    err = np.abs(ge[same] - re[same]).max(axis=1)
+    rel = err / ref["residual_mass"][same]
+    return {"draw_edge_seqs": int(same.sum()), "draw_edge_err": float(err.max()),
+            "draw_edge_rel_err": float(rel.max())}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -62,9 +83,13 @@ def run_pair(case, seed, seq_ids=None, cluster_size=0, modes=None):
 
 def check(g, ref, label="", max_tie_fraction=MAX_TIE_FRACTION):
     res = compare(g["tokens"], g["n_accepted"], ref)
+    acc_ties = int((ref["accept_margin"] < ACCEPT_TIE_REL).sum())
     worst_t = compare_probabilities(g["p_target"], ref["p_target"], ref["n_accepted"])
     worst_d = compare_probabilities(g["p_draft"], ref["p_draft"], ref["n_accepted"])
-    log_case(label, res, worst_t, worst_d)
+    edge = draw_edge_error(g, ref)
+    log_case(label, res, worst_t, worst_d, edge, acc_ties)
+    # the draw's rounding error must stay inside the draw near-tie band
+    assert edge["draw_edge_err"] < DRAW_TIE_ABS, (label, edge)
     assert res["mismatches"] == 0, (label, res)
     assert res["near_ties"] <= max(1, max_tie_fraction * res["sequences"]), (label, res)
     assert res["near_tie_mismatches"] <= max(1, MAX_TIE_MISMATCH_FRACTION * res["sequences"]), \
@@ -77,6 +102,24 @@ def check(g, ref, label="", max_tie_fraction=MAX_TIE_FRACTION):
     return res
 
 
+class Tally:
+    """Near-tie counts of several calls of one case, capped together."""
+
+    def __init__(self, label):
+        self.label = label
+        self.sequences = self.near_ties = self.tie_mismatches = 0
+
+    def add(self, res):
+        self.sequences += res["sequences"]
+        self.near_ties += res["near_ties"]
+        self.tie_mismatches += res["near_tie_mismatches"]
+
+    def check(self, max_tie_fraction=MAX_TIE_FRACTION):
+        got = (self.label, self.near_ties, self.tie_mismatches, self.sequences)
+        assert self.near_ties <= max(1, max_tie_fraction * self.sequences), got
+        assert self.tie_mismatches <= max(1, MAX_TIE_MISMATCH_FRACTION * self.sequences), got
+
+
 # ----------------------------------------------------------------- the workloads
 
 
@@ -84,42 +127,48 @@ def check(g, ref, label="", max_tie_fraction=MAX_TIE_FRACTION):
 def test_c1_thousand_calls(mode):
     """B=1, K=4, V=1000 fp32: call c uses input seed c and verify seed c."""
     dev = torch.device("cuda")
-    ties = 0
+    tally = Tally(f"c1 {mode}")
     for c in range(1000):
         case = synth.make_workload("c1", seed=c, device=dev, modes=mode)
         g, ref = run_pair(case, seed=c)
-        res = check(g, ref, f"c1 call {c}", max_tie_fraction=1.0)
-        ties += res["near_ties"]
-    assert ties <= 20
+        tally.add(check(g, ref, f"c1 call {c}", max_tie_fraction=1.0))
+    tally.check(0.01)
 
 
 @pytest.mark.parametrize("tau", [0.3, 1.0, 3.0])
 def test_c2_sweep(tau):
     dev = torch.device("cuda")
     case = synth.make_workload("c2", seed=2, device=dev, tau=tau)
+    tally = Tally(f"c2 tau={tau}")
     for s in range(100):
         g, ref = run_pair(case, seed=s)
-        check(g, ref, f"c2 tau={tau} seed={s}", max_tie_fraction=1.0)
+        tally.add(check(g, ref, f"c2 tau={tau} seed={s}", max_tie_fraction=1.0))
+    tally.check()  # 800 sequences
 
 
 def test_c3_half_greedy_half_sample():
     dev = torch.device("cuda")
     case = synth.make_workload("c3", seed=3, device=dev)
     assert case.modes[:32].eq(0).all() and case.modes[32:].eq(1).all()
+    tally = Tally("c3")
     for s in range(4):
         g, ref = run_pair(case, seed=s)
-        check(g, ref, f"c3 seed={s}")
+        tally.add(check(g, ref, f"c3 seed={s}"))
         assert (g["n_accepted"] >= 0).all()
+    tally.check(0.02)
 
 
 def test_c4_full_size():
     dev = torch.device("cuda")
     case = synth.make_workload("c4", seed=4, device=dev)
+    tally = Tally("c4")
     for s in range(2):
         g, ref = run_pair(case, seed=s)
         res = check(g, ref, f"c4 seed={s}")
+        tally.add(res)
         # accepted lengths vary within the batch (tau per sequence)
         assert len(set(g["n_accepted"].tolist())) > 3, res
+    tally.check(0.02)  # 512 sequences
 
 
 @pytest.mark.parametrize("name,seeds", [("c2", (5, 6, 7)), ("c3", (3, 4)), ("c4", (4,))])
@@ -133,23 +182,25 @@ def test_full_size_as_the_benchmark_launches(name, seeds):
     outs = [spec_verify_ex(case.target, case.draft, case.tokens, case.temperature, modes=modes, seed=s,
                            debug=True, overlap_previous=True) for s in seeds]
     torch.cuda.synchronize()
+    tally = Tally(f"{name} overlapped")
     for s, out in zip(seeds, outs):
         ref = orc.verify(to_numpy_logits(case.target), to_numpy_logits(case.draft), case.tokens.cpu().numpy(),
                          case.temperature, modes.cpu().numpy(), seed=s, threads=THREADS)
         g = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in out.items()}
-        # c2's 8 flat sequences may all sit near an edge (as in test_c2_sweep):
-        # the disagreement caps still apply
-        check(g, ref, f"{name} overlapped seed={s}", max_tie_fraction=1.0 if name == "c2" else MAX_TIE_FRACTION)
+        tally.add(check(g, ref, f"{name} overlapped seed={s}", max_tie_fraction=1.0))
         assert (g["n_accepted"] >= 0).all()
+    tally.check(0.10 if name == "c2" else MAX_TIE_FRACTION)  # c2: 24 sequences in all
 
 
 @pytest.mark.parametrize("cs", [1, 2, 4, 8, 16])
 def test_every_cluster_size(cs):
     dev = torch.device("cuda")
     case = synth.make_workload("c2", seed=2, device=dev, tau=1.0)
+    tally = Tally(f"cluster {cs}")
     for s in range(10):
         g, ref = run_pair(case, seed=s, cluster_size=cs)
-        check(g, ref, f"cluster {cs} seed={s}", max_tie_fraction=1.0)
+        tally.add(check(g, ref, f"cluster {cs} seed={s}", max_tie_fraction=1.0))
+    tally.check()  # 80 sequences
 
 
 # ----------------------------------------------------------------- edge cases

@@ -45,8 +45,11 @@ def worker(rank, port, results):
         gathered = [torch.empty_like(mine) for _ in range(WORLD)]
         dist.all_gather(gathered, mine)
         slowest = bench.max_over_ranks(1.0 + rank, "cpu", WORLD)
+        # the bench line's whole-job rates: rank r verified 10 + r rows and
+        # 1000 * (r + 1) bytes in (r + 1) ms
+        rates = bench.job_rates(10 + rank, 1000 * (rank + 1), 1.0 + rank, "cpu", WORLD)
         if rank == 0:
-            results.put((torch.stack(gathered).numpy(), slowest))
+            results.put((torch.stack(gathered).numpy(), slowest, rates))
     finally:
         dist.destroy_process_group()
 
@@ -59,7 +62,7 @@ def test_shards_with_global_ids_equal_one_call_and_time_is_the_slowest_rank():
     procs = [ctx.Process(target=worker, args=(r, port, results)) for r in range(WORLD)]
     for p in procs:
         p.start()
-    gathered, slowest = results.get(timeout=120)
+    gathered, slowest, rates = results.get(timeout=120)
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
@@ -73,3 +76,7 @@ def test_shards_with_global_ids_equal_one_call_and_time_is_the_slowest_rank():
         assert (toks == full["tokens"][r * Bs:(r + 1) * Bs]).all()
         assert (n == full["n_accepted"][r * Bs:(r + 1) * Bs]).all()
     assert slowest == float(WORLD)
+    # rows and bytes of both ranks over the slowest rank's 2 ms
+    assert rates["ms_max"] == 2.0
+    assert np.isclose(rates["rows_per_s"], (10 + 11) / 2e-3)
+    assert np.isclose(rates["gbs"], (1000 + 2000) / 2e-3 / 1e9)
