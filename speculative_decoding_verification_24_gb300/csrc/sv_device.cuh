@@ -89,8 +89,9 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 // --------------------------------------------------------------------------
 // Partial softmax statistics in the base-2 domain. With c = log2(e) / T, a
 // partial over a set of logits l is (R, s): R an integer-valued float with
-// R >= max(l * c) - 1, s = sum 2^(l * c - R). Because every R is an integer,
-// two partials merge by an exact power-of-two rescale.
+// max(l * c) - 13 < R <= ceil(max(l * c)), s = sum 2^(l * c - R) (R tracks
+// the maximum only as closely as keeps every term below 2^13). Because every
+// R is an integer, two partials merge by an exact power-of-two rescale.
 // Invalid partials carry R = NaN or R = +inf; an empty one is (-inf, 0).
 // --------------------------------------------------------------------------
 struct SoftPart {
@@ -248,6 +249,26 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
         : "memory");
 }
 
+// An L2 policy under which the lines a copy brings in are evicted before any
+// others. The logits each pass through L2 once per call; a call streams more
+// bytes than L2 holds, and under the default policy that stream also evicts
+// the kernel's own instructions, whose once-per-call phases (decision, final
+// draw) then fetch them from HBM.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// bulk_g2s with an L2 cache policy (l2_evict_first_policy).
+__device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(const void* p) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -299,6 +320,40 @@ __device__ __forceinline__ f32x2 ex2x2(f32x2 x) {
     float a, b;
     unpack2(x, a, b);
     return pack2(ex2(a), ex2(b));
+}
+
+// 2^x of both halves with no MUFU operation, on the FMA and integer pipes, to
+// share the exponentials of an SFU-bound loop between the two. The argument
+// splits as x = n + r, n the nearest integer (adding 1.5 * 2^23 rounds x into
+// the low mantissa bits) and r in [-1/2, 1/2] (exact); 2^r comes from a
+// degree-6 minimax polynomial (relative error 1.9e-9 for the exact
+// coefficients; gen_exp2_poly.py derives them with the Remez exchange and
+// measures 7.9e-8 for this float32 Horner evaluation over [-126, 0], against
+// about 2^-22 for ex2.approx); n is added to the exponent field as an
+// integer. Arguments below -125, -inf included, count as -125: their 2^x
+// (< 2.4e-38) stands in for a term that ex2.approx.ftz flushes to zero, which
+// no float32 sum of terms up to 1 can tell apart. A NaN argument also gives
+// 2^-125: callers track NaN rows through their maxima, not these sums.
+__device__ __forceinline__ f32x2 ex2_poly2(f32x2 x) {
+    float a, b;
+    unpack2(x, a, b);
+    const f32x2 xc = pack2(fmaxf(a, -125.0f), fmaxf(b, -125.0f));
+    const f32x2 M = pack2(12582912.0f, 12582912.0f);
+    const f32x2 t = add2(xc, M);
+    const f32x2 r = fma2(add2(t, pack2(-12582912.0f, -12582912.0f)), pack2(-1.0f, -1.0f), xc);
+    f32x2 p = fma2(pack2(0x1.41d334p-13f, 0x1.41d334p-13f), r, pack2(0x1.5f456ap-10f, 0x1.5f456ap-10f));
+    p = fma2(p, r, pack2(0x1.3b2dbcp-7f, 0x1.3b2dbcp-7f));
+    p = fma2(p, r, pack2(0x1.c6aed4p-5f, 0x1.c6aed4p-5f));
+    p = fma2(p, r, pack2(0x1.ebfbdap-3f, 0x1.ebfbdap-3f));
+    p = fma2(p, r, pack2(0x1.62e43p-1f, 0x1.62e43p-1f));
+    p = fma2(p, r, pack2(1.0f, 1.0f));
+    float pa, pb, ta, tb;
+    unpack2(p, pa, pb);
+    unpack2(t, ta, tb);
+    // t's low mantissa bits hold n (two's complement for n < 0); shifted
+    // left by 23 they are n * 2^23 modulo 2^32, the exponent increment
+    return pack2(__uint_as_float(__float_as_uint(pa) + (__float_as_uint(ta) << 23)),
+                 __uint_as_float(__float_as_uint(pb) + (__float_as_uint(tb) << 23)));
 }
 
 // Element pair of a 32-bit word: bf16 x2 widened exactly, low half first.

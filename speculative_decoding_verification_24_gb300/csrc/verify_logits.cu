@@ -52,6 +52,10 @@ namespace cg = cooperative_groups;
 
 namespace sv {
 
+#ifndef SV_POLY_MASK
+#define SV_POLY_MASK 0
+#endif
+
 constexpr int MAX_K = 31;
 constexpr int MAX_ROWS = 2 * MAX_K + 1;
 constexpr unsigned FULL = 0xFFFFFFFFu;
@@ -297,7 +301,8 @@ __device__ __forceinline__ void soft_group(SoftAcc& a, const uint4 (&d)[U], floa
     for (int u = 0; u < U; ++u) {
 #pragma unroll
         for (int k = 0; k < PAIRS; ++k) {
-            const f32x2 e = ex2x2(fma2(slot_pair<T>(d[u], k), c2, nR2));
+            const f32x2 arg = fma2(slot_pair<T>(d[u], k), c2, nR2);
+            const f32x2 e = ((SV_POLY_MASK >> ((u * PAIRS + k) & 15)) & 1) ? ex2_poly2(arg) : ex2x2(arg);
             switch ((u * PAIRS + k) & 3) {
                 case 0: a.a0 = add2(a.a0, e); break;
                 case 1: a.a1 = add2(a.a1, e); break;
@@ -772,10 +777,53 @@ constexpr int CHUNK_LANE_SLOTS = STAGE_SLOTS / 32;  // 8 slots per lane
 // GROUP_SLOTS slots per lane.
 constexpr int GROUP_SLOTS = 4;
 
+// Limit of a lane's chunk sum on the fast path: below it, no element of the
+// chunk exceeds the lane's R by more than log2(FAST_SUM_LIMIT) = 12 (in units
+// of l * c), so every later sum and product of the step stays far from the
+// float32 range's end.
+constexpr float FAST_SUM_LIMIT = 4096.0f;
+
+// Fast path of a full chunk in sample mode: 2^(l * c - R) at the lane's
+// current R, with no per-group maximum and no rescale, summed into
+// chunk-local pairs. Returns false (and leaves the running partial as it
+// was) when the chunk needs the exact path: a lane without a finite R yet,
+// or a lane sum of FAST_SUM_LIMIT or more, infinite or NaN (an element well
+// above R, +inf or NaN). The decision is warp-uniform.
+template <typename T>
+__device__ __forceinline__ bool soft_chunk_fast(SoftAcc& sa, const uint4 (&d)[CHUNK_LANE_SLOTS], float c) {
+    constexpr int PAIRS = Elem<T>::E / 2;
+    if (__any_sync(FULL, !(sa.R > -INFINITY && sa.R < INFINITY))) return false;
+    const f32x2 c2 = pack2(c, c), nR2 = pack2(-sa.R, -sa.R);
+    f32x2 b0 = 0ull, b1 = 0ull, b2 = 0ull, b3 = 0ull;
+#pragma unroll
+    for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) {
+#pragma unroll
+        for (int k = 0; k < PAIRS; ++k) {
+            const f32x2 e = ex2x2(fma2(slot_pair<T>(d[u], k), c2, nR2));
+            switch ((u * PAIRS + k) & 3) {
+                case 0: b0 = add2(b0, e); break;
+                case 1: b1 = add2(b1, e); break;
+                case 2: b2 = add2(b2, e); break;
+                default: b3 = add2(b3, e); break;
+            }
+        }
+    }
+    float x0, x1;
+    unpack2(add2(add2(b0, b1), add2(b2, b3)), x0, x1);
+    if (__any_sync(FULL, !(x0 + x1 < FAST_SUM_LIMIT))) return false;
+    sa.a0 = add2(sa.a0, b0);
+    sa.a1 = add2(sa.a1, b1);
+    sa.a2 = add2(sa.a2, b2);
+    sa.a3 = add2(sa.a3, b3);
+    return true;
+}
+
 template <typename T, bool SAMPLE>
 __device__ __forceinline__ void reduce_chunk(SoftAcc& sa, ArgAcc& aa, const uint4 (&d)[CHUNK_LANE_SLOTS],
                                              int n, int q0, float c, int lane) {
     const bool whole = n == STAGE_SLOTS;
+    if (SAMPLE && whole && soft_chunk_fast<T>(sa, d, c)) return;
+    // (slots past the end of a partial chunk were loaded as -inf)
 #pragma unroll
     for (int g = 0; g < CHUNK_LANE_SLOTS / GROUP_SLOTS; ++g) {
         uint4 x[GROUP_SLOTS];
@@ -783,11 +831,27 @@ __device__ __forceinline__ void reduce_chunk(SoftAcc& sa, ArgAcc& aa, const uint
 #pragma unroll
         for (int u = 0; u < GROUP_SLOTS; ++u) {
             const int i = (g * GROUP_SLOTS + u) * 32 + lane;
-            x[u] = (whole || i < n) ? d[g * GROUP_SLOTS + u] : neg_inf_slot<T>();
+            x[u] = d[g * GROUP_SLOTS + u];
             qs[u] = q0 + i;
         }
         if (SAMPLE) soft_group<T, GROUP_SLOTS>(sa, x, c);
         else arg_slots<T, GROUP_SLOTS>(aa, x, qs);
+    }
+    if (SAMPLE) {
+        // One R for the whole warp (its lanes' maximum, NaN-propagating; an
+        // exact power-of-two rescale of each lane's sums), so that the fast
+        // path of the next chunks falls back only when an element exceeds
+        // the largest one the warp has seen by 2^12.
+        float Rw = sa.R;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Rw = max_nan(Rw, __shfl_xor_sync(FULL, Rw, o));
+        const float sc = sa.R == -INFINITY ? 0.0f : ex2(fmaxf(sa.R - Rw, -1000.0f));
+        const f32x2 sc2 = pack2(sc, sc);
+        sa.a0 = mul2(sa.a0, sc2);
+        sa.a1 = mul2(sa.a1, sc2);
+        sa.a2 = mul2(sa.a2, sc2);
+        sa.a3 = mul2(sa.a3, sc2);
+        sa.R = Rw;
     }
 }
 
@@ -813,7 +877,8 @@ __device__ __forceinline__ void fill_pass1(SeqShared& sh, WarpRing& wr, char* ri
     const int q0 = ri.ia + (chunk - rc.c0) * STAGE_SLOTS;
     const int n = min(STAGE_SLOTS, ri.ib - q0);
     wr.begin_fill(sh, fseq, (uint32_t)n * 16u, lane);
-    if (lane == 0) bulk_g2s(wr.stage(ring, fseq), ri.base + q0, (uint32_t)n * 16u, wr.bar(sh, fseq));
+    if (lane == 0)
+        bulk_g2s_hint(wr.stage(ring, fseq), ri.base + q0, (uint32_t)n * 16u, wr.bar(sh, fseq), l2_evict_first_policy());
 }
 
 // Where the draft token of row r lies in this CTA's pass-1 chunks: the chunk
@@ -912,10 +977,16 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
         const int n = min(STAGE_SLOTS, ib - q0);
         const char* stage = wr.stage(ring, seq);
         uint4 d[CHUNK_LANE_SLOTS];
+        if (n == STAGE_SLOTS) {  // a full chunk (warp-uniform): no per-slot select
 #pragma unroll
-        for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) {
-            const int i = u * 32 + lane;
-            d[u] = i < n ? lds128(stage + i * 16) : neg_inf_slot<TT>();
+            for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) d[u] = lds128(stage + (u * 32 + lane) * 16);
+        } else {  // slots past the chunk's end read as -inf of the row's own type
+            const uint4 pad = (std::is_same<TT, TD>::value || cur_row <= K) ? neg_inf_slot<TT>() : neg_inf_slot<TD>();
+#pragma unroll
+            for (int u = 0; u < CHUNK_LANE_SLOTS; ++u) {
+                const int i = u * 32 + lane;
+                d[u] = i < n ? lds128(stage + i * 16) : pad;
+            }
         }
         if (SAMPLE && chunk == ts.chunk && lane == 0) {
             if (std::is_same<TT, TD>::value || cur_row <= K) capture_logit<TT>(sh, cluster, CS, stage, ts, K, cur_row);
