@@ -1128,6 +1128,17 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // A call may be launched with programmatic stream serialization, and then
+    // start while the work ahead of it on the stream is finishing. A plain
+    // call (no overlap flag, not the LM-head path) reads no input before that
+    // work has completed: it waits here when its prologue reads inputs
+    // (per-sequence modes or draft counts), otherwise just before its first
+    // input read, once the input-free prologue has run. (Without the launch
+    // attribute the wait returns at once.)
+    const bool fused = p.target_parts != nullptr;
+    const bool plain = !p.overlap_previous && !fused;
+    const bool prologue_reads = p.modes != nullptr || p.draft_lens != nullptr;
+    if (plain && prologue_reads) grid_dependency_wait();
     // Cluster c verifies sequence c, or, with per-sequence modes, the c-th of
     // the order (sample sequences, then the others, each in index order): the
     // sequences with the most rows to read start first. Every CTA derives the
@@ -1168,12 +1179,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const TT* tgt = static_cast<const TT*>(p.target);
     const TD* drf = static_cast<const TD*>(p.draft);
 
-    // Programmatic dependent launch: without overlap, nothing is read before
-    // the work ahead on the stream has completed; with it, the whole call may
-    // run alongside that work, and each thread that stores to global memory
-    // first waits for it to complete, just before its stores.
-    const bool fused = p.target_parts != nullptr;
-    if (!p.overlap_previous && !fused) grid_dependency_wait();
+    // With overlap, the whole call may run alongside the work ahead of it,
+    // and each thread that stores to global memory first waits for that work
+    // to complete, just before its stores.
     const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
     // Kb: the drafts this sequence verifies (continuous batching), 0..K
     const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
@@ -1227,6 +1235,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 
     WarpRing wr{warp, 0u, 0u};
     uint32_t seq = 0;  // chunks this warp has handled, over both passes
+    if (plain && !prologue_reads) grid_dependency_wait();  // the first input read follows
     // Lane i of every warp holds draft token x_i (first used after the
     // warp's first chunk has arrived, so the load overlaps the copies).
     const int x_reg = p.tree_parents ? (lane <= K ? __ldg(p.tokens + (size_t)b * (K + 1) + lane) : -1)
@@ -1905,9 +1914,16 @@ static cudaError_t launch_ms(const VerifyParams& p, int cs, cudaStream_t stream)
     // Calls that overlap the previous one share the GPU with it: two CTAs
     // per SM let more calls' copies be in flight at once (c2 back to back:
     // 2.94 -> 2.70 us per call on GB300); a lone call spreads out instead.
-    fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream,
-                p.overlap_previous ? RING_BYTES : launch_smem<TT, TD, MS>(p.B, cs));
-    if (p.overlap_previous || p.target_parts) {
+    const int smem = p.overlap_previous ? RING_BYTES : launch_smem<TT, TD, MS>(p.B, cs);
+    fill_config(cfg, attr, (unsigned)(p.B * cs), cs, stream, smem);
+    // The call may launch before the work ahead of it has completed; the
+    // kernel waits for that work before its first input read (plain calls)
+    // or first store (overlap). Plain calls do so only when their grid
+    // spreads one CTA per SM: a larger grid whose CTAs took SMs one by one as
+    // the previous grid's left ended up worse placed than one launched onto
+    // an idle GPU (measured on GB300: c3 37.6 -> 42.4 us, c4 235 -> 240 us;
+    // c2, spread, 14.6 -> 13.1 us).
+    if (p.overlap_previous || p.target_parts || smem == SPREAD_SMEM) {
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 2;
