@@ -43,6 +43,10 @@ def contexts(B, L_max, vocab, seed, copy_prob=0.3):
     # one CTA per 4096-token tile, up to 8 per sequence (uneven parts, several
     # tiles per CTA, windows that straddle a part or tile boundary)
     (6, 20000, 7, 3, 8), (4, 40000, 100, 5, 16), (5, 12289, 3, 16, 64),
+    # the whole-context kernel (L_max a multiple of 4, at most 24576 tokens in
+    # shared memory): its largest size, the full benchmark shape, and the
+    # first size past it (the cluster kernel again)
+    (7, 24576, 11, 3, 8), (256, 16384, 32000, 3, 8), (5, 24580, 9, 4, 12),
 ])
 def test_prompt_lookup_matches_oracle(B, L_max, vocab, m, k):
     tok, lens = contexts(B, L_max, vocab, seed=B + L_max + vocab)
@@ -63,3 +67,16 @@ def test_prompt_lookup_invalid_lengths():
     ref = orc.prompt_lookup(tok, lens, 3, 4)
     assert (n.cpu().numpy() == ref["n_drafts"]).all() and (d.cpu().numpy() == ref["drafts"]).all()
     assert n[2] == -1 and n[4] == -1
+
+
+def test_prompt_lookup_unaligned_contexts_take_the_cluster_kernel():
+    # a context buffer that starts 4 bytes past a 16-byte boundary cannot be
+    # bulk-copied; the result must not change
+    tok, lens = contexts(9, 2048, 20, seed=5)
+    big = torch.zeros(tok.size + 1, dtype=torch.int32, device="cuda")
+    view = big[1:].view(9, 2048)
+    view.copy_(torch.from_numpy(tok))
+    d, n = spec_prompt_lookup(view, torch.from_numpy(lens).cuda(), 3, 6)
+    torch.cuda.synchronize()
+    ref = orc.prompt_lookup(tok, lens, 3, 6)
+    assert (n.cpu().numpy() == ref["n_drafts"]).all() and (d.cpu().numpy() == ref["drafts"]).all()
