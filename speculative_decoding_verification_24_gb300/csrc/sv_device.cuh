@@ -322,40 +322,6 @@ __device__ __forceinline__ f32x2 ex2x2(f32x2 x) {
     return pack2(ex2(a), ex2(b));
 }
 
-// 2^x of both halves with no MUFU operation, on the FMA and integer pipes, to
-// share the exponentials of an SFU-bound loop between the two. The argument
-// splits as x = n + r, n the nearest integer (adding 1.5 * 2^23 rounds x into
-// the low mantissa bits) and r in [-1/2, 1/2] (exact); 2^r comes from a
-// degree-6 minimax polynomial (relative error 1.9e-9 for the exact
-// coefficients; gen_exp2_poly.py derives them with the Remez exchange and
-// measures 7.9e-8 for this float32 Horner evaluation over [-126, 0], against
-// about 2^-22 for ex2.approx); n is added to the exponent field as an
-// integer. Arguments below -125, -inf included, count as -125: their 2^x
-// (< 2.4e-38) stands in for a term that ex2.approx.ftz flushes to zero, which
-// no float32 sum of terms up to 1 can tell apart. A NaN argument also gives
-// 2^-125: callers track NaN rows through their maxima, not these sums.
-__device__ __forceinline__ f32x2 ex2_poly2(f32x2 x) {
-    float a, b;
-    unpack2(x, a, b);
-    const f32x2 xc = pack2(fmaxf(a, -125.0f), fmaxf(b, -125.0f));
-    const f32x2 M = pack2(12582912.0f, 12582912.0f);
-    const f32x2 t = add2(xc, M);
-    const f32x2 r = fma2(add2(t, pack2(-12582912.0f, -12582912.0f)), pack2(-1.0f, -1.0f), xc);
-    f32x2 p = fma2(pack2(0x1.41d334p-13f, 0x1.41d334p-13f), r, pack2(0x1.5f456ap-10f, 0x1.5f456ap-10f));
-    p = fma2(p, r, pack2(0x1.3b2dbcp-7f, 0x1.3b2dbcp-7f));
-    p = fma2(p, r, pack2(0x1.c6aed4p-5f, 0x1.c6aed4p-5f));
-    p = fma2(p, r, pack2(0x1.ebfbdap-3f, 0x1.ebfbdap-3f));
-    p = fma2(p, r, pack2(0x1.62e43p-1f, 0x1.62e43p-1f));
-    p = fma2(p, r, pack2(1.0f, 1.0f));
-    float pa, pb, ta, tb;
-    unpack2(p, pa, pb);
-    unpack2(t, ta, tb);
-    // t's low mantissa bits hold n (two's complement for n < 0); shifted
-    // left by 23 they are n * 2^23 modulo 2^32, the exponent increment
-    return pack2(__uint_as_float(__float_as_uint(pa) + (__float_as_uint(ta) << 23)),
-                 __uint_as_float(__float_as_uint(pb) + (__float_as_uint(tb) << 23)));
-}
-
 // Element pair of a 32-bit word: bf16 x2 widened exactly, low half first.
 __device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) {
     return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));

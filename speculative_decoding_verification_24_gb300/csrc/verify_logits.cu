@@ -52,10 +52,6 @@ namespace cg = cooperative_groups;
 
 namespace sv {
 
-#ifndef SV_POLY_MASK
-#define SV_POLY_MASK 0
-#endif
-
 constexpr int MAX_K = 31;
 constexpr int MAX_ROWS = 2 * MAX_K + 1;
 constexpr unsigned FULL = 0xFFFFFFFFu;
@@ -301,8 +297,7 @@ __device__ __forceinline__ void soft_group(SoftAcc& a, const uint4 (&d)[U], floa
     for (int u = 0; u < U; ++u) {
 #pragma unroll
         for (int k = 0; k < PAIRS; ++k) {
-            const f32x2 arg = fma2(slot_pair<T>(d[u], k), c2, nR2);
-            const f32x2 e = ((SV_POLY_MASK >> ((u * PAIRS + k) & 15)) & 1) ? ex2_poly2(arg) : ex2x2(arg);
+            const f32x2 e = ex2x2(fma2(slot_pair<T>(d[u], k), c2, nR2));
             switch ((u * PAIRS + k) & 3) {
                 case 0: a.a0 = add2(a.a0, e); break;
                 case 1: a.a1 = add2(a.a1, e); break;
