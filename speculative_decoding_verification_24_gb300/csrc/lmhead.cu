@@ -209,6 +209,25 @@ __device__ __forceinline__ bool epi_barrier_and(bool v) {
 // two warps ahead of the GEMM. Lane k keeps the running partial of row k of
 // each of its batches across the tiles (in tile order) and writes it once,
 // at the end: one partial per row and CTA.
+// Draft-row loads with an L2 evict-first policy: the verify step needs the
+// draft rows again only for one row per sequence, while the fp32 logits this
+// kernel writes are what its final draw re-reads; evict-first keeps the 41 MB
+// of draft reads (c5) from pushing those logits out of L2.
+__device__ __forceinline__ uint4 ld_draft_v4(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ uint2 ld_draft_v2(const void* p, uint64_t pol) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 template <bool F32>
 __device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int lane, int my_tiles, const int* err) {
     constexpr int RB = F32 ? 16 : 32;
@@ -216,6 +235,7 @@ __device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int la
     using Raw = typename std::conditional<F32, uint4, uint2>::type;
     constexpr int ESZ = F32 ? 4 : 2;
     const bool vec = (reinterpret_cast<uintptr_t>(p.draft) & (uintptr_t)(4 * ESZ - 1)) == 0;
+    const uint64_t pol = policy_evict_first();
     const float2 empty = pack(SoftPart{-INFINITY, 0.0f});
     float2 run[MAXB];  // indexed at run time: a few bytes of local memory per lane
 #pragma unroll
@@ -238,7 +258,7 @@ __device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int la
                     raw[k] = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
                     if (ok) {
                         if (vec) {
-                            raw[k] = ld_stream(reinterpret_cast<const uint4*>(row));
+                            raw[k] = ld_draft_v4(row, pol);
                         } else {
                             const uint32_t* r32 = reinterpret_cast<const uint32_t*>(row);
                             raw[k] = make_uint4(__ldg(r32), __ldg(r32 + 1), __ldg(r32 + 2), __ldg(r32 + 3));
@@ -248,7 +268,7 @@ __device__ __forceinline__ void draft_partials(const LmParams& p, int w2, int la
                     raw[k] = make_uint2(0xFF80FF80u, 0xFF80FF80u);  // bf16 -inf pairs
                     if (ok) {
                         if (vec) {
-                            raw[k] = __ldg(reinterpret_cast<const uint2*>(row));
+                            raw[k] = ld_draft_v2(row, pol);
                         } else {
                             const unsigned short* r16 = reinterpret_cast<const unsigned short*>(row);
                             raw[k] = make_uint2((uint32_t)__ldg(r16) | ((uint32_t)__ldg(r16 + 1) << 16),
