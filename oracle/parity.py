@@ -16,7 +16,7 @@ Near-tie bands:
                 sample sequence of the GPU parity suite (about 10^4 sequences:
                 c1-c4, all cluster sizes, temperatures 0.05-10, misaligned and
                 ragged rows) they differ from the oracle's by at most
-                2.47e-7. The band is twice that. It is absolute, not relative
+                2.85e-7; the band is 1.75 times that. It is absolute, not relative
                 to the draw's total mass S_r: the error comes from the rows'
                 probabilities (each with its own float32 normaliser), so it
                 does not shrink with the residual's mass.
