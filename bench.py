@@ -398,7 +398,12 @@ def logits_timing(sets, steps, warmup, stream, device, world, rank, label):
     res["serial_ms"] = replay_ms(s_graph, stream, f"{label} serial x{steps}")
     del s_graph
     sl = slice(warmup, warmup + steps)
-    res["serial_identical"] = bool(torch.equal(out_tok[sl], s_tok[sl]) and torch.equal(out_n[sl], s_n[sl]))
+    same = (out_tok[sl] == s_tok[sl]).all(dim=2) & (out_n[sl] == s_n[sl])
+    # the two runs may use different cluster sizes, so their float32 sums
+    # differ in rounding and may decide a near-tie differently; the oracle
+    # leg checks both runs
+    res["serial_differing"] = int((~same).sum())
+    res["serial_tok"], res["serial_n"] = s_tok, s_n
     return res
 
 
@@ -500,7 +505,7 @@ def run_ours(args, rank, world, device):
                    "hbm_gbs": serial["gbs"],
                    "frac_of_measured_peak": serial["gbs"] / world / peak,
                    "frac_of_nominal_8tbs": serial["gbs"] / world / NOMINAL_HBM_GBS,
-                   "outputs_identical_to_overlapped": t["serial_identical"],
+                   "sequences_differing_from_overlapped": t["serial_differing"],
                    "how": HOW_SERIAL},
         "eager_rows_per_s": world * rows_per_step * args.steps / (eager_ms / 1e3),
     }
@@ -508,7 +513,7 @@ def run_ours(args, rank, world, device):
     result["e2e"] = run_e2e(args, sets, device, stream, world, rank)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base, check = oracle_leg(sets, t["out_tok"], t["out_n"], args.warmup, args.steps,
-                                 args.cpu_seconds, rank)
+                                 args.cpu_seconds, rank, serial=(t["serial_tok"], t["serial_n"]))
         result["cpu_baseline"] = base
         result["parity"] = check
     if rank == 0 and not args.no_extra and world == 1:
@@ -599,19 +604,27 @@ def run_e2e(args, sets, device, stream, world, rank=0):
     torch.cuda.synchronize()
     ms = replay_ms(g, stream)  # the first replay loads the graph
     ms = max_over_ranks(replay_ms(g, stream, "timed: e2e"), device, world)
-    value = world * B * K1 * args.steps / (ms / 1e3)
-    return {"value": value, "unit": "rows/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
-            "h2d_gbs": h2d * args.steps / (ms / 1e3) / 1e9,
-            "eager_one_stream": {"value": world * B * K1 * args.steps / (eager_ms / 1e3),
-                                 "ms_per_step": eager_ms / args.steps},
-            "how": "every step: its inputs copied from pinned host memory into one of two "
-                   "device buffers on a copy stream, spec_verify_ex, its results copied back "
-                   "to pinned host memory; the K steps replayed from one CUDA graph (step "
-                   "i+1's copy overlaps step i's verify); CUDA events around the replay"}
+    rows = world * B * K1 * args.steps
+    pipelined = {"value": rows / (ms / 1e3), "ms_per_step": ms / args.steps,
+                 "how": "the K steps replayed from one CUDA graph: each step's inputs copied "
+                        "from pinned host memory into one of two device buffers on a copy "
+                        "stream (step i+1's copy overlaps step i's verify), spec_verify_ex, "
+                        "its results copied back to pinned host memory"}
+    eager = {"value": rows / (eager_ms / 1e3), "ms_per_step": eager_ms / args.steps,
+             "how": "the K steps launched eagerly on one stream: copy in, spec_verify_ex, "
+                    "copy out, step after step"}
+    best = "pipelined_graph" if pipelined["value"] >= eager["value"] else "eager_one_stream"
+    best_ms = ms if best == "pipelined_graph" else eager_ms
+    return {"value": max(pipelined["value"], eager["value"]), "unit": "rows/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbs": h2d * args.steps / (best_ms / 1e3) / 1e9,
+            "method": best, "pipelined_graph": pipelined, "eager_one_stream": eager,
+            "how": "every step copies its inputs from pinned host memory and its results "
+                   "back, through the public API (spec_verify_ex); CUDA events around the K "
+                   "steps; value is the faster of the two methods below"}
 
 
-def oracle_leg(sets, out_tok, out_n, first, count, seconds, rank=0, target_of=None):
+def oracle_leg(sets, out_tok, out_n, first, count, seconds, rank=0, target_of=None, serial=None):
     """The cpu_baseline leg: the oracle as it stands, timed on the host cores
     (threads over sequences) on the timed steps of the GPU run, in order and
     with the same seeds and sequence ids, until about `seconds` of oracle
@@ -630,6 +643,8 @@ def oracle_leg(sets, out_tok, out_n, first, count, seconds, rank=0, target_of=No
     host = {}
     tok_all = out_tok.cpu().numpy()
     n_all = out_n.cpu().numpy()
+    ser = None if serial is None else (serial[0].cpu().numpy(), serial[1].cpu().numpy())
+    ser_tot = {"sequences": 0, "near_tie_mismatches": 0, "mismatches": 0}
     rows = calls = used = 0
     el = 0.0
     tot = {"steps_checked": 0, "sequences": 0, "exact": 0, "accept_near_ties": 0, "draw_near_ties": 0,
@@ -664,6 +679,10 @@ def oracle_leg(sets, out_tok, out_n, first, count, seconds, rank=0, target_of=No
         tot["near_tie_mismatches"] += cmp["near_tie_mismatches"]
         tot["mismatches"] += cmp["mismatches"]
         tot["exact"] += cmp["sequences"] - cmp["near_tie_mismatches"] - cmp["mismatches"]
+        if ser is not None:
+            sc = par.compare(ser[0][i], ser[1][i], ref, ties=acc_tie | draw_tie)
+            for key in ser_tot:
+                ser_tot[key] += sc[key]
         first_bad += [dict(step=i, **m) for m in cmp["first_mismatches"]][:3 - len(first_bad)]
     base = {"value": rows / el if el > 0 else None, "unit": "rows/s", "cores": used, "kind": "oracle",
             "sample": f"the first {calls} timed steps ({rows} rows), same inputs, seeds and sequence "
@@ -674,6 +693,9 @@ def oracle_leg(sets, out_tok, out_n, first, count, seconds, rank=0, target_of=No
                             "cumulative interval (probability units)"}
     tot["how"] = ("the oracle (double precision, own Philox) on the GPU's timed steps; tokens and "
                   "accept counts compared exactly outside the near-tie bands")
+    if ser is not None:
+        tot["serial_run"] = dict(ser_tot, how="the one-call-at-a-time run's outputs for the same steps, "
+                                               "against the same oracle outputs")
     if first_bad:
         tot["first_mismatches"] = first_bad
     return base, tot
@@ -727,13 +749,14 @@ def other_workloads(args, device, l2, stream):
                                     "rows_per_s": B * K1 * steps / (serial_ms / 1e3),
                                     "frac_of_measured_peak": ba / (serial_ms / 1e3) / 1e9 / peak,
                                     "frac_of_nominal_8tbs": ba / (serial_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-                                    "outputs_identical_to_overlapped": t["serial_identical"],
+                                    "sequences_differing_from_overlapped": t["serial_differing"],
                                     "how": HOW_SERIAL},
                          "acceptance": acceptance(name, n_all, args.warmup, steps, len(sets), K1 - 1),
                          "input_sets": len(sets)}
             if not args.no_cpu_baseline:
                 out[name]["cpu_baseline"], out[name]["parity"] = oracle_leg(
-                    sets, t["out_tok"], t["out_n"], args.warmup, steps, SUB_ORACLE_SECONDS)
+                    sets, t["out_tok"], t["out_n"], args.warmup, steps, SUB_ORACLE_SECONDS,
+                    serial=(t["serial_tok"], t["serial_n"]))
             del sets, t
             torch.cuda.empty_cache()
         except Exception as e:  # report, do not hide

@@ -90,8 +90,13 @@ typedef enum {
     SV_FLAG_TIMEOUT = 32u,         /* a bounded wait inside the kernel gave up; the
                                       sequence is reported invalid                 */
     SV_FLAG_BAD_LENGTH = 64u,      /* a per-sequence draft length outside [0, K]   */
-    SV_FLAG_BAD_TREE = 128u        /* a tree node whose parent is not an earlier
+    SV_FLAG_BAD_TREE = 128u,       /* a tree node whose parent is not an earlier
                                       node                                         */
+    SV_FLAG_DEBUG_BOUNDS = 256u    /* debug builds only (libspecverify_debug.so,
+                                      compiled with SPECVERIFY_DEBUG): the verify
+                                      kernel was about to access global memory
+                                      outside every buffer of the call; it skipped
+                                      that access instead                          */
 } sv_device_flag;
 
 /* Batched verify over logits already in device memory.
@@ -176,6 +181,13 @@ typedef struct {
  * gives up as a real stalled copy would, and the call reports
  * SV_FLAG_TIMEOUT and marks every sequence invalid, without faulting. */
 #define SV_ARG_TEST_WAIT_TIMEOUT 0x80000000u
+
+/* sv_verify_args.flags, for tests of the debug build only: its bounds checks
+ * take the target logits to end halfway through the buffer, so that every
+ * access of the upper half counts as out of bounds (and is skipped, setting
+ * SV_FLAG_DEBUG_BOUNDS). No access leaves the real buffer. Release builds
+ * ignore the flag. */
+#define SV_ARG_TEST_DEBUG_SHRINK 0x40000000u
 
 /* spec_verify with per-sequence modes, explicit sequence ids and optional
  * probability outputs. Same conventions and errors as spec_verify. */

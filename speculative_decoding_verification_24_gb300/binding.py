@@ -16,6 +16,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+DEBUG_LIB_PATH = os.path.join(_PKG, "libspecverify_debug.so")
 
 SV_F32, SV_BF16 = 0, 1
 SV_GREEDY, SV_SAMPLE = 0, 1
@@ -28,8 +29,10 @@ SV_FLAG_BAD_MODE = 16
 SV_FLAG_TIMEOUT = 32
 SV_FLAG_BAD_LENGTH = 64
 SV_FLAG_BAD_TREE = 128
+SV_FLAG_DEBUG_BOUNDS = 256
 SV_ARG_OVERLAP_PREVIOUS = 1
 SV_ARG_TEST_WAIT_TIMEOUT = 0x80000000
+SV_ARG_TEST_DEBUG_SHRINK = 0x40000000
 SV_ERR_SCRATCH_LIMIT = 12
 SV_LMHEAD_SCRATCH_BYTES = 32 << 20  # include/specverify.h
 
@@ -103,23 +106,30 @@ SIGNATURES = [
 ]
 
 
+def load_library(path: str):
+    """Load one build of the library (release or debug) and declare the
+    signatures of every symbol the header declares; fail loudly when it has
+    not been built."""
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (there is no fallback)")
+    lib = ctypes.CDLL(path)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if lib.sv_verify_args_size() != ctypes.sizeof(sv_verify_args):
+        raise ImportError("sv_verify_args layout differs between the binding and the library")
+    return lib
+
+
 def _load():
-    """Load the in-tree library; fail loudly when it has not been built."""
+    """The in-tree release library, loaded once."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise ImportError(
-                    f"{LIB_PATH} is missing: build it with "
-                    "`python -c 'import __graft_entry__ as g; g.build()'` (there is no fallback)")
-            lib = ctypes.CDLL(LIB_PATH)
-            for name, res, args in SIGNATURES:
-                fn = getattr(lib, name)
-                fn.restype = res
-                fn.argtypes = args
-            if lib.sv_verify_args_size() != ctypes.sizeof(sv_verify_args):
-                raise ImportError("sv_verify_args layout differs between the binding and the library")
-            _lib = lib
+            _lib = load_library(LIB_PATH)
     return _lib
 
 
@@ -198,13 +208,15 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
                    seed=0, seq_ids=None, out_tokens=None, out_n_accepted=None, out_p_target=None,
                    out_p_draft=None, out_residual_mass=None, status_word=None, cluster_size=0,
                    stream=None, debug=False, overlap_previous=False, draft_lens=None, flags=0,
-                   out_draw_edges=None):
+                   out_draw_edges=None, lib=None):
     """Verify with per-sequence modes ([B] int32 tensor, or 'greedy'/'sample'
     for all), explicit Philox sequence ids and optional debug outputs.
     debug=True allocates out_p_target, out_p_draft, out_residual_mass,
     out_draw_edges and status_word. overlap_previous=True sets SV_ARG_OVERLAP_PREVIOUS (the
     inputs are not written by the work just before this call on the stream).
     draft_lens: optional [B] int32 device tensor of per-sequence draft counts.
+    lib: a handle from load_library() to call another build of the library
+    (the debug build); the release library by default.
     Returns a dict of the output tensors."""
     B, K1, V = target_logits.shape
     K = K1 - 1
@@ -251,7 +263,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     a.out_draw_edges = _ptr(out_draw_edges)
     with torch.cuda.device(dev):
         a.stream = _stream(stream, dev)
-        st = _load().spec_verify_ex(ctypes.byref(a))
+        st = (lib or _load()).spec_verify_ex(ctypes.byref(a))
     _check(st, "spec_verify_ex")
     return {"tokens": out_tokens, "n_accepted": out_n_accepted, "p_target": out_p_target,
             "p_draft": out_p_draft, "residual_mass": out_residual_mass,
@@ -332,8 +344,10 @@ def spec_verify_lmhead_workspace_bytes(B: int, K: int, d: int, V: int) -> int:
 
 
 def spec_verify_lmhead(hidden, W, draft_logits, draft_tokens, temperature=1.0, mode="sample",
-                       seed=0, workspace=None, out_tokens=None, out_n_accepted=None, stream=None):
-    """Fused LM head + verify: hidden [B, K+1, d] bf16, W [d, V] bf16."""
+                       seed=0, workspace=None, out_tokens=None, out_n_accepted=None, stream=None,
+                       lib=None):
+    """Fused LM head + verify: hidden [B, K+1, d] bf16, W [d, V] bf16. lib: as
+    in spec_verify_ex."""
     B, K1, d = hidden.shape
     K = K1 - 1
     V = W.shape[1]
@@ -347,7 +361,7 @@ def spec_verify_lmhead(hidden, W, draft_logits, draft_tokens, temperature=1.0, m
         out_n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
     ddt = _dtype_code(draft_logits) if draft_logits is not None else SV_BF16
     with torch.cuda.device(dev):
-        st = _load().spec_verify_lmhead(
+        st = (lib or _load()).spec_verify_lmhead(
             _ptr(hidden), _ptr(W), _ptr(draft_logits), _ptr(draft_tokens), B, K, d, V, ddt,
             float(temperature), _mode_code(mode), ctypes.c_uint64(int(seed) & (2**64 - 1)),
             _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out_tokens),

@@ -139,6 +139,9 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     p.status_word = a->status_word;
     p.overlap_previous = (a->flags & SV_ARG_OVERLAP_PREVIOUS) != 0;
     p.test_wait_timeout = (a->flags & SV_ARG_TEST_WAIT_TIMEOUT) != 0;
+    p.test_debug_shrink = (a->flags & SV_ARG_TEST_DEBUG_SHRINK) != 0;
+    p.es_t = (int)es_t;
+    p.es_d = (int)es_d;
     p.draft_lens = a->draft_lens;
     p.target_parts = target_parts;
     p.part_tiles = part_tiles;
@@ -234,6 +237,7 @@ extern "C" sv_status spec_verify_tree(const void* target_logits, sv_dtype dtype,
     p.out_n_accepted = out_n_accepted;
     p.tree_parents = tree_parents;
     p.out_last_node = out_last_node;
+    p.es_t = p.es_d = esize_of(dtype);
     cudaError_t e = sv::launch_verify_logits(p, (int)dtype, (int)dtype, cs, (cudaStream_t)stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return SV_OK;

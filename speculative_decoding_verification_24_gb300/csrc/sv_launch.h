@@ -33,6 +33,8 @@ struct VerifyParams {
     const int32_t* tree_parents;
     int32_t* out_last_node;    // [B] or nullptr (tree mode)
     int test_wait_timeout;     // tests of the failure path: a bounded wait that gives up
+    int es_t, es_d;            // element sizes of the target and draft rows (debug build's checks)
+    int test_debug_shrink;     // debug build's tests: the target's checked extent is halved
     // LM-head path: the target rows' statistics come as partials from the
     // GEMM epilogue, one per row and GEMM CTA (parts[cta * part_M + b * (K+1)
     // + i], part_tiles CTAs), written by the grid launched just before this

@@ -56,6 +56,81 @@ constexpr int MAX_K = 31;
 constexpr int MAX_ROWS = 2 * MAX_K + 1;
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
+// ---------------------------------------------------------------------------
+// Debug builds (SPECVERIFY_DEBUG, built as libspecverify_debug.so): every
+// global load and store of this kernel is first checked against the buffers
+// of the call. A load must fall inside one of the inputs (logits, tokens,
+// modes, draft counts, sequence ids, tree parents, LM-head partials), a
+// store inside one of the outputs; the extents come from B, K, V and the
+// element sizes. An access that does not is skipped (a load keeps its fill
+// value; a bulk copy is not issued, and its stage completes empty) and sets
+// SV_FLAG_DEBUG_BOUNDS in the status word. Nothing traps. Release builds
+// compile every check away.
+// ---------------------------------------------------------------------------
+#ifdef SPECVERIFY_DEBUG
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+__device__ __forceinline__ bool dbg_within(const void* a, size_t bytes, const void* base, size_t extent) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), lo = reinterpret_cast<uintptr_t>(base);
+    return base != nullptr && x >= lo && bytes <= extent && x - lo <= extent - bytes;
+}
+
+__device__ __noinline__ bool dbg_load_ok(const VerifyParams& p, const void* a, size_t bytes) {
+    const size_t B = (size_t)p.B, K1 = (size_t)p.K + 1, V = (size_t)p.V;
+    const size_t tgt = B * K1 * V * (size_t)p.es_t;
+    const bool ok = dbg_within(a, bytes, p.target, p.test_debug_shrink ? tgt / 2 : tgt) ||
+                    dbg_within(a, bytes, p.draft, B * (K1 - 1) * V * (size_t)p.es_d) ||
+                    dbg_within(a, bytes, p.tokens, B * K1 * 4) ||  // [B, K]; [B, K+1] for trees
+                    dbg_within(a, bytes, p.modes, B * 4) || dbg_within(a, bytes, p.draft_lens, B * 4) ||
+                    dbg_within(a, bytes, p.seq_ids, B * 8) || dbg_within(a, bytes, p.tree_parents, B * K1 * 4) ||
+                    dbg_within(a, bytes, p.target_parts, (size_t)p.part_tiles * (size_t)p.part_M * 8) ||
+                    dbg_within(a, bytes, p.draft_parts, (size_t)p.part_tiles * B * (K1 - 1) * 8);
+    if (!ok && p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_DEBUG_BOUNDS);
+    return ok;
+}
+
+__device__ __noinline__ bool dbg_store_ok(const VerifyParams& p, const void* a, size_t bytes) {
+    const size_t B = (size_t)p.B, K1 = (size_t)p.K + 1;
+    const bool ok = dbg_within(a, bytes, p.out_tokens, B * K1 * 4) || dbg_within(a, bytes, p.out_n_accepted, B * 4) ||
+                    dbg_within(a, bytes, p.out_p_target, B * (K1 - 1) * 4) ||
+                    dbg_within(a, bytes, p.out_p_draft, B * (K1 - 1) * 4) ||
+                    dbg_within(a, bytes, p.out_residual_mass, B * 4) ||
+                    dbg_within(a, bytes, p.out_draw_edges, B * 8) || dbg_within(a, bytes, p.out_last_node, B * 4);
+    if (!ok && p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_DEBUG_BOUNDS);
+    return ok;
+}
+
+__device__ __forceinline__ bool load_ok(const VerifyParams& p, const void* a, size_t bytes) {
+    if constexpr (kDebugBounds) return dbg_load_ok(p, a, bytes);
+    return true;
+}
+
+// __ldg(a), or `fill` when a debug build finds `a` outside every input
+template <typename T>
+__device__ __forceinline__ T ld_in(const VerifyParams& p, const T* a, T fill) {
+    if (!load_ok(p, a, sizeof(T))) return fill;
+    return __ldg(a);
+}
+
+// __ldcg(a) (cached in L2 only: data another grid wrote), or `fill` as ld_in
+template <typename T>
+__device__ __forceinline__ T ldcg_in(const VerifyParams& p, const T* a, T fill) {
+    if (!load_ok(p, a, sizeof(T))) return fill;
+    return __ldcg(a);
+}
+
+// *a = v, skipped when a debug build finds `a` outside every output
+template <typename T>
+__device__ __forceinline__ void st_out(const VerifyParams& p, T* a, T v) {
+    if constexpr (kDebugBounds) {
+        if (!dbg_store_ok(p, a, sizeof(T))) return;
+    }
+    *a = v;
+}
+
 template <typename T>
 struct Elem;
 template <>
@@ -102,14 +177,14 @@ __device__ __forceinline__ float elem_rt(const uint4& d, int e) {
 }
 
 template <typename T>
-__device__ __forceinline__ float load_logit(const T* row, int i);
+__device__ __forceinline__ float load_logit(const VerifyParams& p, const T* row, int i);
 template <>
-__device__ __forceinline__ float load_logit<float>(const float* row, int i) {
-    return __ldg(row + i);
+__device__ __forceinline__ float load_logit<float>(const VerifyParams& p, const float* row, int i) {
+    return ld_in(p, row + i, 0.0f);
 }
 template <>
-__device__ __forceinline__ float load_logit<__nv_bfloat16>(const __nv_bfloat16* row, int i) {
-    const unsigned short bits = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+__device__ __forceinline__ float load_logit<__nv_bfloat16>(const VerifyParams& p, const __nv_bfloat16* row, int i) {
+    const unsigned short bits = ld_in(p, reinterpret_cast<const unsigned short*>(row) + i, (unsigned short)0);
     return __uint_as_float((uint32_t)bits << 16);
 }
 
@@ -135,7 +210,7 @@ __device__ __forceinline__ RowGeom row_geom(const T* row, int V) {
 // Slot of row elements starting at element index i0 (which may be negative or
 // run past V): elements outside [0, V) read as -inf.
 template <typename T>
-__device__ __forceinline__ uint4 load_partial_slot(const T* row, int V, int i0) {
+__device__ __forceinline__ uint4 load_partial_slot(const VerifyParams& p, const T* row, int V, int i0) {
     constexpr int E = Elem<T>::E;
     uint32_t w[4] = {Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF};
 #pragma unroll
@@ -143,9 +218,9 @@ __device__ __forceinline__ uint4 load_partial_slot(const T* row, int V, int i0) 
         const int i = i0 + e;
         if (i < 0 || i >= V) continue;
         if constexpr (sizeof(T) == 4) {
-            w[e] = __ldg(reinterpret_cast<const uint32_t*>(row) + i);
+            w[e] = ld_in(p, reinterpret_cast<const uint32_t*>(row) + i, Elem<T>::NEG_INF);
         } else {
-            const uint32_t bits = __ldg(reinterpret_cast<const unsigned short*>(row) + i);
+            const uint32_t bits = ld_in(p, reinterpret_cast<const unsigned short*>(row) + i, (unsigned short)0xFF80u);
             const int k = e >> 1, sh = (e & 1) * 16;
             w[k] = (w[k] & ~(0xFFFFu << sh)) | (bits << sh);
         }
@@ -160,17 +235,17 @@ __device__ __forceinline__ bool slot_full(const RowGeom& g, int V, int q) {
     return i0 >= 0 && i0 + E <= V;
 }
 
-// Any slot of a row, full or partial.
-template <typename T>
-__device__ __forceinline__ uint4 load_slot(const RowGeom& g, const T* row, int V, int q) {
-    constexpr int E = Elem<T>::E;
-    if (slot_full<T>(g, V, q)) return ld_stream(g.base + q);
-    return load_partial_slot<T>(row, V, q * E - g.head);
-}
-
 template <typename T>
 __device__ __forceinline__ uint4 neg_inf_slot() {
     return make_uint4(Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF, Elem<T>::NEG_INF);
+}
+
+// Any slot of a row, full or partial.
+template <typename T>
+__device__ __forceinline__ uint4 load_slot(const VerifyParams& p, const RowGeom& g, const T* row, int V, int q) {
+    constexpr int E = Elem<T>::E;
+    if (slot_full<T>(g, V, q)) return load_ok(p, g.base + q, 16) ? ld_stream(g.base + q) : neg_inf_slot<T>();
+    return load_partial_slot<T>(p, row, V, q * E - g.head);
 }
 
 // Contiguous split of [0, n) into G parts; part g is [lo, hi). The host keeps
@@ -423,9 +498,9 @@ __device__ __forceinline__ const TD* draft_row(const TD* drf, int b, int K, int 
 // format of TT (elements outside [0, V) read as -inf). The mixed case widens
 // bf16 draft elements exactly into fp32 words.
 template <typename TT, typename TD>
-__device__ __forceinline__ uint4 load_elems_as(const TD* row, int V, int i0) {
+__device__ __forceinline__ uint4 load_elems_as(const VerifyParams& p, const TD* row, int V, int i0) {
     if constexpr (std::is_same<TT, TD>::value) {
-        return load_partial_slot<TT>(row, V, i0);
+        return load_partial_slot<TT>(p, row, V, i0);
     } else {
         static_assert(sizeof(TT) == 4 && sizeof(TD) == 2, "mixed rows: fp32 target, bf16 draft");
         uint32_t w[4];
@@ -433,7 +508,7 @@ __device__ __forceinline__ uint4 load_elems_as(const TD* row, int V, int i0) {
         for (int e = 0; e < 4; ++e) {
             const int i = i0 + e;
             w[e] = (i >= 0 && i < V)
-                       ? ((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(row) + i) << 16)
+                       ? ((uint32_t)ld_in(p, reinterpret_cast<const unsigned short*>(row) + i, (unsigned short)0xFF80u) << 16)
                        : 0xFF800000u;
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
@@ -506,18 +581,18 @@ struct DrawSrc {
 // Target slot q (target geometry) and the draft elements with the same
 // indices, from global memory; q < 0 gives empty slots.
 template <typename TT, typename TD>
-__device__ __forceinline__ void load_draw_slot(const DrawSrc<TT, TD>& src, bool use_d, int q, uint4& dt,
-                                               uint4& dd) {
+__device__ __forceinline__ void load_draw_slot(const VerifyParams& p, const DrawSrc<TT, TD>& src, bool use_d, int q,
+                                               uint4& dt, uint4& dd) {
     constexpr int E = Elem<TT>::E;
     if (q < 0) {
         dt = neg_inf_slot<TT>();
         dd = neg_inf_slot<TT>();
         return;
     }
-    dt = load_slot<TT>(src.gt, src.trow, src.V, q);
+    dt = load_slot<TT>(p, src.gt, src.trow, src.V, q);
     if (!use_d) dd = neg_inf_slot<TT>();
-    else if (src.same_slots) dd = load_slot<TT>(src.gd, reinterpret_cast<const TT*>(src.drow), src.V, q);
-    else dd = load_elems_as<TT, TD>(src.drow, src.V, q * E - src.gt.head);
+    else if (src.same_slots) dd = load_slot<TT>(p, src.gd, reinterpret_cast<const TT*>(src.drow), src.V, q);
+    else dd = load_elems_as<TT, TD>(p, src.drow, src.V, q * E - src.gt.head);
 }
 
 // One 32-slot step of the final search, for the warp that owns it: lane l
@@ -533,12 +608,12 @@ struct DrawStep {
     int last_pos;      // the warp's last element with positive mass (-1: none)
     int i0;            // row element index of this lane's first element
 
-    __device__ __forceinline__ void load(const DrawSrc<TT, TD>& src, const DrawRows& w, int q_begin,
-                                         int n, int step, int lane) {
+    __device__ __forceinline__ void load(const VerifyParams& p, const DrawSrc<TT, TD>& src, const DrawRows& w,
+                                         int q_begin, int n, int step, int lane) {
         const int i = step * 32 + lane;
         const int q = i < n ? q_begin + i : -1;
         uint4 dt, dd;
-        load_draw_slot<TT, TD>(src, w.use_d, q, dt, dd);
+        load_draw_slot<TT, TD>(p, src, w.use_d, q, dt, dd);
         i0 = q * E - src.gt.head;
         float ls = 0.0f;
         int lp = -1;
@@ -653,7 +728,7 @@ static_assert(2 * (RING_BYTES + sizeof(SeqShared) + 1024) <= 228 * 1024,
 __device__ __forceinline__ void tree_decide(const VerifyParams& p, SeqShared& sh, int b, int N, int V,
                                             int lane, int rank, bool mode_ok, int x_reg) {
     const bool node = lane < N && N <= 32;
-    const int par = (lane > 0 && node) ? __ldg(p.tree_parents + (size_t)b * N + lane) : -1;
+    const int par = (lane > 0 && node) ? ld_in(p, p.tree_parents + (size_t)b * N + lane, -1) : -1;
     bool bad_row = false;
     if (node) {
         const ArgPart ap = as_arg(sh.merged[lane]);
@@ -697,15 +772,15 @@ __device__ __forceinline__ void tree_decide(const VerifyParams& p, SeqShared& sh
         for (int k = min(n, N) - 1; k >= 0; --k) {  // the path, from its last node up to the root
             const int tok = __shfl_sync(FULL, x_reg, cur & 31);
             const int up = __shfl_sync(FULL, par, cur & 31);
-            if (lane == 0) out[k] = tok;
+            if (lane == 0) st_out(p, out + k, tok);
             cur = up < 0 ? 0 : up;
         }
     }
     if (node && (invalid || lane >= n))
-        out[lane] = (!invalid && lane == n && last >= 0 && last < N) ? as_arg(sh.merged[last]).i : -1;
+        st_out(p, out + lane, (!invalid && lane == n && last >= 0 && last < N) ? as_arg(sh.merged[last]).i : -1);
     if (lane == 0) {
-        p.out_n_accepted[b] = n;
-        if (p.out_last_node) p.out_last_node[b] = last;
+        st_out(p, p.out_n_accepted + (b), n);
+        if (p.out_last_node) st_out(p, p.out_last_node + (b), last);
         if (p.status_word && invalid)
             atomicOr(p.status_word, any_bad_link    ? (unsigned)SV_FLAG_BAD_TREE
                                     : any_bad_token ? (unsigned)SV_FLAG_BAD_TOKEN
@@ -865,14 +940,16 @@ __device__ __forceinline__ void seek_row(RowCursor& rc, const RowInfo* rows, int
 
 // Issues the bulk copy of pass-1 chunk `chunk` (one piece of one row) as fill
 // `fseq` of the warp; lane 0 issues.
-__device__ __forceinline__ void fill_pass1(SeqShared& sh, WarpRing& wr, char* ring, uint32_t fseq, int chunk,
-                                           RowCursor& rc, int lane) {
+__device__ __forceinline__ void fill_pass1(const VerifyParams& p, SeqShared& sh, WarpRing& wr, char* ring,
+                                           uint32_t fseq, int chunk, RowCursor& rc, int lane) {
     seek_row(rc, sh.rows, chunk);
     const RowInfo& ri = sh.rows[rc.r];
     const int q0 = ri.ia + (chunk - rc.c0) * STAGE_SLOTS;
     const int n = min(STAGE_SLOTS, ri.ib - q0);
-    wr.begin_fill(sh, fseq, (uint32_t)n * 16u, lane);
-    if (lane == 0)
+    // (a debug build that finds the copy out of bounds completes the stage empty)
+    const bool ok = lane != 0 || load_ok(p, ri.base + q0, (size_t)n * 16u);
+    wr.begin_fill(sh, fseq, ok ? (uint32_t)n * 16u : 0u, lane);
+    if (lane == 0 && ok)
         bulk_g2s_hint(wr.stage(ring, fseq), ri.base + q0, (uint32_t)n * 16u, wr.bar(sh, fseq), l2_evict_first_policy());
 }
 
@@ -932,14 +1009,14 @@ __device__ __forceinline__ void capture_edge_logit(SeqShared& sh, cg::cluster_gr
 // Pass 1 of one warp: chunks warp, warp + NCW, ... of the schedule, buffered
 // in the warp's NBUF stages. Writes one partial per row it saw.
 template <typename TT, typename TD, bool SAMPLE, typename WhileWaiting>
-__device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* ring, int nchunks,
+__device__ __forceinline__ void stream_pass1(const VerifyParams& p, SeqShared& sh, WarpRing& wr, char* ring, int nchunks,
                                              float c, int warp, int lane, uint32_t& seq,
                                              cg::cluster_group& cluster, int CS, int K, int x_reg,
                                              WhileWaiting&& while_waiting) {
     RowCursor fill_rc{-1, 0, 0}, rc{-1, 0, 0};
     for (int j = 0; j < NBUF; ++j) {
         const int chunk = warp + NCW * j;
-        if (chunk < nchunks) fill_pass1(sh, wr, ring, seq + j, chunk, fill_rc, lane);
+        if (chunk < nchunks) fill_pass1(p, sh, wr, ring, seq + j, chunk, fill_rc, lane);
     }
     while_waiting();  // work that fits in the first copies' latency
     int cur_row = -1, ia = 0, ib = 0, head = 0;
@@ -990,7 +1067,7 @@ __device__ __forceinline__ void stream_pass1(SeqShared& sh, WarpRing& wr, char* 
         fence_proxy_async_smem();
         __syncwarp();
         if (chunk + NBUF * NCW < nchunks)
-            fill_pass1(sh, wr, ring, seq + NBUF, chunk + NBUF * NCW, fill_rc, lane);
+            fill_pass1(p, sh, wr, ring, seq + NBUF, chunk + NBUF * NCW, fill_rc, lane);
         if (std::is_same<TT, TD>::value || cur_row <= K) reduce_chunk<TT, SAMPLE>(sa, aa, d, n, q0, c, lane);
         else reduce_chunk<TD, SAMPLE>(sa, aa, d, n, q0, c, lane);
     }
@@ -1036,18 +1113,24 @@ __device__ __forceinline__ uint4 span_slot(const char* span, uint32_t off, int i
 // the target's alignment, or the draft's span of them when the draft is bf16
 // under an fp32 target) as fill `fseq` of the warp.
 template <typename TT, typename TD>
-__device__ __forceinline__ void fill_pass2(SeqShared& sh, WarpRing& wr, char* ring, uint32_t fseq,
-                                           const DrawSrc<TT, TD>& src, int ia, int ib, int ci, bool ring_d,
-                                           bool span_d, int lane) {
+__device__ __forceinline__ void fill_pass2(const VerifyParams& p, SeqShared& sh, WarpRing& wr, char* ring,
+                                           uint32_t fseq, const DrawSrc<TT, TD>& src, int ia, int ib, int ci,
+                                           bool ring_d, bool span_d, int lane) {
     const int q = ia + ci * P2_SLOTS;
     const int n = min(P2_SLOTS, ib - q);
     const DraftSpan ds = span_d ? draft_span<TT, TD>(src, q, n) : DraftSpan{nullptr, 0u, 0u};
-    wr.begin_fill(sh, fseq, (uint32_t)n * 16u * (ring_d ? 2u : 1u) + ds.bytes, lane);
+    // (a debug build issues only the copies it finds in bounds, and expects their bytes)
+    const bool ok_t = lane != 0 || load_ok(p, src.gt.base + q, (size_t)n * 16u);
+    const bool ok_d = !ring_d || lane != 0 || load_ok(p, src.gd.base + q, (size_t)n * 16u);
+    const bool ok_s = !span_d || lane != 0 || load_ok(p, ds.base, ds.bytes);
+    wr.begin_fill(sh, fseq,
+                  (ok_t ? (uint32_t)n * 16u : 0u) + (ring_d && ok_d ? (uint32_t)n * 16u : 0u) + (ok_s ? ds.bytes : 0u),
+                  lane);
     if (lane == 0) {
         char* stage = wr.stage(ring, fseq);
-        bulk_g2s(stage, src.gt.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
-        if (ring_d) bulk_g2s(stage + P2_DRAFT_OFF, src.gd.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
-        if (span_d) bulk_g2s(stage + P2_DRAFT_OFF, ds.base, ds.bytes, wr.bar(sh, fseq));
+        if (ok_t) bulk_g2s(stage, src.gt.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
+        if (ring_d && ok_d) bulk_g2s(stage + P2_DRAFT_OFF, src.gd.base + q, (uint32_t)n * 16u, wr.bar(sh, fseq));
+        if (span_d && ok_s) bulk_g2s(stage + P2_DRAFT_OFF, ds.base, ds.bytes, wr.bar(sh, fseq));
     }
 }
 
@@ -1055,14 +1138,14 @@ __device__ __forceinline__ void fill_pass2(SeqShared& sh, WarpRing& wr, char* ri
 // One partial edge slot per lane (lane 0: the low end, lane 1: the high end of
 // this CTA's slice of row r), reduced like the chunks.
 template <typename T, bool SAMPLE>
-__device__ __forceinline__ float2 edge_row(SeqShared& sh, const T* row, const RowInfo& ri, int r,
+__device__ __forceinline__ float2 edge_row(const VerifyParams& p, SeqShared& sh, const T* row, const RowInfo& ri, int r,
                                            int K, int V, float c, int lane, cg::cluster_group& cluster,
                                            int CS, int x_reg) {
     const RowGeom g{ri.base, ri.head, 0};
     uint4 d[1];
     int qs[1];
     qs[0] = lane == 0 ? ri.edge_lo : lane == 1 ? ri.edge_hi : -1;
-    d[0] = qs[0] >= 0 ? load_slot<T>(g, row, V, qs[0]) : neg_inf_slot<T>();
+    d[0] = qs[0] >= 0 ? load_slot<T>(p, g, row, V, qs[0]) : neg_inf_slot<T>();
     if (SAMPLE) {
         capture_edge_logit<T>(sh, cluster, CS, d[0], qs[0], r, K, x_reg, ri.head, lane);
         SoftAcc ea = soft_acc_empty();
@@ -1085,7 +1168,7 @@ __device__ __forceinline__ float2 edge_row(SeqShared& sh, const T* row, const Ro
 
 // Partial slots at the two ends of this CTA's slices (warp 0).
 template <typename TT, typename TD, bool SAMPLE>
-__device__ __forceinline__ void edge_pass1(SeqShared& sh, const TT* tgt, const TD* drf, int b, int K,
+__device__ __forceinline__ void edge_pass1(const VerifyParams& p, SeqShared& sh, const TT* tgt, const TD* drf, int b, int K,
                                            int Kb, int V, int nrows, float c, int lane,
                                            cg::cluster_group& cluster, int CS, int x_reg) {
     for (int r = 0; r < nrows; ++r) {
@@ -1094,9 +1177,9 @@ __device__ __forceinline__ void edge_pass1(SeqShared& sh, const TT* tgt, const T
         if (ri.edge_lo < 0 && ri.edge_hi < 0) {
             part = SAMPLE ? pack(SoftPart{-INFINITY, 0.0f}) : pack(ArgPart{-INFINITY, INT_MAX});
         } else if (r <= Kb) {
-            part = edge_row<TT, SAMPLE>(sh, target_row(tgt, b, K, V, r), ri, r, Kb, V, c, lane, cluster, CS, x_reg);
+            part = edge_row<TT, SAMPLE>(p, sh, target_row(tgt, b, K, V, r), ri, r, Kb, V, c, lane, cluster, CS, x_reg);
         } else {
-            part = edge_row<TD, SAMPLE>(sh, draft_row(drf, b, K, V, r - Kb - 1), ri, r, Kb, V, c, lane, cluster,
+            part = edge_row<TD, SAMPLE>(p, sh, draft_row(drf, b, K, V, r - Kb - 1), ri, r, Kb, V, c, lane, cluster,
                                         CS, x_reg);
         }
         if (lane == 0) sh.edge_part[r] = part;
@@ -1148,7 +1231,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 #pragma unroll
             for (int k = 0; k < PER; ++k) {
                 const int i = k * 32 + lane;
-                const bool s = i < p.B && __ldg(p.modes + i) == 1;
+                const bool s = i < p.B && ld_in(p, p.modes + i, 0) == 1;
                 smask[k] = __ballot_sync(FULL, s);
                 ns += __popc(smask[k]);
             }
@@ -1177,9 +1260,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // With overlap, the whole call may run alongside the work ahead of it,
     // and each thread that stores to global memory first waits for that work
     // to complete, just before its stores.
-    const int mode = p.modes ? __ldg(p.modes + b) : p.mode;
+    const int mode = p.modes ? ld_in(p, p.modes + b, -1) : p.mode;
     // Kb: the drafts this sequence verifies (continuous batching), 0..K
-    const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
+    const int Kb = p.draft_lens ? ld_in(p, p.draft_lens + b, -1) : K;
     const bool len_ok = Kb >= 0 && Kb <= K;
     const bool mode_ok = (mode == 0 || mode == 1) && !(mode == 1 && drf == nullptr) && len_ok;
     const bool sample = CAN_SAMPLE && (!CAN_GREEDY || mode == 1) && mode_ok;
@@ -1233,33 +1316,33 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     if (plain && !prologue_reads) grid_dependency_wait();  // the first input read follows
     // Lane i of every warp holds draft token x_i (first used after the
     // warp's first chunk has arrived, so the load overlaps the copies).
-    const int x_reg = p.tree_parents ? (lane <= K ? __ldg(p.tokens + (size_t)b * (K + 1) + lane) : -1)
-                                     : (mode_ok && lane < Kb) ? __ldg(p.tokens + (size_t)b * K + lane) : -1;
+    const int x_reg = p.tree_parents ? (lane <= K ? ld_in(p, p.tokens + (size_t)b * (K + 1) + lane, -1) : -1)
+                                     : (mode_ok && lane < Kb) ? ld_in(p, p.tokens + (size_t)b * K + lane, -1) : -1;
 
     // ---------------- pass 1: row partials over this CTA's slice ----------------
     // Warp 0 draws the Philox uniforms of positions 0..K while its first
     // copies are in flight; the decision reads them from shared memory.
-    const uint64_t seqid = (sample && warp == 0 && p.seq_ids) ? __ldg(p.seq_ids + b) : (uint64_t)b;
+    const uint64_t seqid = (sample && warp == 0 && p.seq_ids) ? ld_in(p, p.seq_ids + b, (uint64_t)b) : (uint64_t)b;
     auto draw_uniforms = [&] {
         if (warp == 0 && lane <= Kb) position_uniforms(p.seed, seqid, (uint32_t)lane, sh.u_pos[lane], sh.u2_pos[lane]);
     };
     if (mode_ok) {
         if constexpr (!CAN_GREEDY) {
-            stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
+            stream_pass1<TT, TD, true>(p, sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
         } else if constexpr (!CAN_SAMPLE) {
-            stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
+            stream_pass1<TT, TD, false>(p, sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
         } else {
-            if (sample) stream_pass1<TT, TD, true>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
-            else stream_pass1<TT, TD, false>(sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
+            if (sample) stream_pass1<TT, TD, true>(p, sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, draw_uniforms);
+            else stream_pass1<TT, TD, false>(p, sh, wr, ring, total_chunks, c, warp, lane, seq, cluster, CS, Kb, x_reg, [] {});
         }
         if (warp == 0) {
             if constexpr (!CAN_GREEDY) {
-                edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+                edge_pass1<TT, TD, true>(p, sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
             } else if constexpr (!CAN_SAMPLE) {
-                edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+                edge_pass1<TT, TD, false>(p, sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
             } else {
-                if (sample) edge_pass1<TT, TD, true>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
-                else edge_pass1<TT, TD, false>(sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+                if (sample) edge_pass1<TT, TD, true>(p, sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
+                else edge_pass1<TT, TD, false>(p, sh, tgt, drf, b, K, Kb, V, nrows, c, lane, cluster, CS, x_reg);
             }
         }
     }
@@ -1270,14 +1353,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // the draft logits at the draft tokens are inputs: read before the wait
     float ld_early = 0.0f;
     if (fused_d && sample && warp == 1 && lane < Kb && x_reg >= 0 && x_reg < V)
-        ld_early = load_logit<TD>(draft_row(drf, b, K, V, lane), x_reg);
+        ld_early = load_logit<TD>(p, draft_row(drf, b, K, V, lane), x_reg);
     if (fused) grid_dependency_wait();  // the GEMM grid ahead has completed; its stores are visible
     if (fused && mode_ok) {
         // the target logits at the draft tokens: in flight during the merge
         float lt_early = 0.0f;
         if constexpr (sizeof(TT) == 4) {
             if (sample && warp == 0 && lane < Kb && x_reg >= 0 && x_reg < V)
-                lt_early = __ldcg(target_row(tgt, b, K, V, lane) + x_reg);
+                lt_early = ldcg_in(p, target_row(tgt, b, K, V, lane) + x_reg, 0.0f);
         }
         // This CTA's share of every row computed by the GEMM is the merge of
         // its contiguous run of the GEMM CTAs' partials: lanes take every
@@ -1311,8 +1394,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const bool in = t + 32 * u < t1;
-                    v0[u] = in ? __ldcg(c0 + (size_t)(t + 32 * u) * s0) : empty;
-                    v1[u] = in && r1 < n_fused ? __ldcg(c1 + (size_t)(t + 32 * u) * s1) : empty;
+                    v0[u] = in ? ldcg_in(p, c0 + (size_t)(t + 32 * u) * s0, empty) : empty;
+                    v1[u] = in && r1 < n_fused ? ldcg_in(p, c1 + (size_t)(t + 32 * u) * s1, empty) : empty;
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -1438,19 +1521,19 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 if (!invalid) tok = lane < j ? x : (lane == j ? greedy_tok : -1);
                 // in sample mode position j belongs to the CTA that finds the draw
                 if (!(sample && !invalid && lane == j))
-                    p.out_tokens[(size_t)b * (K + 1) + lane] = tok;
+                    st_out(p, p.out_tokens + ((size_t)b * (K + 1) + lane), tok);
             }
-            if (lane == 0) p.out_n_accepted[b] = invalid ? -1 : j;
+            if (lane == 0) st_out(p, p.out_n_accepted + (b), invalid ? -1 : j);
             if (lane < K) {
                 const float qnan = __int_as_float(0x7fc00000);
                 const bool tested = sample && !invalid && lane < Kb;
-                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = tested ? et / St : qnan;
-                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = tested ? ed / Sd : qnan;
+                if (p.out_p_target) st_out(p, p.out_p_target + ((size_t)b * K + lane), tested ? et / St : qnan);
+                if (p.out_p_draft) st_out(p, p.out_p_draft + ((size_t)b * K + lane), tested ? ed / Sd : qnan);
             }
             if (lane == 0 && (!sample || invalid) && p.out_residual_mass)
-                p.out_residual_mass[b] = __int_as_float(0x7fc00000);
+                st_out(p, p.out_residual_mass + (b), __int_as_float(0x7fc00000));
             if (lane < 2 && (!sample || invalid) && p.out_draw_edges)
-                p.out_draw_edges[2 * (size_t)b + lane] = __int_as_float(0x7fc00000);
+                st_out(p, p.out_draw_edges + (2 * (size_t)b + lane), __int_as_float(0x7fc00000));
             if (lane == 0 && p.status_word && invalid)
                 atomicOr(p.status_word, !len_ok        ? (unsigned)SV_FLAG_BAD_LENGTH
                                         : !mode_ok     ? (unsigned)SV_FLAG_BAD_MODE
@@ -1515,7 +1598,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
         if (!sh.err) {
             for (int jj = 0; !resident && jj < NBUF; ++jj) {
                 const int ci = warp + NCW * jj;
-                if (ci < n_chunks) fill_pass2<TT, TD>(sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, span_d, lane);
+                if (ci < n_chunks) fill_pass2<TT, TD>(p, sh, wr, ring, seq + jj, src, sl.ia, sl.ib, ci, ring_d, span_d, lane);
             }
             for (int ci = warp; ci < n_chunks; ci += NCW) {
                 const int q = sl.ia + ci * P2_SLOTS;
@@ -1550,7 +1633,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (ci + NBUF * NCW < n_chunks)
-                        fill_pass2<TT, TD>(sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, span_d,
+                        fill_pass2<TT, TD>(p, sh, wr, ring, seq + NBUF, src, sl.ia, sl.ib, ci + NBUF * NCW, ring_d, span_d,
                                            lane);
                     ++seq;
                 }
@@ -1560,7 +1643,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 for (int kk = 0; kk < STEPS; ++kk) {
                     const int i = kk * 32 + lane;
                     if (w.use_d && !draft_in_ring && !span_d && i < n)
-                        dd[kk] = load_elems_as<TT, TD>(src.drow, V, (q + i) * Elem<TT>::E - src.gt.head);
+                        dd[kk] = load_elems_as<TT, TD>(p, src.drow, V, (q + i) * Elem<TT>::E - src.gt.head);
 #pragma unroll
                     for (int k2 = 0; k2 < Elem<TT>::E / 2; ++k2)
                         acc = add2(acc, draw_mass2(w, slot_pair<TT>(dt[kk], k2), slot_pair<TT>(dd[kk], k2)));
@@ -1579,7 +1662,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             if (sl.edge_lo >= 0 || sl.edge_hi >= 0) {
                 uint4 dt, dd;
                 const int q = lane == 0 ? sl.edge_lo : lane == 1 ? sl.edge_hi : -1;
-                load_draw_slot<TT, TD>(src, w.use_d, q, dt, dd);
+                load_draw_slot<TT, TD>(p, src, w.use_d, q, dt, dd);
                 const float m = slot_mass<TT>(w, dt, dd);
                 e_lo = __shfl_sync(FULL, m, 0);
                 e_hi = __shfl_sync(FULL, m, 1);
@@ -1717,7 +1800,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             const bool tw_inf = isinf(tw.hi);
             DrawStep<TT, TD> st;
             if (warp < STEPS) {
-                st.load(src, w, q0, n, warp, lane);
+                st.load(p, src, w, q0, n, warp, lane);
                 if (lane == 0) {
                     sh.step_tot[warp] = st.tot;
                     sh.step_lp[warp] = st.last_pos;
@@ -1740,20 +1823,20 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                 const int token = st.walk(run, tw, l, d0, d1);
                 if (lane == l) {
                     if (p.overlap_previous) grid_dependency_wait();
-                    p.out_tokens[(size_t)b * (K + 1) + j] = token;
+                    st_out(p, p.out_tokens + ((size_t)b * (K + 1) + j), token);
                     if (p.out_draw_edges) {
-                        p.out_draw_edges[2 * (size_t)b] = d0;
-                        p.out_draw_edges[2 * (size_t)b + 1] = d1;
+                        st_out(p, p.out_draw_edges + (2 * (size_t)b), d0);
+                        st_out(p, p.out_draw_edges + (2 * (size_t)b + 1), d1);
                     }
                 }
             } else if (kstar < 0 && tid == 0) {
                 int lp = -1;  // tw past the part's mass: its last positive element
                 for (int k = 0; k < STEPS; ++k) lp = max(lp, sh.step_lp[k]);
                 if (p.overlap_previous) grid_dependency_wait();
-                p.out_tokens[(size_t)b * (K + 1) + j] = lp;
+                st_out(p, p.out_tokens + ((size_t)b * (K + 1) + j), lp);
                 if (p.out_draw_edges) {
-                    p.out_draw_edges[2 * (size_t)b] = 0.0f;
-                    p.out_draw_edges[2 * (size_t)b + 1] = 0.0f;
+                    st_out(p, p.out_draw_edges + (2 * (size_t)b), 0.0f);
+                    st_out(p, p.out_draw_edges + (2 * (size_t)b + 1), 0.0f);
                 }
             }
         }
@@ -1765,8 +1848,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             grid_dependency_wait();
             // the decision's stores, deferred from the decide step (lanes
             // other than j; position j is the draw's)
-            if (lane <= K && lane != j) p.out_tokens[(size_t)b * (K + 1) + lane] = lane < j ? x_reg : -1;
-            if (lane == 0) p.out_n_accepted[b] = j;
+            if (lane <= K && lane != j) st_out(p, p.out_tokens + ((size_t)b * (K + 1) + lane), lane < j ? x_reg : -1);
+            if (lane == 0) st_out(p, p.out_n_accepted + (b), j);
             if (lane < K && (p.out_p_target || p.out_p_draft)) {
                 const float qnan = __int_as_float(0x7fc00000);
                 float pt = qnan, pd = qnan;
@@ -1776,8 +1859,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
                     pt = ex2(fmaf(sh.lt_x[lane], c, -st.R)) / st.s;
                     pd = ex2(fmaf(sh.ld_x[lane], c, -sd.R)) / sd.s;
                 }
-                if (p.out_p_target) p.out_p_target[(size_t)b * K + lane] = pt;
-                if (p.out_p_draft) p.out_p_draft[(size_t)b * K + lane] = pd;
+                if (p.out_p_target) st_out(p, p.out_p_target + ((size_t)b * K + lane), pt);
+                if (p.out_p_draft) st_out(p, p.out_p_draft + ((size_t)b * K + lane), pd);
             }
             if (lane == 0 && p.status_word && sh.err) atomicOr(p.status_word, (unsigned)SV_FLAG_TIMEOUT);
         }
@@ -1788,15 +1871,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             if (sh.cstar < 0) {
                 // No mass at all (cannot happen for a valid row): report the
                 // sequence as invalid rather than leave a slot unwritten.
-                p.out_tokens[(size_t)b * (K + 1) + j] = -1;
-                p.out_n_accepted[b] = -1;
+                st_out(p, p.out_tokens + ((size_t)b * (K + 1) + j), -1);
+                st_out(p, p.out_n_accepted + (b), -1);
                 if (p.out_draw_edges) {
-                    p.out_draw_edges[2 * (size_t)b] = __int_as_float(0x7fc00000);
-                    p.out_draw_edges[2 * (size_t)b + 1] = __int_as_float(0x7fc00000);
+                    st_out(p, p.out_draw_edges + (2 * (size_t)b), __int_as_float(0x7fc00000));
+                    st_out(p, p.out_draw_edges + (2 * (size_t)b + 1), __int_as_float(0x7fc00000));
                 }
                 if (p.status_word) atomicOr(p.status_word, (unsigned)SV_FLAG_BAD_ROW);
             }
-            if (p.out_residual_mass) p.out_residual_mass[b] = sh.total.hi + sh.total.lo;
+            if (p.out_residual_mass) st_out(p, p.out_residual_mass + (b), sh.total.hi + sh.total.lo);
         }
     }
     wr.drain(sh);

@@ -54,6 +54,21 @@ def test_every_declared_symbol_is_exported(lib):
     assert names <= bound, f"binding misses {sorted(names - bound)}"
 
 
+def test_debug_build_exports_the_same_boundary(lib):
+    # libspecverify_debug.so: the same sources with SPECVERIFY_DEBUG (bounds
+    # checks in the verify kernel); it loads without a GPU like the release
+    # build and exports every declared symbol with the same struct layout
+    dbg = binding.load_library(binding.DEBUG_LIB_PATH)
+    so = ctypes.CDLL(binding.DEBUG_LIB_PATH)
+    for name in sorted(declared_functions()):
+        assert hasattr(so, name), f"{name} declared but not exported by the debug build"
+    assert dbg.sv_verify_args_size() == ctypes.sizeof(binding.sv_verify_args)
+    assert dbg.sv_version() == lib.sv_version()
+    # host validation is the same code in both builds
+    assert dbg.spec_verify_lmhead_workspace_bytes(32, 5, 4096, 128256) == \
+        lib.spec_verify_lmhead_workspace_bytes(32, 5, 4096, 128256)
+
+
 def test_struct_layout_matches(lib):
     assert lib.sv_verify_args_size() == ctypes.sizeof(binding.sv_verify_args)
     assert lib.sv_version() >= 100
