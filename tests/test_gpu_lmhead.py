@@ -294,6 +294,42 @@ def test_verify_lmhead_exact_logits(mode, B, K, d, V, T):
         check(res, 0.0)
 
 
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_verify_lmhead_full_size_exact_logits(mode):
+    # c5's full shape (B=32, K=5, d=4096, V=128256) with hidden and W in
+    # {-1, 0, 1}: every partial sum is an integer of magnitude <= 4096, so the
+    # GEMM is exact and the fused verify must decide exactly as the oracle
+    # does on its own logits (ordinary near-tie bands; greedy ties resolve to
+    # the lowest index on both sides)
+    B, K, d, V, T = 32, 5, 4096, 128256, 8.0
+    g = torch.Generator().manual_seed(55)
+    hidden = torch.randint(-1, 2, (B, K + 1, d), generator=g).to(torch.bfloat16)
+    W = torch.randint(-1, 2, (d, V), generator=g).to(torch.bfloat16)
+    ref_logits = orc.lmhead_logits(bits(hidden.reshape(B * (K + 1), d)), bits(W)).reshape(B, K + 1, V)
+    draft = (torch.from_numpy(ref_logits[:, :K]).float() + torch.randn(B, K, V, generator=g) * 8.0).to(torch.bfloat16)
+    p = torch.softmax(draft.float() / T, dim=-1).reshape(B * K, V)
+    tokens = torch.multinomial(p, 1, generator=g).reshape(B, K).to(torch.int32)
+    if mode == "greedy":
+        top = torch.from_numpy(ref_logits[:, :K].argmax(axis=2)).to(torch.int32)
+        tokens = torch.where(torch.rand(B, K, generator=g) < 0.7, top, tokens)
+    ws = torch.empty(spec_verify_lmhead_workspace_bytes(B, K, d, V), dtype=torch.uint8, device="cuda")
+    out_t, out_n = spec_verify_lmhead(hidden.cuda(), W.cuda(), draft.cuda() if mode == "sample" else None,
+                                      tokens.cuda(), T, mode=mode, seed=21, workspace=ws)
+    torch.cuda.synchronize()
+    gpu_logits = ws[:B * (K + 1) * V * 4].view(torch.float32).reshape(B, K + 1, V).cpu().numpy()
+    assert np.array_equal(gpu_logits.astype(np.float64), ref_logits)
+    ref = orc.verify(ref_logits, bits(draft) if mode == "sample" else None, tokens.numpy(), T,
+                     1 if mode == "sample" else 0, seed=21, threads=16)
+    got_t, got_n = out_t.cpu().numpy(), out_n.cpu().numpy()
+    if mode == "greedy":
+        assert np.array_equal(got_t, ref["tokens"]) and np.array_equal(got_n, ref["n_accepted"])
+    else:
+        res = compare(got_t, got_n, ref)
+        check(res, 0.0)
+        assert res["near_ties"] <= 0.35 * res["sequences"], res
+    assert (ref["n_accepted"] >= 0).all()
+
+
 def misaligned_copy(x, elems):
     """x on the GPU, starting `elems` elements past a 256-byte aligned base
     (the rows keep that misalignment: V is a multiple of 8)."""
