@@ -164,6 +164,20 @@ typedef struct {
                                     the kernel computed them (0, 0 when rounding
                                     left t at or past the total); NaN for greedy
                                     or invalid sequences                          */
+    int seqs_per_cluster;        /* calls without SV_ARG_OVERLAP_PREVIOUS only:
+                                    0 = automatic; 1 = one cluster per sequence;
+                                    2..8 = clusters of cluster_size CTAs (8 when
+                                    cluster_size is 0) that each verify up to
+                                    this many sequences, every CTA streaming its
+                                    slice of V of all of them, so that a large
+                                    batch spreads evenly over the SMs (B <= 256,
+                                    at most 120 rows read per cluster, each of
+                                    its drawing sequences keeping at least
+                                    cluster_size / seqs_per_cluster CTAs;
+                                    otherwise SV_ERR_CONFIG). Automatic groups
+                                    a batch of at least 19 sequences when such a
+                                    plan fills about two CTAs per SM and
+                                    cluster_size is 0                              */
 } sv_verify_args;
 
 /* sv_verify_args.flags: the inputs of this call are not written by the work

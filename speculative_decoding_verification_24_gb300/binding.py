@@ -78,6 +78,7 @@ class sv_verify_args(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("draft_lens", ctypes.c_void_p),
         ("out_draw_edges", ctypes.c_void_p),
+        ("seqs_per_cluster", ctypes.c_int),
     ]
 
 
@@ -208,7 +209,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
                    seed=0, seq_ids=None, out_tokens=None, out_n_accepted=None, out_p_target=None,
                    out_p_draft=None, out_residual_mass=None, status_word=None, cluster_size=0,
                    stream=None, debug=False, overlap_previous=False, draft_lens=None, flags=0,
-                   out_draw_edges=None, lib=None):
+                   out_draw_edges=None, lib=None, seqs_per_cluster=0):
     """Verify with per-sequence modes ([B] int32 tensor, or 'greedy'/'sample'
     for all), explicit Philox sequence ids and optional debug outputs.
     debug=True allocates out_p_target, out_p_draft, out_residual_mass,
@@ -217,6 +218,8 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     draft_lens: optional [B] int32 device tensor of per-sequence draft counts.
     lib: a handle from load_library() to call another build of the library
     (the debug build); the release library by default.
+    seqs_per_cluster: 0 automatic, 1 one cluster per sequence, 2..8 that many
+    sequences per cluster of cluster_size CTAs (calls without overlap).
     Returns a dict of the output tensors."""
     B, K1, V = target_logits.shape
     K = K1 - 1
@@ -261,6 +264,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     a.flags = (SV_ARG_OVERLAP_PREVIOUS if overlap_previous else 0) | int(flags)
     a.draft_lens = _ptr(draft_lens)
     a.out_draw_edges = _ptr(out_draw_edges)
+    a.seqs_per_cluster = int(seqs_per_cluster)
     with torch.cuda.device(dev):
         a.stream = _stream(stream, dev)
         st = (lib or _load()).spec_verify_ex(ctypes.byref(a))

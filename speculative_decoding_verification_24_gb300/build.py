@@ -27,7 +27,7 @@ LIB_DEBUG = os.path.join(PKG, "libspecverify_debug.so")
 # (library, object directory, extra flags)
 VARIANTS = [(LIB, BUILD_DIR, []), (LIB_DEBUG, os.path.join(BUILD_DIR, "debug"), ["-DSPECVERIFY_DEBUG"])]
 
-SOURCES = ["verify_logits.cu", "lmhead.cu", "prompt_lookup.cu", "api.cu"]
+SOURCES = ["verify_logits.cu", "verify_grouped.cu", "lmhead.cu", "prompt_lookup.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -118,6 +118,24 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     if (a->cluster_size && usable != cs) return SV_ERR_CONFIG;
     cs = usable;
 
+    // Several sequences per cluster (plain calls): asked for, or automatic
+    // when it spreads a large batch evenly over the SMs.
+    const bool plain = !target_parts && !(a->flags & SV_ARG_OVERLAP_PREVIOUS);
+    if (a->seqs_per_cluster < 0 || a->seqs_per_cluster > 8 || (a->seqs_per_cluster > 1 && !plain))
+        return SV_ERR_CONFIG;
+    int n_cl = 0, gcs = 0;
+    bool grouped = false;
+    if (plain && a->seqs_per_cluster > 1) {
+        gcs = a->cluster_size ? a->cluster_size : 8;
+        n_cl = (a->B + a->seqs_per_cluster - 1) / a->seqs_per_cluster;
+        if (!sv::group_plan_fits(a->B, a->K, may_sample, a->V, (int)es_t, n_cl, gcs)) return SV_ERR_CONFIG;
+        if (sv::usable_cluster_size((int)dtype_t, (int)dtype_d, gcs) != gcs) return SV_ERR_CONFIG;
+        grouped = true;
+    } else if (plain && a->seqs_per_cluster == 0 && a->cluster_size == 0) {
+        grouped = sv::auto_group_plan(a->B, a->K, may_sample, a->V, (int)es_t, sms, n_cl, gcs) &&
+                  sv::usable_cluster_size((int)dtype_t, (int)dtype_d, gcs) == gcs;
+    }
+
     sv::VerifyParams p = {};
     p.target = a->target_logits;
     p.draft = a->draft_logits;
@@ -147,7 +165,8 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
     p.part_tiles = part_tiles;
     p.part_M = a->B * (a->K + 1);
     p.draft_parts = draft_parts;
-    cudaError_t e = sv::launch_verify_logits(p, (int)dtype_t, (int)dtype_d, cs, (cudaStream_t)a->stream);
+    cudaError_t e = grouped ? sv::launch_verify_grouped(p, (int)dtype_t, (int)dtype_d, n_cl, gcs, (cudaStream_t)a->stream)
+                            : sv::launch_verify_logits(p, (int)dtype_t, (int)dtype_d, cs, (cudaStream_t)a->stream);
     if (e != cudaSuccess) return fail_cuda(e);
     return SV_OK;
 }
@@ -201,7 +220,7 @@ extern "C" const char* sv_status_string(sv_status s) {
 
 extern "C" int sv_last_cuda_error(void) { return g_last_cuda_error; }
 
-extern "C" int sv_version(void) { return 101; }
+extern "C" int sv_version(void) { return 102; }
 
 extern "C" size_t sv_verify_args_size(void) { return sizeof(sv_verify_args); }
 

@@ -70,6 +70,16 @@ int usable_cluster_size(int dtype_target, int dtype_draft, int cs);
 cudaError_t launch_verify_logits(const VerifyParams& p, int dtype_target, int dtype_draft, int cs,
                                  cudaStream_t stream);
 
+// Grouped verify (plain calls): n_cl clusters of cs CTAs, cluster c taking
+// the sequences the batch's snake order deals it. group_plan_fits: whether
+// the kernel's tables hold such a plan for these sizes (can_sample: the call
+// may have sample sequences); auto_group_plan: the plan a lone call uses by
+// default, or false for one cluster per sequence.
+bool group_plan_fits(int B, int K, bool can_sample, int V, int esize, int n_cl, int cs);
+bool auto_group_plan(int B, int K, bool can_sample, int V, int esize, int num_sms, int& n_cl, int& cs);
+cudaError_t launch_verify_grouped(const VerifyParams& p, int dtype_target, int dtype_draft, int n_cl, int cs,
+                                  cudaStream_t stream);
+
 // LM head: logits[M, V] (fp32) = hidden[M, d] . W[d, V] (bf16) on the tensor
 // cores; 1 <= M <= 256, d a multiple of 64, V a multiple of 8, 16-byte
 // aligned bases.

@@ -68,15 +68,17 @@ def _built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-def run_pair(case, seed, seq_ids=None, cluster_size=0, modes=None):
+def run_pair(case, seed, seq_ids=None, cluster_size=0, modes=None, draft_lens=None, **kw):
     modes = case.modes if modes is None else modes
     out = spec_verify_ex(case.target, case.draft, case.tokens, case.temperature, modes=modes,
-                         seed=seed, seq_ids=seq_ids, cluster_size=cluster_size, debug=True)
+                         seed=seed, seq_ids=seq_ids, cluster_size=cluster_size, debug=True,
+                         draft_lens=None if draft_lens is None else draft_lens.to(case.target.device), **kw)
     torch.cuda.synchronize()
     ids = None if seq_ids is None else seq_ids.cpu().numpy()
     ref = orc.verify(to_numpy_logits(case.target), to_numpy_logits(case.draft),
                      case.tokens.cpu().numpy(), case.temperature, modes.cpu().numpy(), seed=seed,
-                     seq_ids=ids, threads=THREADS)
+                     seq_ids=ids, threads=THREADS,
+                     draft_lens=None if draft_lens is None else draft_lens.cpu().numpy())
     g = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in out.items()}
     return g, ref
 
@@ -159,6 +161,8 @@ def test_c3_half_greedy_half_sample():
 
 
 def test_c4_full_size():
+    """A lone c4 call as the library launches it by default (several
+    sequences per cluster)."""
     dev = torch.device("cuda")
     case = synth.make_workload("c4", seed=4, device=dev)
     tally = Tally("c4")
@@ -169,6 +173,17 @@ def test_c4_full_size():
         # accepted lengths vary within the batch (tau per sequence)
         assert len(set(g["n_accepted"].tolist())) > 3, res
     tally.check(0.02)  # 512 sequences
+
+
+@pytest.mark.parametrize("name", ["c3", "c4"])
+def test_full_size_one_cluster_per_sequence(name):
+    """The same batches with one cluster per sequence (the kernel a lone
+    call used before batches were grouped, and still uses for small ones)."""
+    dev = torch.device("cuda")
+    case = synth.make_workload(name, seed=int(name[1]), device=dev)
+    g, ref = run_pair(case, seed=7, seqs_per_cluster=1)
+    res = check(g, ref, f"{name} one cluster per sequence")
+    assert (g["n_accepted"] >= 0).all(), res
 
 
 @pytest.mark.parametrize("name,seeds", [("c2", (5, 6, 7)), ("c3", (3, 4)), ("c4", (4,))])
