@@ -2,12 +2,12 @@
 
 A plain call over a large batch runs clusters that each verify several
 sequences, every CTA of a cluster streaming its slice of V of all of them
-(seqs_per_cluster; the library picks such a plan by default for c3 and c4).
+(seqs_per_cluster; the library picks such a plan by default for c3).
 These cases force the plan over shapes that reach its corners: clusters with
 unequal sequence counts, mixed modes and per-sequence draft counts (so the
 in-kernel ordering by rows read matters), odd and unaligned rows (partial
 edge slots), 31 rows per sequence, B = 256, many clusters, every cluster
-size, invalid inputs and the slow paths of the reductions.
+size, invalid inputs, the timeout path and the slow paths of the reductions.
 """
 import numpy as np
 import pytest
