@@ -582,7 +582,14 @@ struct DrawStep {
         const int q = i < n ? q_begin + i : -1;
         uint4 dt, dd;
         load_draw_slot<TT, TD>(p, src, w.use_d, q, dt, dd);
-        i0 = q * E - src.gt.head;
+        take(w, dt, dd, q, src.gt.head, lane);
+    }
+
+    // The same from slots already at hand: target slot q (q < 0: none) and
+    // the draft elements with the same indices, in the target's slot format.
+    __device__ __forceinline__ void take(const DrawRows& w, const uint4& dt, const uint4& dd, int q, int head,
+                                         int lane) {
+        i0 = q * E - head;
         float ls = 0.0f;
         int lp = -1;
 #pragma unroll

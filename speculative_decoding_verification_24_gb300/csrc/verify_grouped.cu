@@ -68,6 +68,7 @@ struct GroupShared {
     unsigned char row_flags[GROWS];       // ROW_DRAFT, ROW_SOFT
     GSeq seqs[GMAX];
     float p2_part[MAX_P2_CHUNKS];
+    unsigned char p2_stage[MAX_P2_CHUNKS];  // the ring stage each pass-2 chunk landed in
     float p2_edge[2];
     float2 gathered_tot[2][G_MAX_CS];     // every CTA's draw mass (float-float), by cluster rank
     int G, nrows, total_chunks, err, overflow;
@@ -683,10 +684,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_grouped_kernel(VerifyParam
     constexpr int STEPS = P2_SLOTS / 32;
     fence_proxy_async_smem();  // the ring, last written through generic stores, takes bulk copies again
     __syncthreads();
-    bool fell_back = false;
+    bool fell_back = false;  // this group's residual summed to zero: it draws again from P_t
     for (int attempt = 0;; ++attempt) {
-        const bool active = attempt == 0 || sh.retry_mine;
-        w.use_d = me.use_d && attempt == 0;
+        // a group that does not go again keeps its first attempt (its parts,
+        // its stages and its draw rows) for the search
+        const bool active = attempt == 0 || fell_back;
+        if (active) w.use_d = me.use_d && attempt == 0;
         const bool ring_d = w.use_d && draft_in_ring;
         const bool span_d = SPAN_TYPES && w.use_d;
         if (active && !sh.err) {
@@ -703,6 +706,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_grouped_kernel(VerifyParam
                     break;
                 }
                 const char* stage = wr.stage(ring, seq);
+                if (lane == 0) sh.p2_stage[ci] = (unsigned char)(warp + NCW * (int)(seq % NBUF));
 #pragma unroll
                 for (int kk = 0; kk < STEPS; ++kk) {
                     const int i = kk * 32 + lane;
@@ -804,7 +808,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_grouped_kernel(VerifyParam
         if (!sh.any_retry) break;
         // Some group's residual summed to zero in float: that group falls
         // back to P_t of row j (reported at the end); the others keep theirs.
-        fell_back = fell_back || sh.retry_mine;
+        fell_back = sh.retry_mine != 0;
     }
 
     if (sub_rank == sh.cstar) {  // the CTA holding the draw (uniform over the CTA)
@@ -880,9 +884,27 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_grouped_kernel(VerifyParam
             }
             const ff tw = sh.tw;
             const bool tw_inf = isinf(tw.hi);
+            // When no stage was refilled during pass 2 (at most NSTAGE
+            // chunks), the part's chunk is still in its stage: the search
+            // takes it from there instead of reading the row again.
+            const bool in_ring = n_chunks <= NSTAGE && found > 0 && found < P - 1 && !sh.err;
             DrawStep<TT, TD> st;
             if (warp < STEPS) {
-                st.load(p, src, w, q0, n, warp, lane);
+                if (in_ring) {
+                    const char* stage = ring + (size_t)sh.p2_stage[found - 1] * STAGE_BYTES;
+                    const int i = warp * 32 + lane;
+                    const int q = i < n ? q0 + i : -1;
+                    uint4 dt = neg_inf_slot<TT>(), dd = neg_inf_slot<TT>();
+                    if (i < n) {
+                        dt = lds128(stage + i * 16);
+                        if (w.use_d && draft_in_ring) dd = lds128(stage + P2_DRAFT_OFF + i * 16);
+                        else if (SPAN_TYPES && w.use_d) dd = span_slot(stage + P2_DRAFT_OFF, span_off, i);
+                        else if (w.use_d) dd = load_elems_as<TT, TD>(p, src.drow, V, q * Elem<TT>::E - src.gt.head);
+                    }
+                    st.take(w, dt, dd, q, src.gt.head, lane);
+                } else {
+                    st.load(p, src, w, q0, n, warp, lane);
+                }
                 if (lane == 0) {
                     sh.step_tot[warp] = st.tot;
                     sh.step_lp[warp] = st.last_pos;
@@ -969,7 +991,7 @@ static cudaError_t launch_grouped_ms(const VerifyParams& p, int n_cl, int cs, cu
         if (dev >= 0 && dev < 64) g_grouped_attr[dev][ci][MS - 1].store(1, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3((unsigned)(n_cl * cs), 1, 1);
     cfg.blockDim = dim3(NTHREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)RING_BYTES;
@@ -978,8 +1000,13 @@ static cudaError_t launch_grouped_ms(const VerifyParams& p, int n_cl, int cs, cu
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // The call may launch before the work ahead of it on the stream has
+    // completed; the kernel reads no input before that work has (measured on
+    // GB300, B=64 half-greedy calls one after another: 30.7 -> 30.5 us).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, verify_grouped_kernel<TT, TD, MS>, p);
 }
 

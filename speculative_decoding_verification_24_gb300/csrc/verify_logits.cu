@@ -55,6 +55,7 @@ struct SeqShared {
     float2 merged[MAX_ROWS];
     float p2_part[MAX_P2_CHUNKS];
     float p2_edge[2];
+    unsigned char p2_seq0[NCW];         // each warp's fill count mod NBUF when pass 2 began
     float lt_x[MAX_K], ld_x[MAX_K];     // the logits at the draft tokens (captured in pass 1)
     float2 gathered_tot[2][MAX_CS];     // every CTA's draw mass (float-float), pushed by their owners
     float u_pos[MAX_K + 1], u2_pos[MAX_K + 1];  // Philox uniforms of positions 0..K
@@ -722,11 +723,14 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     const bool resident_d = resident_t && draft_in_ring && rd.ia == sl.ia && rd.ib == sl.ib;
     int attempt = 0;
     bool fell_back = false;
+    bool last_resident = false;  // the last attempt read row j from pass 1's stages
     for (;; ++attempt) {
         w.use_d = sh.use_d && attempt == 0;
         const bool ring_d = w.use_d && draft_in_ring;
         const bool span_d = SPAN_TYPES && w.use_d;
         const bool resident = resident_t && (!ring_d || resident_d) && !span_d;
+        last_resident = resident;
+        if (lane == 0) sh.p2_seq0[warp] = (unsigned char)(seq % NBUF);
         if (!sh.err) {
             for (int jj = 0; !resident && jj < NBUF; ++jj) {
                 const int ci = warp + NCW * jj;
@@ -930,9 +934,36 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
             }
             const ff tw = sh.tw;
             const bool tw_inf = isinf(tw.hi);
+            // The part's chunk may still be in shared memory: in pass 1's
+            // stages (row j read back from them), or in the stage pass 2 copied
+            // it to when no stage was refilled (at most NSTAGE chunks).
+            const bool interior = found > 0 && found < P - 1 && !sh.err;
+            const char* at_t = nullptr;
+            const char* at_d = nullptr;
+            if (interior && last_resident) {
+                at_t = ring + (size_t)(rt_c0 * STAGE_SLOTS + (found - 1) * P2_SLOTS) * 16;
+                at_d = ring + (size_t)(rd_c0 * STAGE_SLOTS + (found - 1) * P2_SLOTS) * 16;
+            } else if (interior && n_chunks <= NSTAGE) {
+                const int ci = found - 1, wc = ci % NCW;
+                at_t = ring + (size_t)(wc + NCW * ((sh.p2_seq0[wc] + ci / NCW) % NBUF)) * STAGE_BYTES;
+                at_d = at_t + P2_DRAFT_OFF;
+            }
             DrawStep<TT, TD> st;
             if (warp < STEPS) {
-                st.load(p, src, w, q0, n, warp, lane);
+                if (at_t) {
+                    const int i = warp * 32 + lane;
+                    const int q = i < n ? q0 + i : -1;
+                    uint4 dt = neg_inf_slot<TT>(), dd = neg_inf_slot<TT>();
+                    if (i < n) {
+                        dt = lds128(at_t + i * 16);
+                        if (w.use_d && draft_in_ring) dd = lds128(at_d + i * 16);
+                        else if (SPAN_TYPES && w.use_d && !last_resident) dd = span_slot(at_d, span_off, i);
+                        else if (w.use_d) dd = load_elems_as<TT, TD>(p, src.drow, V, q * Elem<TT>::E - src.gt.head);
+                    }
+                    st.take(w, dt, dd, q, src.gt.head, lane);
+                } else {
+                    st.load(p, src, w, q0, n, warp, lane);
+                }
                 if (lane == 0) {
                     sh.step_tot[warp] = st.tot;
                     sh.step_lp[warp] = st.last_pos;
