@@ -50,10 +50,11 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
-# Sources of the kernels the traffic record covers (the verify kernel, the
+# Sources of the kernels the traffic record covers (the verify kernels, the
 # LM-head GEMM and the launch decisions made for them); the drafting and
 # commit kernels of the decode loop are not in it.
-TRAFFIC_SOURCES = ("api.cu", "lmhead.cu", "sv_device.cuh", "sv_launch.h", "verify_logits.cu")
+TRAFFIC_SOURCES = ("api.cu", "lmhead.cu", "sv_device.cuh", "sv_launch.h", "verify_common.cuh", "verify_logits.cu",
+                   "verify_grouped.cu")
 
 
 def kernel_source_hash() -> str:
@@ -1084,7 +1085,9 @@ def profile_run(args, device):
     """--profile NAME: warmup + steps eager calls of one workload and no bench
     line, for ncu (every launch of the verify kernel, launched as the bench
     times it, with SV_ARG_OVERLAP_PREVIOUS and so the same cluster size; or
-    for c5 the LM-head GEMM then the verify kernel; inputs larger than L2)."""
+    for c5 the LM-head GEMM then the verify kernel; inputs larger than L2).
+    NAME-alone: the same calls without the flag, as the bench's one-call-at-a-
+    time block launches them (c3: the grouped kernel)."""
     from speculative_decoding_verification_24_gb300 import (spec_verify_ex, spec_verify_lmhead,
                                                             spec_verify_lmhead_workspace_bytes)
     from speculative_decoding_verification_24_gb300.build import build
@@ -1102,11 +1105,12 @@ def profile_run(args, device):
     else:
         props = torch.cuda.get_device_properties(device)
         l2 = int(getattr(props, "L2_cache_size", 0) or 129 * 2**20)
-        sets, _ = workload_sets(args.profile, device, l2)
+        name = args.profile.replace("-alone", "")
+        sets, _ = workload_sets(name, device, l2)
         for i in range(n):
             c = sets[i % len(sets)]
             spec_verify_ex(c.target, c.draft, c.tokens, c.temperature, modes=uniform_mode(c.modes),
-                           seed=i, overlap_previous=True)
+                           seed=i, overlap_previous=not args.profile.endswith("-alone"))
     torch.cuda.synchronize()
     print(f"profile run: {args.profile}, {n} steps", flush=True)
 
@@ -1126,7 +1130,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5"],
+    ap.add_argument("--profile", choices=["c1", "c2", "c3", "c4", "c5", "c2-alone", "c3-alone", "c4-alone"],
                     help="run warmup+steps calls of one workload for ncu; no bench line")
     args = ap.parse_args()
     args.also = [a for a in args.also.split(",") if a]

@@ -65,6 +65,18 @@ def test_debug_build_on_unaligned_rows_and_ragged_lengths(dbg):
     assert_same(*both(case, dbg, draft_lens=lens))
 
 
+@pytest.mark.parametrize("B,K,V,dtype,modes,cs,spc", [(40, 4, 3001, "bf16", "half", 8, 4),
+                                                        (37, 3, 2000, "f32", "sample", 4, 3),
+                                                        (64, 4, 20000, "bf16", "half", 8, 2)])
+def test_debug_build_grouped_kernel(dbg, B, K, V, dtype, modes, cs, spc):
+    # several sequences per cluster (the plan a lone call over a large batch
+    # gets), with per-sequence draft counts: every access checked, none outside
+    case = synth.make_logits_case(B=B, K=K, V=V, dtype=dtype, modes=modes, seed=B + V, device="cuda")
+    lens = torch.tensor([(3 * b) % (K + 1) for b in range(B)], dtype=torch.int32, device="cuda")
+    assert_same(*both(case, dbg, cluster_size=cs, seqs_per_cluster=spc))
+    assert_same(*both(case, dbg, seed=4, cluster_size=cs, seqs_per_cluster=spc, draft_lens=lens))
+
+
 def test_debug_build_tree_verification(dbg):
     t, x, par = synth.make_tree_case(4, 8, 3000, "bf16", seed=9, device="cuda")
     rel = spec_verify_tree(t, x, par)
