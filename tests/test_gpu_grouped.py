@@ -169,3 +169,20 @@ def test_grouped_plans_the_kernel_cannot_hold_are_refused():
         spec_verify_ex(small.target, small.draft, small.tokens, 1.0, modes="sample", seed=0,
                        cluster_size=2, seqs_per_cluster=4)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name,explicit", [("c3", {"cluster_size": 8, "seqs_per_cluster": 2}),
+                                           ("c4", {"seqs_per_cluster": 1})])
+def test_the_automatic_plan(name, explicit):
+    """The plan a plain call gets by default: c3 (B=64, half greedy) runs 32
+    clusters of 8 CTAs with two sequences each; c4 (B=256), for which no
+    grouped plan fits the GPU in one wave, one cluster per sequence. The
+    default call equals, bit for bit, the call that asks for that plan."""
+    case = synth.make_workload(name, seed=31, device="cuda")
+    a = spec_verify_ex(case.target, case.draft, case.tokens, case.temperature, modes=case.modes, seed=2,
+                       debug=True)
+    b = spec_verify_ex(case.target, case.draft, case.tokens, case.temperature, modes=case.modes, seed=2,
+                       debug=True, **explicit)
+    torch.cuda.synchronize()
+    for k in ("tokens", "n_accepted", "p_target", "p_draft", "residual_mass", "draw_edges", "status_word"):
+        torch.testing.assert_close(a[k], b[k], rtol=0, atol=0, equal_nan=True, msg=k)
