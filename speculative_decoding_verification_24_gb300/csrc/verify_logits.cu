@@ -13,15 +13,17 @@
 //   pass 1  Each of the CS CTAs of a cluster owns a contiguous slice of V and
 //           streams that slice of every row the sequence needs (K+1 target
 //           rows; plus K draft rows in sample mode). The slices' 16-byte
-//           slots form one schedule cut into 4 KB chunks (a chunk may hold
-//           pieces of several short rows). Each of the 8 warps owns two
-//           shared-memory stages and streams every 8th chunk itself: bulk
-//           copies (cp.async.bulk, no multicast) complete on the stage's
-//           mbarrier; the warp copies the chunk into registers, refills the
-//           stage with its chunk 16 ahead, then reduces: (R, s) base-2
-//           softmax partials with packed fp32x2 arithmetic for sample rows,
-//           (max, lowest index) for greedy rows. Partial 16-byte slots at a
-//           row's two ends use plain loads.
+//           slots form one schedule cut into 4 KB chunks, row after row (a
+//           row's last chunk may be shorter). Each of the 8 warps owns three
+//           shared-memory stages and streams its own chunks: every 8th one,
+//           or a contiguous run when the slices are short (see
+//           stream_pass1). Bulk copies (cp.async.bulk, evict-first in L2, no
+//           multicast) complete on the stage's mbarrier; the warp copies the
+//           chunk into registers, refills the stage with its chunk three
+//           ahead, then reduces: (R, s) base-2 softmax partials with packed
+//           fp32x2 arithmetic for sample rows, (max, lowest index) for
+//           greedy rows. Partial 16-byte slots at a row's two ends use plain
+//           loads.
 //   decide  Every CTA pushes its per-row partials into every CTA of the
 //           cluster (distributed shared memory); after one cluster barrier
 //           each CTA merges them in rank order (so all hold bit-identical
