@@ -382,6 +382,17 @@ HOW_SERIAL = ("one call at a time, as a decode loop whose next verify depends on
               "each call starts after the previous one has completed")
 
 
+def launch_plans(sets):
+    """The launches of the overlapped and the one-call-at-a-time runs, as the
+    library reports them (spec_verify_plan; nothing is enqueued)."""
+    from speculative_decoding_verification_24_gb300 import spec_verify_plan
+
+    c = sets[0]
+    return {how: spec_verify_plan(c.target, c.draft, c.tokens, c.temperature, modes=uniform_mode(c.modes), seed=0,
+                                  overlap_previous=(how == "overlapped"))
+            for how in ("overlapped", "serial")}
+
+
 def logits_timing(sets, steps, warmup, stream, device, world, rank, label):
     """Both timings of a logits workload over the same steps and seeds:
     overlapped (independent batches back to back) and serial (one call at a
@@ -420,6 +431,7 @@ def run_ours(args, rank, world, device):
     rows_per_step = B * K1
     stream = torch.cuda.Stream(device)
     t = logits_timing(sets, args.steps, args.warmup, stream, device, world, rank, args.workload)
+    plans = launch_plans(sets)
     graph = t["graph"]
 
     sampler = ClockSampler(device.index if device.index is not None else 0)
@@ -507,7 +519,9 @@ def run_ours(args, rank, world, device):
                    "frac_of_measured_peak": serial["gbs"] / world / peak,
                    "frac_of_nominal_8tbs": serial["gbs"] / world / NOMINAL_HBM_GBS,
                    "sequences_differing_from_overlapped": t["serial_differing"],
+                   "plan": plans["serial"],
                    "how": HOW_SERIAL},
+        "plan": plans["overlapped"],
         "eager_rows_per_s": world * rows_per_step * args.steps / (eager_ms / 1e3),
     }
     result["acceptance"] = acceptance(args.workload, n_all, args.warmup, args.steps, len(sets), K1 - 1)
@@ -751,7 +765,9 @@ def other_workloads(args, device, l2, stream):
                                     "frac_of_measured_peak": ba / (serial_ms / 1e3) / 1e9 / peak,
                                     "frac_of_nominal_8tbs": ba / (serial_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                                     "sequences_differing_from_overlapped": t["serial_differing"],
+                                    "plan": launch_plans(sets)["serial"],
                                     "how": HOW_SERIAL},
+                         "plan": launch_plans(sets)["overlapped"],
                          "acceptance": acceptance(name, n_all, args.warmup, steps, len(sets), K1 - 1),
                          "input_sets": len(sets)}
             if not args.no_cpu_baseline:

@@ -207,6 +207,21 @@ typedef struct {
  * probability outputs. Same conventions and errors as spec_verify. */
 sv_status spec_verify_ex(const sv_verify_args* args);
 
+/* The launch spec_verify_ex would make for these arguments. */
+typedef struct {
+    int grouped;              /* 1: several sequences per cluster (each CTA
+                                 streams its slice of V of all of them);
+                                 0: one cluster per sequence               */
+    int clusters;             /* clusters in the grid                       */
+    int cluster_size;         /* CTAs per cluster                           */
+    int max_seqs_per_cluster; /* 1 unless grouped                           */
+} sv_verify_plan;
+
+/* Validates args exactly as spec_verify_ex does (same status on error) and
+ * fills *plan with the launch it would make; reads no device memory and
+ * enqueues nothing (it queries the current device's properties). */
+sv_status spec_verify_plan(const sv_verify_args* args, sv_verify_plan* plan);
+
 /* Bytes of device workspace spec_verify_lmhead needs for these sizes:
  * the fp32 logits B*(K+1)*V*4, then 8 bytes per target row and 128-column
  * tile of V (ceil(V/128)*B*(K+1)*8), then 8 bytes per draft row and tile

@@ -82,6 +82,16 @@ class sv_verify_args(ctypes.Structure):
     ]
 
 
+class sv_verify_plan(ctypes.Structure):
+    """Mirror of sv_verify_plan in include/specverify.h."""
+    _fields_ = [
+        ("grouped", ctypes.c_int),
+        ("clusters", ctypes.c_int),
+        ("cluster_size", ctypes.c_int),
+        ("max_seqs_per_cluster", ctypes.c_int),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -91,6 +101,7 @@ I = ctypes.c_int
 SIGNATURES = [
     ("spec_verify", I, [P, P, P, I, I, I, I, ctypes.c_float, I, ctypes.c_uint64, P, P, P]),
     ("spec_verify_ex", I, [ctypes.POINTER(sv_verify_args)]),
+    ("spec_verify_plan", I, [ctypes.POINTER(sv_verify_args), ctypes.POINTER(sv_verify_plan)]),
     ("spec_verify_lmhead_workspace_bytes", ctypes.c_size_t, [I, I, I, I]),
     ("spec_verify_lmhead", I, [P, P, P, P, I, I, I, I, I, ctypes.c_float, I, ctypes.c_uint64, P,
                                ctypes.c_size_t, P, P, P]),
@@ -209,7 +220,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
                    seed=0, seq_ids=None, out_tokens=None, out_n_accepted=None, out_p_target=None,
                    out_p_draft=None, out_residual_mass=None, status_word=None, cluster_size=0,
                    stream=None, debug=False, overlap_previous=False, draft_lens=None, flags=0,
-                   out_draw_edges=None, lib=None, seqs_per_cluster=0):
+                   out_draw_edges=None, lib=None, seqs_per_cluster=0, plan_only=False):
     """Verify with per-sequence modes ([B] int32 tensor, or 'greedy'/'sample'
     for all), explicit Philox sequence ids and optional debug outputs.
     debug=True allocates out_p_target, out_p_draft, out_residual_mass,
@@ -220,6 +231,9 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     (the debug build); the release library by default.
     seqs_per_cluster: 0 automatic, 1 one cluster per sequence, 2..8 that many
     sequences per cluster of cluster_size CTAs (calls without overlap).
+    plan_only=True: enqueue nothing and return the launch the call would make
+    (spec_verify_plan): {"grouped", "clusters", "cluster_size",
+    "max_seqs_per_cluster"}.
     Returns a dict of the output tensors."""
     B, K1, V = target_logits.shape
     K = K1 - 1
@@ -267,11 +281,23 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature=1.0, m
     a.seqs_per_cluster = int(seqs_per_cluster)
     with torch.cuda.device(dev):
         a.stream = _stream(stream, dev)
+        if plan_only:
+            plan = sv_verify_plan()
+            st = (lib or _load()).spec_verify_plan(ctypes.byref(a), ctypes.byref(plan))
+            _check(st, "spec_verify_plan")
+            return {"grouped": bool(plan.grouped), "clusters": plan.clusters, "cluster_size": plan.cluster_size,
+                    "max_seqs_per_cluster": plan.max_seqs_per_cluster}
         st = (lib or _load()).spec_verify_ex(ctypes.byref(a))
     _check(st, "spec_verify_ex")
     return {"tokens": out_tokens, "n_accepted": out_n_accepted, "p_target": out_p_target,
             "p_draft": out_p_draft, "residual_mass": out_residual_mass,
             "draw_edges": out_draw_edges, "status_word": status_word}
+
+
+def spec_verify_plan(target_logits, draft_logits, draft_tokens, temperature=1.0, **kw):
+    """The launch spec_verify_ex would make for these arguments (nothing is
+    enqueued): {"grouped", "clusters", "cluster_size", "max_seqs_per_cluster"}."""
+    return spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature, plan_only=True, **kw)
 
 
 def spec_verify_tree(target_logits, tree_tokens, tree_parents, out_tokens=None, out_n_accepted=None,

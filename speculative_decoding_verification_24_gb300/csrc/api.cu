@@ -60,9 +60,11 @@ bool valid_cluster_request(int cs) { return cs == 0 || cs == 1 || cs == 2 || cs 
 // dtype_t and the draft rows type dtype_d (equal, or fp32 target with bf16
 // draft rows for the LM-head path).
 // target_parts: the LM-head path's per-tile target-row partials (or NULL).
+// plan_only: validate and choose the launch as a call would, report it there
+// and enqueue nothing.
 static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype dtype_d,
                              const float2* target_parts = nullptr, int part_tiles = 0,
-                             const float2* draft_parts = nullptr) {
+                             const float2* draft_parts = nullptr, sv_verify_plan* plan_only = nullptr) {
     if (!a) return SV_ERR_NULL;
     if (!a->target_logits || !a->draft_tokens || !a->out_tokens || !a->out_n_accepted)
         return SV_ERR_NULL;
@@ -136,6 +138,14 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
                   sv::usable_cluster_size((int)dtype_t, (int)dtype_d, gcs) == gcs;
     }
 
+    if (plan_only) {
+        plan_only->grouped = grouped ? 1 : 0;
+        plan_only->clusters = grouped ? n_cl : a->B;
+        plan_only->cluster_size = grouped ? gcs : cs;
+        plan_only->max_seqs_per_cluster = grouped ? (a->B + n_cl - 1) / n_cl : 1;
+        return SV_OK;
+    }
+
     sv::VerifyParams p = {};
     p.target = a->target_logits;
     p.draft = a->draft_logits;
@@ -174,6 +184,11 @@ static sv_status verify_impl(const sv_verify_args* a, sv_dtype dtype_t, sv_dtype
 extern "C" sv_status spec_verify_ex(const sv_verify_args* a) {
     if (!a) return SV_ERR_NULL;
     return verify_impl(a, a->dtype, a->dtype);
+}
+
+extern "C" sv_status spec_verify_plan(const sv_verify_args* a, sv_verify_plan* plan) {
+    if (!a || !plan) return SV_ERR_NULL;
+    return verify_impl(a, a->dtype, a->dtype, nullptr, 0, nullptr, plan);
 }
 
 extern "C" sv_status spec_verify(const void* target_logits, const void* draft_logits,

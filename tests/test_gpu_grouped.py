@@ -186,3 +186,22 @@ def test_the_automatic_plan(name, explicit):
     torch.cuda.synchronize()
     for k in ("tokens", "n_accepted", "p_target", "p_draft", "residual_mass", "draw_edges", "status_word"):
         torch.testing.assert_close(a[k], b[k], rtol=0, atol=0, equal_nan=True, msg=k)
+
+
+@pytest.mark.parametrize("name,overlap,want", [
+    ("c3", False, {"grouped": True, "clusters": 32, "cluster_size": 8, "max_seqs_per_cluster": 2}),
+    ("c4", False, {"grouped": False, "clusters": 256, "cluster_size": 1, "max_seqs_per_cluster": 1}),
+    ("c2", False, {"grouped": False, "clusters": 8, "cluster_size": 16, "max_seqs_per_cluster": 1}),
+    ("c3", True, {"grouped": False, "clusters": 64, "cluster_size": 1, "max_seqs_per_cluster": 1}),
+])
+def test_spec_verify_plan_reports_the_launch(name, overlap, want):
+    """spec_verify_plan reports the launch a call makes (nothing enqueued):
+    the grouped plan for c3 alone, one cluster per sequence otherwise."""
+    from speculative_decoding_verification_24_gb300 import spec_verify_plan
+    case = synth.make_workload(name, seed=32, device="cuda", **({"tau": 1.0} if name == "c2" else {}))
+    got = spec_verify_plan(case.target, case.draft, case.tokens, case.temperature, modes=case.modes, seed=0,
+                           overlap_previous=overlap)
+    assert got == want, (name, overlap, got)
+    with pytest.raises(SpecVerifyError):  # refused exactly as the call would be
+        spec_verify_plan(case.target, case.draft, case.tokens, case.temperature, modes=case.modes, seed=0,
+                         seqs_per_cluster=9)
