@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import synth
+from speculative_decoding_verification_24_gb300 import spec_verify_ex
 from test_gpu_parity import Tally, check, run_pair
 
 pytestmark = pytest.mark.gpu
@@ -70,3 +71,24 @@ def test_random_shape(i, tally):
     g, ref = run_pair(case, seed=c["seed"] % 1000, draft_lens=c["lens"], **c["kw"])
     tally.add(check(g, ref, label, max_tie_fraction=1.0))
     assert int(g["status_word"][0]) == 0, label
+
+
+@pytest.mark.parametrize("i", range(2000, 2024))
+def test_repeated_calls_agree_bit_for_bit(i):
+    """The same call three times gives the same bits in every output (the
+    kernels' merge orders are fixed; a race would show here), and reports
+    nothing."""
+    c = draw_case(i)
+    case = synth.make_logits_case(B=c["B"], K=c["K"], V=c["V"], dtype=c["dtype"], modes=c["modes"], T=c["T"],
+                                  seed=c["seed"], device="cuda")
+    lens = None if c["lens"] is None else c["lens"].cuda()
+    outs = []
+    for _ in range(3):
+        o = spec_verify_ex(case.target, case.draft, case.tokens, case.temperature, modes=case.modes.cuda(),
+                           seed=c["seed"] % 1000, debug=True, draft_lens=lens, **c["kw"])
+        outs.append({k: v.clone() for k, v in o.items() if isinstance(v, torch.Tensor)})
+    torch.cuda.synchronize()
+    assert int(outs[0]["status_word"][0]) == 0
+    for o in outs[1:]:
+        for k, v in o.items():
+            torch.testing.assert_close(v, outs[0][k], rtol=0, atol=0, equal_nan=True, msg=f"case {i} {k}")
