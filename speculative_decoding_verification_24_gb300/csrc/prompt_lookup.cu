@@ -106,10 +106,17 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_kernel(const int32_t
         const int t0 = p0 + ti * PL_TILE, buf = ti & 1;
         if (ti + 1 < n_tiles) load(t0 + PL_TILE, p1);  // in flight during the scan below
         const int32_t* tl = tile[buf] + PL_HALO - t0;  // tl[i] = token i for t0 - PL_HALO <= i < t0 + PL_TILE
+        // this thread's positions of the tile read at once, then compared
+        int32_t v[PL_PER];
 #pragma unroll
         for (int k = 0; k < PL_PER; ++k) {
             const int e = t0 + k * PL_THREADS + tid;
-            if (e < p1 && tl[e] == s0) {
+            v[k] = e < p1 ? tl[e] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < PL_PER; ++k) {
+            const int e = t0 + k * PL_THREADS + tid;
+            if (e < p1 && v[k] == s0) {
                 int ml = 1;
                 while (ml < max_ngram && e - ml >= 0 && tl[e - ml] == suffix[ml]) ++ml;
                 const long long key = ((long long)ml << 32) | (unsigned)e;
@@ -191,6 +198,7 @@ constexpr int PLW_TILE = 4096;     // tokens per bulk copy (16 KB)
 constexpr int PLW_MAX_TILES = 6;
 constexpr int PLW_MAX_L = PLW_TILE * PLW_MAX_TILES;  // 24576 tokens, 96 KB of shared memory
 constexpr uint32_t PLW_WAIT_LIMIT = 1u << 22;        // polls before a copy's wait gives up
+constexpr int PLW_SPREAD_BYTES = 80 * 1024;        // more than a third of an SM's shared memory
 
 __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_whole_kernel(const int32_t* tokens, const int32_t* lengths,
                                                                          int L_max, int max_ngram, int n_drafts,
@@ -244,10 +252,23 @@ __global__ void __launch_bounds__(PL_THREADS) prompt_lookup_whole_kernel(const i
             atomicExch(&s_err, 1);
             break;
         }
+        // This thread's positions of the tile are read first, all at once (one
+        // shared-memory latency per tile rather than one per position), then
+        // compared. Measured on GB300, 256 contexts of up to 16384 tokens,
+        // calls back to back: 6.4 us per call reading and comparing one
+        // position at a time, 5.1 us reading them at once, 4.9 us with at most
+        // two CTAs per SM (see the launch).
+        constexpr int PER_T = PLW_TILE / PL_THREADS;
+        int32_t v[PER_T];
 #pragma unroll
-        for (int k = 0; k < PLW_TILE / PL_THREADS; ++k) {
+        for (int k = 0; k < PER_T; ++k) {
             const int e = t * PLW_TILE + k * PL_THREADS + tid;
-            if (e < n_pos && ctx[e] == s0) {
+            v[k] = e < n_pos ? ctx[e] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < PER_T; ++k) {
+            const int e = t * PLW_TILE + k * PL_THREADS + tid;
+            if (e < n_pos && v[k] == s0) {
                 int ml = 1;
                 while (ml < max_ngram && e - ml >= 0 && ctx[e - ml] == suffix[ml]) ++ml;
                 const long long key = ((long long)ml << 32) | (unsigned)e;
@@ -328,7 +349,10 @@ cudaError_t launch_prompt_lookup(const int32_t* tokens, const int32_t* lengths, 
         cudaLaunchAttribute attr[1];
         cfg.gridDim = dim3((unsigned)B, 1, 1);
         cfg.blockDim = dim3(PL_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = (size_t)L_max * 4;
+        // At least PLW_SPREAD_BYTES, so that no SM holds more than two CTAs:
+        // with three on some SMs and one on others, the SMs with three set the
+        // call's time.
+        cfg.dynamicSmemBytes = (size_t)(L_max * 4 > PLW_SPREAD_BYTES ? L_max * 4 : PLW_SPREAD_BYTES);
         cfg.stream = stream;
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
