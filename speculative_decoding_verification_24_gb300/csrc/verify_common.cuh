@@ -293,9 +293,10 @@ __device__ __forceinline__ float warp_incl_scan(float x, int lane) {
 struct SoftAcc {
     float R;
     f32x2 a0, a1, a2, a3;  // eight running sums as four packed pairs
+    bool ready;            // R is one finite value in every lane of the warp (set by the exact path)
 };
 
-__device__ __forceinline__ SoftAcc soft_acc_empty() { return SoftAcc{-INFINITY, 0ull, 0ull, 0ull, 0ull}; }
+__device__ __forceinline__ SoftAcc soft_acc_empty() { return SoftAcc{-INFINITY, 0ull, 0ull, 0ull, 0ull, false}; }
 
 __device__ __forceinline__ float soft_acc_sum(const SoftAcc& a) {
     const f32x2 t = add2(add2(a.a0, a.a1), add2(a.a2, a.a3));
@@ -735,7 +736,7 @@ constexpr float FAST_SUM_LIMIT = 4096.0f;
 template <typename T>
 __device__ __forceinline__ bool soft_chunk_fast(SoftAcc& sa, const uint4 (&d)[CHUNK_LANE_SLOTS], float c) {
     constexpr int PAIRS = Elem<T>::E / 2;
-    if (__any_sync(FULL, !(sa.R > -INFINITY && sa.R < INFINITY))) return false;
+    if (!sa.ready) return false;
     const f32x2 c2 = pack2(c, c), nR2 = pack2(-sa.R, -sa.R);
     f32x2 b0 = 0ull, b1 = 0ull, b2 = 0ull, b3 = 0ull;
 #pragma unroll
@@ -795,12 +796,20 @@ __device__ __forceinline__ void reduce_chunk(SoftAcc& sa, ArgAcc& aa, const uint
         sa.a2 = mul2(sa.a2, sc2);
         sa.a3 = mul2(sa.a3, sc2);
         sa.R = Rw;
+        sa.ready = Rw > -INFINITY && Rw < INFINITY;
     }
 }
 
 // The row of pass-1 chunk `chunk` for a warp that visits chunks in order.
 struct RowCursor {
     int r, c0, c1;
+};
+
+// The refill cursor, with its row's geometry in registers (looked up once a row).
+struct FillCursor {
+    RowCursor rc;
+    const uint4* base;
+    int ia, ib;
 };
 
 __device__ __forceinline__ void seek_row(RowCursor& rc, const RowInfo* rows, int chunk) {
@@ -815,16 +824,21 @@ __device__ __forceinline__ void seek_row(RowCursor& rc, const RowInfo* rows, int
 // `fseq` of the warp; lane 0 issues.
 template <class SH>
 __device__ __forceinline__ void fill_pass1(const VerifyParams& p, SH& sh, WarpRing& wr, char* ring,
-                                           uint32_t fseq, int chunk, RowCursor& rc, int lane) {
-    seek_row(rc, sh.rows, chunk);
-    const RowInfo& ri = sh.rows[rc.r];
-    const int q0 = ri.ia + (chunk - rc.c0) * STAGE_SLOTS;
-    const int n = min(STAGE_SLOTS, ri.ib - q0);
+                                           uint32_t fseq, int chunk, FillCursor& fc, int lane) {
+    if (chunk >= fc.rc.c1) {
+        seek_row(fc.rc, sh.rows, chunk);
+        const RowInfo& ri = sh.rows[fc.rc.r];
+        fc.base = ri.base;
+        fc.ia = ri.ia;
+        fc.ib = ri.ib;
+    }
+    const int q0 = fc.ia + (chunk - fc.rc.c0) * STAGE_SLOTS;
+    const int n = min(STAGE_SLOTS, fc.ib - q0);
     // (a debug build that finds the copy out of bounds completes the stage empty)
-    const bool ok = lane != 0 || load_ok(p, ri.base + q0, (size_t)n * 16u);
+    const bool ok = lane != 0 || load_ok(p, fc.base + q0, (size_t)n * 16u);
     wr.begin_fill(sh, fseq, ok ? (uint32_t)n * 16u : 0u, lane);
     if (lane == 0 && ok)
-        bulk_g2s_hint(wr.stage(ring, fseq), ri.base + q0, (uint32_t)n * 16u, wr.bar(sh, fseq), l2_evict_first_policy());
+        bulk_g2s_hint(wr.stage(ring, fseq), fc.base + q0, (uint32_t)n * 16u, wr.bar(sh, fseq), l2_evict_first_policy());
 }
 
 // The 16-byte aligned span of a bf16 draft row that holds the elements of

@@ -162,7 +162,7 @@ __device__ __forceinline__ WarpChunks warp_chunks(int total_chunks, int warp) {
 // The first NBUF fills of a warp's chunks.
 __device__ __forceinline__ void first_fills(const VerifyParams& p, GroupShared& sh, WarpRing& wr, char* ring,
                                             const WarpChunks& wc, uint32_t seq, int lane) {
-    RowCursor frc{-1, 0, 0};
+    FillCursor frc{{-1, 0, 0}, nullptr, 0, 0};
     for (int k = 0; k < NBUF; ++k) {
         const int chunk = wc.first + k * wc.step;
         if (chunk < wc.end) fill_pass1(p, sh, wr, ring, seq + k, chunk, frc, lane);
@@ -178,6 +178,7 @@ __device__ __forceinline__ void group_pass1(const VerifyParams& p, GroupShared& 
     constexpr bool CAN_SAMPLE = (MS & MS_SAMPLE) != 0, CAN_GREEDY = (MS & MS_GREEDY) != 0;
     constexpr bool SAME = std::is_same<TT, TD>::value;
     RowCursor rc{-1, 0, 0};
+    FillCursor frc{{-1, 0, 0}, nullptr, 0, 0};  // the refills' chunks only increase
     int cur_row = -1, ia = 0, ib = 0, head = 0;
     bool soft = !CAN_GREEDY, draft = false;
     TokenSpotG ts{-1, 0};
@@ -235,10 +236,8 @@ __device__ __forceinline__ void group_pass1(const VerifyParams& p, GroupShared& 
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (chunk + NBUF * wc.step < wc.end) {
-            RowCursor frc = rc;  // the refill's row lies at or after this one
+        if (chunk + NBUF * wc.step < wc.end)
             fill_pass1(p, sh, wr, ring, seq + NBUF, chunk + NBUF * wc.step, frc, lane);
-        }
         if (CAN_SAMPLE && soft) {
             if (SAME || !draft) reduce_chunk<TT, true>(sa, aa, d, n, q0, c, lane);
             else reduce_chunk<TD, true>(sa, aa, d, n, q0, c, lane);

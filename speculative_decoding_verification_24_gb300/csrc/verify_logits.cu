@@ -230,7 +230,8 @@ __device__ __forceinline__ void stream_pass1(const VerifyParams& p, SeqShared& s
         split_range(nchunks, warp, NCW, first, end);
         step = 1;
     }
-    RowCursor fill_rc{-1, 0, 0}, rc{-1, 0, 0};
+    FillCursor fill_rc{{-1, 0, 0}, nullptr, 0, 0};
+    RowCursor rc{-1, 0, 0};
     for (int j = 0; j < NBUF; ++j) {
         const int chunk = first + step * j;
         if (chunk < end) fill_pass1(p, sh, wr, ring, seq + j, chunk, fill_rc, lane);
