@@ -69,6 +69,16 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 __device__ __forceinline__ bool is_nan(float x) { return x != x; }
 
+// Every CTA of a cluster must have started before any of them accesses
+// another's shared memory. A kernel announces its start as its first
+// instruction (every thread, no ordering) and waits for the whole cluster's
+// announcements just before its first remote access; both run exactly once
+// per thread, so the barrier phase always completes, and by then it has.
+__device__ __forceinline__ void cluster_arrive_started() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_started() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // Programmatic dependent launch: wait until the grids this one depends on
 // have completed and their memory is visible (returns at once when the
 // launch had no such dependency); let the next grid on the stream launch.

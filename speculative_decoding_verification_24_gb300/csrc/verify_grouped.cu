@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_grouped_kernel(VerifyParam
     extern __shared__ __align__(128) char ring[];
     __shared__ GroupShared sh;
     launch_dependents();
+    cluster_arrive_started();
     cg::cluster_group cluster = cg::this_cluster();
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -486,6 +487,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_grouped_kernel(VerifyParam
             position_uniforms(p.seed, seqid, (uint32_t)lane, sh.u_pos[s.row0 + lane], sh.u2_pos[s.row0 + lane]);
         }
     }
+    cluster_wait_started();  // pass 1 writes the captured logits into every CTA of the cluster
     group_pass1<TT, TD, MS>(p, sh, wr, ring, wc, c, warp, lane, seq, cluster, CS, tok);
     // the partial slots at the slices' ends (rows not 16-byte aligned)
     for (int r = warp; r < nrows; r += NCW) {

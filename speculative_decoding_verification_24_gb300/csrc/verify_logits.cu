@@ -356,6 +356,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // thing, so that consecutive calls launch at the hardware's pace rather
     // than one prologue apart.
     launch_dependents();
+    cluster_arrive_started();
     cg::cluster_group cluster = cg::this_cluster();
     const int CS = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -472,6 +473,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) verify_logits_kernel(VerifyParams
     // warp's first chunk has arrived, so the load overlaps the copies).
     const int x_reg = p.tree_parents ? (lane <= K ? ld_in(p, p.tokens + (size_t)b * (K + 1) + lane, -1) : -1)
                                      : (mode_ok && lane < Kb) ? ld_in(p, p.tokens + (size_t)b * K + lane, -1) : -1;
+
+    // Pass 1 writes the captured logits into every CTA of the cluster.
+    cluster_wait_started();
 
     // ---------------- pass 1: row partials over this CTA's slice ----------------
     // Warp 0 draws the Philox uniforms of positions 0..K while its first
