@@ -10,6 +10,8 @@ mode (integer logits tie often; the lowest index must win on both sides),
 exactly outside the ordinary near-tie bands in sample mode. A second group
 repeats calls and requires the same bits each time.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -21,7 +23,8 @@ from test_gpu_lmhead import bits, check, check_parts
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 16
+# SV_SOAK_CASES raises the count (a longer soak of the same seeded cases)
+N_CASES = int(os.environ.get("SV_SOAK_CASES", "16"))
 
 
 def draw_case(i):

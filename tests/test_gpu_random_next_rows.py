@@ -8,6 +8,8 @@ time; they reach both prompt-lookup kernels (the whole-context one for
 L_max <= 24576, a multiple of 4, on a 16-byte aligned buffer; the cluster
 one otherwise).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -20,6 +22,9 @@ from test_gpu_prompt_lookup import contexts
 from test_gpu_tree import random_trees
 
 pytestmark = pytest.mark.gpu
+
+# SV_SOAK_CASES raises the count (a longer soak of the same seeded cases)
+N_CASES = int(os.environ.get("SV_SOAK_CASES", "12"))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,7 +43,7 @@ def draw_tree_case(i):
     return B, N, V, dtype, p_follow, int(rng.integers(0, 1 << 20))
 
 
-@pytest.mark.parametrize("i", range(12))
+@pytest.mark.parametrize("i", range(N_CASES))
 def test_random_tree_matches_oracle(i):
     B, N, V, dtype, p_follow, seed = draw_tree_case(i)
     target, tokens, parents = random_trees(B, N, V, seed=seed, dtype=dtype, p_follow=p_follow)
@@ -65,7 +70,7 @@ def draw_lookup_case(i):
     return B, L_max, vocab, m, k, copy_prob, unaligned, int(rng.integers(0, 1 << 20))
 
 
-@pytest.mark.parametrize("i", range(12))
+@pytest.mark.parametrize("i", range(N_CASES))
 def test_random_prompt_lookup_matches_oracle(i):
     B, L_max, vocab, m, k, copy_prob, unaligned, seed = draw_lookup_case(i)
     tok, lens = contexts(B, L_max, vocab, seed=seed, copy_prob=copy_prob)

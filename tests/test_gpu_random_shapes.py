@@ -8,6 +8,8 @@ every time. Every case is compared with the oracle as the other parity tests
 do (exact outside the near-tie bands); the near-ties of all cases together are
 capped.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,8 @@ from test_gpu_parity import Tally, check, run_pair
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 32
+# SV_SOAK_CASES raises the count (a longer soak of the same seeded cases)
+N_CASES = int(os.environ.get("SV_SOAK_CASES", "32"))
 
 
 def draw_case(i):
