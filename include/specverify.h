@@ -247,11 +247,13 @@ size_t spec_verify_lmhead_workspace_bytes(int B, int K, int d, int V);
  *   hidden and W 16-byte aligned. Greedy mode ignores draft_dtype.
  *   workspace: device buffer of at least
  *   spec_verify_lmhead_workspace_bytes(B, K, d, V) bytes, 256-byte aligned;
- *   it receives the fp32 target logits [B*(K+1), V], then the target rows'
- *   partials (one per row and GEMM CTA, room for ceil(V/128) CTAs) and
- *   (sample mode) the draft rows', 8 bytes each (every byte the call reads
- *   there it wrote first, so no initial contents are needed); it may be
- *   reused once the call's work on `stream` has completed.
+ *   its first part holds the fp32 target logits [B*(K+1), V] (sample mode
+ *   only: a greedy call decides from the partials and leaves that part as
+ *   it was), then the target rows' partials (one per row and GEMM CTA, room
+ *   for ceil(V/128) CTAs) and (sample mode) the draft rows', 8 bytes each
+ *   (every byte the call reads there it wrote first, so no initial contents
+ *   are needed); it may be reused once the call's work on `stream` has
+ *   completed. The size does not depend on the mode.
  * Other arguments as in spec_verify. */
 sv_status spec_verify_lmhead(const void* hidden, const void* W,
                              const void* draft_logits,

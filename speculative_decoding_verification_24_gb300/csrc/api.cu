@@ -402,7 +402,11 @@ extern "C" sv_status spec_verify_lmhead(const void* hidden, const void* W, const
     sv::LmDraftParts dp{draft_logits, B * K, draft_dtype == SV_F32 ? 1 : 0, dparts};
     const bool sample = mode == SV_SAMPLE;
     int gemm_ctas = 0;
-    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, (int)M, d, V, static_cast<float*>(workspace), parts, c,
+    // Greedy decisions and the token after them come from the (max, lowest
+    // index) partials alone; only a sample call's final draw reads logits
+    // (row j's), so a greedy call stores none of them.
+    cudaError_t e = sv::launch_lmhead_gemm(hidden, W, (int)M, d, V, sample ? static_cast<float*>(workspace) : nullptr,
+                                           parts, c,
                                            sample ? 1 : 0, sample ? &dp : nullptr, nullptr, (cudaStream_t)stream,
                                            &gemm_ctas);
     if (e != cudaSuccess) return fail_cuda(e);

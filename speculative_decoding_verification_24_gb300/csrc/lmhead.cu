@@ -82,7 +82,7 @@ struct LmParams {
     int M, d, V, N;     // N: M rounded up to 16
     int stages;         // ring stages (<= LM_MAX_STAGES)
     int tiles;          // ceil(V / LM_BLOCK_V)
-    float* out;         // [M, V]
+    float* out;         // [M, V], or nullptr (partials only: no logit is stored)
     uint32_t* status;   // optional
     float2* parts;      // [grid, M] each CTA's row partials over its tiles, or nullptr (logits only)
     float c;            // log2(e) / temperature (soft partials)
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(LM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const int m = c0 + c;
-                    if (m < p.M && v < p.V) p.out[(size_t)m * p.V + v] = __uint_as_float(r[c]);
+                    if (p.out && m < p.M && v < p.V) p.out[(size_t)m * p.V + v] = __uint_as_float(r[c]);
                 }
                 if (p.parts) {
                     // turn the 32 x 32 block over: lane l then holds row c0 + l

@@ -190,9 +190,14 @@ def run_lmhead_case(case, seed, mode):
                                       case.temperature, mode=mode, seed=seed, workspace=ws)
     logits = spec_lmhead_logits(hidden, W)
     torch.cuda.synchronize()
-    # the fused call's logits are the standalone GEMM's, bit for bit
-    ws_logits = ws[:B * K1 * V * 4].view(torch.float32).reshape(B * K1, V)
-    assert torch.equal(ws_logits, logits)
+    if mode == "sample":
+        # the fused call's logits are the standalone GEMM's, bit for bit
+        ws_logits = ws[:B * K1 * V * 4].view(torch.float32).reshape(B * K1, V)
+        assert torch.equal(ws_logits, logits)
+    else:
+        # a greedy call stores no logits (it decides from the partials): the
+        # standalone GEMM's are the same bits (the sample cases check that)
+        ws_logits = logits
     # the epilogue's per-tile partials are the reductions of those logits
     check_parts(ws, logits.cpu().numpy().astype(np.float64), V, mode, case.temperature)
     ref_logits = orc.lmhead_logits(bits(case.hidden.reshape(B * K1, d)), bits(case.W))
@@ -316,7 +321,10 @@ def test_verify_lmhead_full_size_exact_logits(mode):
     out_t, out_n = spec_verify_lmhead(hidden.cuda(), W.cuda(), draft.cuda() if mode == "sample" else None,
                                       tokens.cuda(), T, mode=mode, seed=21, workspace=ws)
     torch.cuda.synchronize()
-    gpu_logits = ws[:B * (K + 1) * V * 4].view(torch.float32).reshape(B, K + 1, V).cpu().numpy()
+    if mode == "sample":
+        gpu_logits = ws[:B * (K + 1) * V * 4].view(torch.float32).reshape(B, K + 1, V).cpu().numpy()
+    else:  # a greedy call stores no logits; the GEMM alone computes the same
+        gpu_logits = spec_lmhead_logits(hidden.reshape(B * (K + 1), d).cuda(), W.cuda()).cpu().numpy().reshape(B, K + 1, V)
     assert np.array_equal(gpu_logits.astype(np.float64), ref_logits)
     ref = orc.verify(ref_logits, bits(draft) if mode == "sample" else None, tokens.numpy(), T,
                      1 if mode == "sample" else 0, seed=21, threads=16)
